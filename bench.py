@@ -1,0 +1,346 @@
+"""Benchmark: batch-1 decode tokens/s of the Qwen3-0.6B-shape decoder on one GB300.
+
+Workload (default "qwen3_0p6b_decode"): full Qwen3-0.6B shape, random-init bf16
+weights from the seeded generator, a 128-token uniform-random prompt prefilled, then
+greedy decode.  One timed step = one decode token (one pass of the whole decode hot
+path: embedding gather, 28 layers, final norm, tied lm_head, argmax).  Inputs are
+resident in HBM before the timed region; the 1.19 GB of weights streamed per token
+are larger than L2, so no flush is needed between steps.
+
+Output: one JSON line (rank 0).  `--impl reference` times the CPU oracle instead
+(the reference arm: the plain fp32 restatement of the same forward on host cores).
+Multi-GPU runs (torchrun) are independent replicas, one sequence per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import qw_inputs as qi  # noqa: E402
+
+METRIC = "batch-1 decode tokens/s (Qwen3-0.6B shape); achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 7900.0
+
+
+# ------------------------------------------------------------------ byte model
+
+def weight_bytes(wl) -> int:
+    """Bytes of weights one decode token reads once (incl. the tied head and one embedding row)."""
+    H, d, Hq, Hkv, I, V = wl.hidden, wl.head_dim, wl.n_heads, wl.n_kv_heads, wl.intermediate, wl.vocab
+    mats = [Hq * d * H, 2 * Hkv * d * H, H * Hq * d, 3 * I * H]  # q, k+v, o, gate+up+down
+    n = sum(mats)
+    if wl.weight_format == "int8_g32":
+        per_layer = n + 2 * (n // 32)  # int8 codes + fp16 scales
+    else:
+        per_layer = 2 * n
+    per_layer += 2 * (2 * H + 2 * d)  # norms
+    return wl.n_layers * per_layer + 2 * V * H + 2 * H + 2 * H  # + lm_head + final norm + embedding row
+
+
+def kv_bytes_per_pos(wl) -> int:
+    esz = 4 if wl.kv_format == "f32" else 2
+    return wl.n_layers * wl.n_kv_heads * wl.head_dim * 2 * esz  # K and V rows of one position
+
+
+def token_bytes(wl, pos: int) -> int:
+    """Algorithmic HBM bytes of the decode step at position pos: weights once, the pos cached
+    K/V rows read, this position's K/V written, f32 logits written."""
+    return weight_bytes(wl) + kv_bytes_per_pos(wl) * (pos + 1) + 4 * wl.vocab
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic():
+    """Per-launch DRAM bytes from the committed ncu capture, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "runtime_qwen3_decode_gb300", "csrc", "decode.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if d.get("decode_cu_sha256_16") != sha:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_decode_rate(wl, host, n_ctx: int, n_steps: int, warmup: int = 1):
+    """Time the CPU oracle's decode steps after importing an n_ctx-position synthetic cache."""
+    import oracle
+
+    ref = oracle.OracleModel(wl, host, max_ctx=n_ctx + warmup + n_steps + 1)
+    k, v = qi.kv_fill(wl, n_ctx)
+    ref.kv_import(k, v, n_ctx)
+    del k, v
+    tok = qi.first_decode_token(wl)
+    for _ in range(warmup):
+        lg, _ = ref.step(tok)
+        tok = oracle.argmax(lg)
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        lg, _ = ref.step(tok)
+        tok = oracle.argmax(lg)
+    dt = time.perf_counter() - t0
+    cores = int(ref.cfg.nthreads)
+    ref.close()
+    return n_steps / dt, dt, cores
+
+
+# -------------------------------------------------------------------- arms
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    host = qi.make_weights(wl)
+    steps = args.steps
+    rate, dt, cores = oracle_decode_rate(wl, host, wl.prompt_len, steps, warmup=max(1, min(args.warmup, 2)))
+    sample = (f"{steps} oracle decode steps at positions {wl.prompt_len}.. after importing a "
+              f"{wl.prompt_len}-position synthetic bf16 K/V cache; full Qwen3-0.6B shape")
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "prompt": wl.prompt_len, "decode_steps": wl.decode_steps},
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import torch
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from runtime_qwen3_decode_gb300 import build as qbuild
+    from runtime_qwen3_decode_gb300 import qw
+
+    qbuild.build()
+    host = qi.make_weights(wl)
+    dev = qw.weights_to_device(host, int8=wl.weight_format == "int8_g32")
+    prompt = qi.prompt(wl)
+    W, K = args.warmup, args.steps
+    per_seq = wl.decode_steps
+    max_ctx = wl.prompt_len + max(per_seq, min(W + K, per_seq)) + 1
+    model = qw.Model(wl, dev, max_ctx=max_ctx)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # prefill of the workload's prompt (timed on its own, reported beside the headline)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    model.prefill(prompt, want_token=False)  # warm
+    model.kv_reset()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    model.prefill(prompt, want_token=False)
+    ev1.record(stream)
+    model.sync()
+    prefill_ms = ev0.elapsed_time(ev1)
+
+    # decode: W warm-up tokens, then exactly K timed tokens; a new sequence starts (reset +
+    # prefill, inside the timed region) whenever the workload's decode budget is used up
+    toks = torch.zeros(max(K, 1), dtype=torch.int32, device="cuda")
+    positions = []
+    done_in_seq = 0
+
+    def run_tokens(n, out=None, record=False):
+        nonlocal done_in_seq
+        i = 0
+        while i < n:
+            if done_in_seq == per_seq:
+                model.kv_reset()
+                model.prefill(prompt, want_token=False)
+                done_in_seq = 0
+            m = min(n - i, per_seq - done_in_seq)
+            if record:
+                positions.extend(range(model.kv_length, model.kv_length + m))
+            model.generate(m, -1, out[i:i + m] if out is not None else None)
+            done_in_seq += m
+            i += m
+
+    run_tokens(W)
+    model.sync()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    run_tokens(K, toks, record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    model.sync()
+    ms = t0.elapsed_time(t1)
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = K * ws / (ms / 1000.0)
+
+    # end to end through the public call: host token in, host token out, every step
+    model.kv_reset()
+    tok = model.prefill(prompt)
+    n_e2e = min(K, per_seq)
+    torch.cuda.synchronize()
+    t_e = time.perf_counter()
+    for _ in range(n_e2e):
+        tok = model.decode_step(tok)
+    e2e_s = time.perf_counter() - t_e
+    e2e_val = n_e2e / e2e_s
+
+    if rank != 0:
+        model.close()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    bytes_timed = sum(token_bytes(wl, p) for p in positions)
+    achieved = bytes_timed / (ms / 1000.0) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.weight_format == "bf16" else "int8",
+        "data": "synthetic (seeded random-init weights, uniform-random prompt)",
+        "config": {"workload": wl.name, "prompt": wl.prompt_len, "decode_steps": per_seq,
+                   "positions_timed": [positions[0], positions[-1]] if positions else None,
+                   "compute": "bf16 weights x f32 activations, f32 accumulation",
+                   "l2": "no flush: inputs larger than L2 (weights streamed per token)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "frac_of_nominal_7.9TBs": achieved / NOMINAL_HBM_GBS,
+                     "bytes_per_token_at_first_pos": token_bytes(wl, positions[0]) if positions else None,
+                     "kernel": "qw::decode_kernel (one persistent launch per token)",
+                     "traffic": kernel_traffic()},
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 16,
+                "how": "qw_decode_step(token_from_host, &next_token_host) per token, host-synchronous"},
+        "gpu_launches": K,
+        "clocks": clk,
+        "prefill": {"tokens": wl.prompt_len, "ms": prefill_ms, "tokens_per_s": wl.prompt_len / (prefill_ms / 1e3)},
+    }
+    model.close()
+    if not args.no_cpu_baseline and ws == 1:
+        n = args.cpu_steps
+        rate, dt, cores = oracle_decode_rate(wl, host, wl.prompt_len, n)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} oracle decode steps after a {wl.prompt_len}-position synthetic "
+                                          f"K/V import, full shape ({dt:.1f} s of CPU)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=376)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_0p6b_decode", choices=sorted(qi.WORKLOADS))
+    ap.add_argument("--cpu-steps", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = qi.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

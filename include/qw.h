@@ -1,0 +1,236 @@
+/*
+ * qw.h - C ABI of the GB300 batch-one Qwen3 decoder (libqw.so).
+ *
+ * What the library computes: the Qwen3 decoder forward for one sequence,
+ * as laid out in "Scalar-Native Qwen3 Reference Runtime As The Numerical
+ * Authority", section 2 "Decoder-Layer Mathematical Formulation" steps 1-7:
+ * embedding gather, then per layer RMSNorm, bias-free Q/K/V projections,
+ * per-head QK-Norm, RoPE, grouped-query causal attention over a K/V cache,
+ * o_proj with residual, RMSNorm and the SwiGLU MLP with residual; then the
+ * final RMSNorm, the tied lm_head and a greedy argmax (ties to the lowest
+ * token id, "Portable WebAssembly Runtime Architecture for TinyRustLM",
+ * section "Deterministic sampling contract", sampling order step 6).
+ *
+ * Interface conventions follow "Portable WebAssembly Runtime Architecture
+ * for TinyRustLM", section "Typed host/Wasm API": extern "C", fixed-width
+ * integers, an opaque handle checked on every call, status codes instead
+ * of exceptions, and borrowed pointers.  Status values reuse that page's
+ * TrResult numbering.
+ *
+ * Ownership.  The caller owns every device buffer: the weights (borrowed
+ * for the model's lifetime, never copied or written) and the workspace
+ * (sized by qw_workspace_bytes, carved by the library into the K/V cache,
+ * activation buffers and bookkeeping).  The library allocates no device
+ * memory.  The qw_model handle itself is host memory owned by the library
+ * until qw_model_destroy.
+ *
+ * Streams and synchronisation.  Every call enqueues work on the stream given
+ * at creation and returns without waiting, except where it writes a host
+ * pointer (next_token_host), which waits for that stream.  Errors raised on
+ * the device (non-finite logits, a bounded wait that expired) are recorded
+ * in the workspace and reported by the next call that waits on the stream.
+ *
+ * Device: one GB300 (sm_103a).  There is no CPU fallback: if the device
+ * code cannot run, calls fail with QW_CUDA_ERROR.
+ */
+#ifndef QW_H
+#define QW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QW_ABI_VERSION 1
+
+typedef struct qw_model qw_model;
+
+/* Status codes (values from the TrResult table of the typed host API). */
+enum qw_status {
+    QW_OK = 0,
+    QW_INVALID_ARGUMENT = 1,          /* NULL pointer, negative count, token id out of range */
+    QW_INVALID_HANDLE = 4,            /* handle not created by qw_model_create, or destroyed */
+    QW_ALIGNMENT = 7,                 /* a weight or workspace pointer is not 16/256-byte aligned */
+    QW_INTEGER_OVERFLOW = 8,          /* a size computed from the config overflows */
+    QW_OUT_OF_MEMORY = 9,             /* workspace smaller than qw_workspace_bytes */
+    QW_UNSUPPORTED_QUANTIZATION = 12, /* weight format unknown, or a dimension not a multiple of 32 */
+    QW_UNSUPPORTED_SHAPE = 13,        /* dims outside what the kernels are built for (see qw_config) */
+    QW_CONTEXT_EXCEEDED = 14,         /* the step would pass max_ctx; the cache is left unchanged */
+    QW_NUMERICAL_FAILURE = 18,        /* non-finite logits were produced */
+    QW_INTERNAL_INVARIANT = 20,       /* a device-side bounded wait expired; the model must be reset */
+    QW_CUDA_ERROR = 21                /* a CUDA runtime call failed (no device, launch failure ...) */
+};
+
+/* Weight storage of the seven projection matrices (q, k, v, o, gate, up, down). */
+enum qw_weight_format {
+    QW_W_BF16 = 0,      /* bf16 [out, in] row-major */
+    QW_W_INT8_G32 = 1   /* int8 codes [out, in] + fp16 scales [out, in/32]; w = f32(q) * f32(s)
+                           ("Scalar-Native ...", section 3 "Mixed-Q8 Quantization Definition") */
+};
+
+/*
+ * Element type of the K/V cache.  The reference keeps K and V in f32
+ * ("Scalar-Native ...", section 6 "Extents and Bytes Formulas"); bf16 halves the
+ * cache and its per-token read traffic at the cost of rounding every stored
+ * row (about 3e-3 relative L2 on the residual stream after a few hundred
+ * freshly computed positions).
+ */
+enum qw_kv_format {
+    QW_KV_F32 = 0,
+    QW_KV_BF16 = 1
+};
+
+/*
+ * Model dimensions.  Supported by the kernels: head_dim == 128;
+ * n_heads % n_kv_heads == 0 with group size n_heads/n_kv_heads in {1, 2};
+ * hidden, n_heads*head_dim and intermediate each a multiple of 1024 and at
+ * most 3072; vocab >= 1; 1 <= n_layers <= 64; 1 <= max_ctx <= 131072.
+ * Anything else returns QW_UNSUPPORTED_SHAPE.  rms_eps is the RMSNorm epsilon
+ * (1e-6 for Qwen3), rope_theta the RoPE base (1e6 for Qwen3).
+ */
+typedef struct {
+    int32_t n_layers;
+    int32_t hidden;
+    int32_t n_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t intermediate;
+    int32_t vocab;
+    float rms_eps;
+    double rope_theta;
+    int32_t max_ctx;
+    int32_t weight_format; /* enum qw_weight_format */
+    int32_t kv_format;     /* enum qw_kv_format */
+} qw_config;
+
+/* Matrix slots of qw_layer_weights.w / .s, in checkpoint order. */
+enum { QW_Q = 0, QW_K = 1, QW_V = 2, QW_O = 3, QW_GATE = 4, QW_UP = 5, QW_DOWN = 6 };
+
+/*
+ * One decoder block's device pointers ("M1 - Load the weights", the 11-tensor
+ * block).  Norm weights are bf16 vectors: input_norm and post_norm [hidden],
+ * q_norm and k_norm [head_dim].  w[i] is the matrix [out, in] row-major
+ * (bf16, or int8 for QW_W_INT8_G32); s[i] its fp16 scales [out, in/32] for
+ * QW_W_INT8_G32, else ignored.  Every pointer must be 16-byte aligned.
+ */
+typedef struct {
+    const void *input_norm;
+    const void *q_norm;
+    const void *k_norm;
+    const void *post_norm;
+    const void *w[7];
+    const void *s[7];
+} qw_layer_weights;
+
+/*
+ * Whole-model weight table.  embed: bf16 [vocab, hidden] (device);
+ * final_norm: bf16 [hidden]; lm_head: bf16 [vocab, hidden] or NULL for a head
+ * tied to embed; layers: HOST array of n_layers entries (copied at create).
+ */
+typedef struct {
+    const void *embed;
+    const void *final_norm;
+    const void *lm_head;
+    const qw_layer_weights *layers;
+} qw_weights;
+
+/*
+ * Bytes of device workspace the model needs: the K/V cache
+ * [n_layers][n_kv_heads][max_ctx][head_dim] twice (f32 or bf16 elements), the RoPE table, decode
+ * activations and split-attention partials, prefill activations for up to
+ * min(max_ctx, 2048) rows, f32 logits [vocab] and bookkeeping.  Returns 0 for
+ * an invalid or unsupported config.
+ */
+size_t qw_workspace_bytes(const qw_config *cfg);
+
+/*
+ * Create a model over borrowed weights and a caller-allocated device
+ * workspace (256-byte aligned, at least qw_workspace_bytes(cfg) bytes).
+ * cuda_stream is a cudaStream_t (NULL = the legacy default stream); every
+ * later call is ordered on it.  Validates everything before touching the
+ * device; fills the RoPE table and clears the bookkeeping.  On success
+ * *out receives the handle and the K/V length is 0.
+ */
+int qw_model_create(const qw_config *cfg, const qw_weights *weights, void *workspace, size_t workspace_bytes,
+                    void *cuda_stream, qw_model **out);
+
+/*
+ * Prefill: run n prompt tokens (host array of ids in [0, vocab)) at positions
+ * len .. len+n-1, appending their K/V.  The logits and greedy pick of the last
+ * prompt position become the model's "last" result (qw_logits; the device-side
+ * token that qw_decode_step(-1) consumes).  If next_token_host is not NULL the
+ * call waits and writes the greedy pick there.  n == 0 is a no-op.
+ * QW_CONTEXT_EXCEEDED if len + n > max_ctx, with nothing changed.
+ */
+int qw_prefill(qw_model *m, const int32_t *tokens_host, int32_t n, int32_t *next_token_host);
+
+/*
+ * Decode one token at position len.  token >= 0 is fed as given; token == -1
+ * feeds the greedy pick of the previous call (already on the device, no host
+ * round trip).  If next_token_host is not NULL the call waits and writes this
+ * step's greedy pick there; with NULL nothing waits.
+ */
+int qw_decode_step(qw_model *m, int32_t token, int32_t *next_token_host);
+
+/*
+ * Greedy generation of n tokens without host synchronisation: feeds `token`
+ * (or the previous pick if -1), then each step's pick into the next.  The n
+ * picks are written to tokens_dev (device int32 [n]) if not NULL.
+ */
+int qw_generate(qw_model *m, int32_t token, int32_t n, int32_t *tokens_dev);
+
+/* Copy the f32 logits [vocab] of the last processed position to dst_dev (device); n must equal vocab. */
+int qw_logits(qw_model *m, float *dst_dev, int64_t n);
+
+/* Forget the cache: len = 0 (no memset; "Scalar-Native ...", section 6 "Cancellation and Reset").
+ * Also clears a recorded device error. */
+int qw_kv_reset(qw_model *m);
+
+/* Current K/V length (number of processed positions). */
+int qw_kv_length(const qw_model *m, int32_t *out);
+
+/* Wait for the stream and report any device-side error recorded since the last check. */
+int qw_sync(qw_model *m);
+
+/* Release the handle (the caller's device buffers are untouched). NULL is allowed. */
+void qw_model_destroy(qw_model *m);
+
+/* ---------------------------------------------------------------- testing */
+
+/*
+ * Replace the cache with n_pos positions of bf16 K and V, each laid out
+ * [n_layers][n_kv_heads][n_pos][head_dim] (device pointers); len = n_pos.
+ * An f32 cache receives the exact widening of the bf16 values.  Used to start
+ * decode from a pre-filled long context.
+ */
+int qw_kv_import(qw_model *m, const void *k_dev, const void *v_dev, int32_t n_pos);
+
+/* Copy cache rows back, layout [n_layers][n_kv_heads][n_pos][head_dim], positions
+ * [0, n_pos), in the cache's own element type (f32 or bf16). */
+int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos);
+
+/*
+ * Debug flags.  QW_DEBUG_HIDDEN: every decode step also stores the residual
+ * stream after the embedding and after each layer, read by qw_debug_hidden.
+ * QW_DEBUG_PREFILL_BY_TOKEN: qw_prefill runs the prompt through the decode
+ * path one token at a time (the differential baseline of the batched prefill).
+ */
+enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2 };
+int qw_set_debug(qw_model *m, int32_t flags);
+
+/* f32 [n_layers+1][hidden] residual stream of the last decode step (needs QW_DEBUG_HIDDEN). */
+int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
+
+/* Static text for a status code. */
+const char *qw_status_string(int status);
+
+/* ABI version the library was built with (QW_ABI_VERSION). */
+int32_t qw_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QW_H */

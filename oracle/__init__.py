@@ -96,6 +96,9 @@ def lib():
             L.ora_kv_import.argtypes = [vp, u16p, u16p, ctypes.c_int32]
             L.ora_step.argtypes = [vp, ctypes.c_int32, f32p, vp]
             L.ora_full.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, f32p]
+            L.ora_set_kv_round_bf16.argtypes = [vp, ctypes.c_int]
+            L.ora_set_kv_round_bf16.restype = None
+            L.ora_kv_row.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p, f32p]
             _LIB = L
     return _LIB
 
@@ -238,6 +241,19 @@ class OracleModel:
                                  v.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), n_pos)
         if rc:
             raise OracleError(rc, "kv_import")
+
+    def set_kv_round_bf16(self, on: bool):
+        """Error attribution only: store K/V rounded to bf16 (not the reference computation)."""
+        lib().ora_set_kv_round_bf16(self._h, 1 if on else 0)
+
+    def kv_row(self, l: int, kvh: int, pos: int):
+        """The cached f32 (key, value) rows of one layer, KV head and position."""
+        k = np.empty(self.cfg.head_dim, np.float32)
+        v = np.empty(self.cfg.head_dim, np.float32)
+        rc = lib().ora_kv_row(self._h, l, kvh, pos, _fp(k), _fp(v))
+        if rc:
+            raise OracleError(rc, "kv_row")
+        return k, v
 
     def step(self, token: int, want_hidden: bool = False):
         """One decode step: (logits [V], hidden [L+1, H] or None)."""

@@ -83,6 +83,7 @@ typedef struct ora_model {
     float *k_cache, *v_cache;   /* f32 [L][Hkv][max_ctx][d] */
     int32_t len;
     float *cos_t, *sin_t;       /* f32 [max_ctx][d/2] */
+    int kv_round_bf16;          /* error attribution only: store K/V rounded to bf16 */
 } ora_model;
 
 /* ------------------------------------------------------------ scalars */
@@ -393,6 +394,32 @@ int ora_kv_import(ora_model *m, const uint16_t *k, const uint16_t *v, int32_t n_
     return ORA_OK;
 }
 
+/*
+ * Error attribution switch (not part of the reference computation): when set,
+ * K/V rows are rounded to bf16 (nearest even) as they are stored, which
+ * isolates the effect of a bf16 cache from every other source of difference.
+ */
+void ora_set_kv_round_bf16(ora_model *m, int on) { m->kv_round_bf16 = on; }
+
+static float round_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Copy the cached f32 key and value rows of (layer, kv head, position). */
+int ora_kv_row(const ora_model *m, int l, int kvh, int pos, float *k, float *v) {
+    const ora_config *c = &m->cfg;
+    if (l < 0 || l >= c->n_layers || kvh < 0 || kvh >= c->n_kv_heads || pos < 0 || pos >= m->len)
+        return ORA_INVALID_ARGUMENT;
+    memcpy(k, kv_row(m, m->k_cache, l, kvh, pos), sizeof(float) * (size_t)c->head_dim);
+    memcpy(v, kv_row(m, m->v_cache, l, kvh, pos), sizeof(float) * (size_t)c->head_dim);
+    return ORA_OK;
+}
+
 typedef struct {
     const ora_model *m;
     int l, pos;
@@ -447,8 +474,14 @@ static int layer_step(ora_model *md, int l, float *x, int pos, float *buf) {
     for (int hh = 0; hh < Hkv; ++hh) ora_qk_norm_rope(k + hh * d, ly->k_norm, d, c->rms_eps, cs, sn, tmp);
     /* 5. K/V append at [l][kvh][pos][:] */
     for (int hh = 0; hh < Hkv; ++hh) {
-        memcpy(kv_row(md, md->k_cache, l, hh, pos), k + hh * d, sizeof(float) * d);
-        memcpy(kv_row(md, md->v_cache, l, hh, pos), v + hh * d, sizeof(float) * d);
+        float *kd = kv_row(md, md->k_cache, l, hh, pos), *vd = kv_row(md, md->v_cache, l, hh, pos);
+        memcpy(kd, k + hh * d, sizeof(float) * d);
+        memcpy(vd, v + hh * d, sizeof(float) * d);
+        if (md->kv_round_bf16)
+            for (int t = 0; t < d; ++t) {
+                kd[t] = round_bf16(kd[t]);
+                vd[t] = round_bf16(vd[t]);
+            }
     }
     /* 6. grouped-query attention over positions 0..pos */
     attn_ctx ac;

@@ -25,6 +25,7 @@ class Workload:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     weight_format: str = "bf16"      # "bf16" | "int8_g32"
+    kv_format: str = "f32"           # K/V cache element type: "f32" (the reference's) | "bf16"
     prompt_len: int = 0              # prefill tokens
     kv_prefill: int = 0              # positions imported into the K/V cache instead of a prompt
     decode_steps: int = 0
@@ -49,7 +50,7 @@ WORKLOADS = {
         "qwen3_0p6b_prefill2048", seed=3, prompt_len=2048, decode_steps=16,
         notes="full 0.6B shape; 2048-token prompt + 16 decode steps"),
     "qwen3_0p6b_ctx32k": Workload(
-        "qwen3_0p6b_ctx32k", seed=4, kv_prefill=32768, decode_steps=64,
+        "qwen3_0p6b_ctx32k", seed=4, kv_prefill=32768, decode_steps=64, kv_format="bf16",
         notes="full 0.6B shape; K/V cache pre-filled to 32768 positions with N(0,1) bf16, 64 decode steps"),
     "qwen3_0p6b_int8": Workload(
         "qwen3_0p6b_int8", seed=5, weight_format="int8_g32", prompt_len=256, decode_steps=768,

@@ -1,0 +1,493 @@
+// qw_api.cu - host side of the C ABI declared in include/qw.h.
+//
+// Everything here is validation, workspace carving and launch bookkeeping; all
+// arithmetic of the decoder runs in the device kernels (decode.cu, prefill.cu).
+// Conventions ("Portable WebAssembly Runtime Architecture for TinyRustLM",
+// section "Typed host/Wasm API"): status codes, handles checked against a table
+// of live models on every call, no exceptions across the boundary.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include "qw.h"
+#include "qw_internal.h"
+#include "qw_prefill.h"
+
+namespace {
+
+constexpr int kMaxCtas = 1024;  // upper bound on SMs, for the split-attention partials
+constexpr size_t kAlign = 256;
+constexpr int kPrefillRowsMax = 2048;
+
+struct Layout {
+    size_t kc, vc, rope, layers, x, qkv, o, act, part, logits, hidden, step, flags;
+    size_t prefill, prefill_bytes;
+    size_t total;
+};
+
+bool mul_ok(size_t a, size_t b, size_t *out) {
+    if (a != 0 && b > SIZE_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+int validate_config(const qw_config *c) {
+    if (!c) return QW_INVALID_ARGUMENT;
+    if (c->weight_format != QW_W_BF16 && c->weight_format != QW_W_INT8_G32) return QW_UNSUPPORTED_QUANTIZATION;
+    if (c->kv_format != QW_KV_F32 && c->kv_format != QW_KV_BF16) return QW_INVALID_ARGUMENT;
+    if (c->n_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+        c->intermediate < 1 || c->vocab < 1 || c->max_ctx < 1)
+        return QW_INVALID_ARGUMENT;
+    if (!(c->rms_eps > 0.0f) || !std::isfinite(c->rms_eps) || !(c->rope_theta > 0.0) || !std::isfinite(c->rope_theta))
+        return QW_INVALID_ARGUMENT;
+    // Q8 blocks are 32 wide and tail groups are not allowed ("Scalar-Native ...", section 3).
+    if (c->hidden % 32 || c->intermediate % 32 || (c->n_heads * c->head_dim) % 32) return QW_UNSUPPORTED_QUANTIZATION;
+    if (c->head_dim != qw::kHeadDim) return QW_UNSUPPORTED_SHAPE;
+    if (c->n_heads % c->n_kv_heads) return QW_UNSUPPORTED_SHAPE;
+    const int g = c->n_heads / c->n_kv_heads;
+    if (g != 1 && g != 2) return QW_UNSUPPORTED_SHAPE;
+    const int qd = c->n_heads * c->head_dim;
+    for (int k : {c->hidden, qd, c->intermediate})
+        if (k % 1024 || k > 3072) return QW_UNSUPPORTED_SHAPE;
+    if (c->n_layers > qw::kMaxLayers || c->max_ctx > 131072 || c->vocab > (1 << 24)) return QW_UNSUPPORTED_SHAPE;
+    return QW_OK;
+}
+
+int make_layout(const qw_config *c, Layout *L) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off += (bytes + kAlign - 1) / kAlign * kAlign;
+        return at;
+    };
+    size_t kv;
+    const size_t esz = c->kv_format == QW_KV_F32 ? 4 : 2;
+    if (!mul_ok((size_t)c->n_layers * c->n_kv_heads, (size_t)c->max_ctx * c->head_dim * esz, &kv))
+        return QW_INTEGER_OVERFLOW;
+    const int g = c->n_heads / c->n_kv_heads;
+    L->kc = take(kv);
+    L->vc = take(kv);
+    L->rope = take((size_t)c->max_ctx * (c->head_dim / 2) * sizeof(float2));
+    L->layers = take((size_t)c->n_layers * sizeof(qw::DevLayer));
+    L->x = take((size_t)c->hidden * 4);
+    L->qkv = take((size_t)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim * 4);
+    L->o = take((size_t)c->n_heads * c->head_dim * 4);
+    L->act = take((size_t)c->intermediate * 4);
+    L->part = take((size_t)kMaxCtas * g * qw::kPartStride * 4);
+    L->logits = take((size_t)c->vocab * 4);
+    L->hidden = take((size_t)(c->n_layers + 1) * c->hidden * 4);
+    L->step = take(qw::step_block_bytes(c->n_layers, c->n_kv_heads));
+    L->flags = take(sizeof(qw::StepFlags));
+    const int rows = c->max_ctx < kPrefillRowsMax ? c->max_ctx : kPrefillRowsMax;
+    L->prefill_bytes = qw::prefill_workspace_bytes(*c, rows);
+    L->prefill = take(L->prefill_bytes);
+    L->total = off;
+    return QW_OK;
+}
+
+std::mutex g_live_mu;
+std::unordered_set<const void *> g_live;
+
+}  // namespace
+
+struct qw_model {
+    qw_config cfg;
+    int group = 0, ncta = 0, nsm = 0, device = 0;
+    cudaStream_t stream = nullptr;
+    uint8_t *ws = nullptr;
+    Layout lay{};
+    qw::DecodeArgs args{};
+    qw::StepFlags *flags = nullptr;
+    void *step_block = nullptr;
+    size_t step_bytes = 0;
+    qw::PrefillState pf{};
+    int32_t len = 0;
+    int has_last = 0;
+    int debug = 0;
+    int failed = 0;  // device error seen; cleared by qw_kv_reset
+    float *logits = nullptr;
+    float *hidden = nullptr;
+};
+
+namespace {
+
+bool live(const qw_model *m) {
+    std::lock_guard<std::mutex> g(g_live_mu);
+    return m && g_live.count(m);
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return QW_OK;
+    fprintf(stderr, "qw: CUDA error %d (%s)\n", (int)e, cudaGetErrorString(e));
+    return QW_CUDA_ERROR;
+}
+
+bool aligned(const void *p, size_t a) { return p && ((uintptr_t)p % a) == 0; }
+
+int split_for(const qw_model *m, int pos) {
+    int s = (pos + 127) / 128;
+    const int cap = m->ncta / m->cfg.n_kv_heads;
+    if (s > cap) s = cap;
+    if (s > pos) s = pos;
+    if (s < 1) s = 1;
+    return s;
+}
+
+// One decode step at position len; token >= 0 or -1 (device-resident previous pick).
+int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
+    qw::DecodeArgs a = m->args;
+    a.pos = m->len;
+    a.token = token;
+    a.n_split = split_for(m, m->len);
+    a.debug = m->debug;
+    a.tok_out = tok_out_dev;
+    a.phase_begin = 0;
+    a.phase_end = qw::kPhasesPerLayer * m->cfg.n_layers + 1;
+    int rc = cuda_status(cudaMemsetAsync(m->step_block, 0, m->step_bytes, m->stream));
+    if (rc) return rc;
+    rc = cuda_status(qw::launch_decode(a, m->group, m->ncta, m->stream));
+    if (rc) return rc;
+    m->len += 1;
+    m->has_last = 1;
+    return QW_OK;
+}
+
+// Wait for the stream, read the flags; returns the device error (if any) and the last pick.
+int read_flags(qw_model *m, int32_t *tok) {
+    qw::StepFlags f;
+    int rc = cuda_status(cudaMemcpyAsync(&f, m->flags, sizeof(f), cudaMemcpyDeviceToHost, m->stream));
+    if (rc) return rc;
+    rc = cuda_status(cudaStreamSynchronize(m->stream));
+    if (rc) return rc;
+    if (f.err) {
+        m->failed = (int)f.err;
+        return (int)f.err;
+    }
+    if (tok) *tok = f.next_tok;
+    return QW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t qw_abi_version(void) { return QW_ABI_VERSION; }
+
+const char *qw_status_string(int s) {
+    switch (s) {
+        case QW_OK: return "ok";
+        case QW_INVALID_ARGUMENT: return "invalid argument";
+        case QW_INVALID_HANDLE: return "invalid handle";
+        case QW_ALIGNMENT: return "pointer misaligned";
+        case QW_INTEGER_OVERFLOW: return "size overflow";
+        case QW_OUT_OF_MEMORY: return "workspace too small";
+        case QW_UNSUPPORTED_QUANTIZATION: return "unsupported quantization (format or a dimension not a multiple of 32)";
+        case QW_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case QW_CONTEXT_EXCEEDED: return "context exceeded";
+        case QW_NUMERICAL_FAILURE: return "non-finite logits";
+        case QW_INTERNAL_INVARIANT: return "device wait expired (internal invariant)";
+        case QW_CUDA_ERROR: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+size_t qw_workspace_bytes(const qw_config *cfg) {
+    if (validate_config(cfg) != QW_OK) return 0;
+    Layout L;
+    if (make_layout(cfg, &L) != QW_OK) return 0;
+    return L.total;
+}
+
+int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, size_t workspace_bytes,
+                    void *cuda_stream, qw_model **out) {
+    if (!out) return QW_INVALID_ARGUMENT;
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!w || !w->layers || !workspace) return QW_INVALID_ARGUMENT;
+    Layout L;
+    rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    if (!aligned(workspace, kAlign)) return QW_ALIGNMENT;
+    if (workspace_bytes < L.total) return QW_OUT_OF_MEMORY;
+    if (!aligned(w->embed, 16) || !aligned(w->final_norm, 16) || (w->lm_head && !aligned(w->lm_head, 16)))
+        return w->embed && w->final_norm ? QW_ALIGNMENT : QW_INVALID_ARGUMENT;
+    const bool i8 = cfg->weight_format == QW_W_INT8_G32;
+    std::vector<qw::DevLayer> host_layers((size_t)cfg->n_layers);
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const qw_layer_weights &lw = w->layers[l];
+        const void *norms[4] = {lw.input_norm, lw.q_norm, lw.k_norm, lw.post_norm};
+        for (const void *p : norms) {
+            if (!p) return QW_INVALID_ARGUMENT;
+            if (!aligned(p, 16)) return QW_ALIGNMENT;
+        }
+        for (int i = 0; i < 7; ++i) {
+            if (!lw.w[i] || (i8 && !lw.s[i])) return QW_INVALID_ARGUMENT;
+            if (!aligned(lw.w[i], 16) || (i8 && !aligned(lw.s[i], 16))) return QW_ALIGNMENT;
+        }
+        qw::DevLayer &d = host_layers[(size_t)l];
+        d.input_norm = (const __nv_bfloat16 *)lw.input_norm;
+        d.q_norm = (const __nv_bfloat16 *)lw.q_norm;
+        d.k_norm = (const __nv_bfloat16 *)lw.k_norm;
+        d.post_norm = (const __nv_bfloat16 *)lw.post_norm;
+        for (int i = 0; i < 7; ++i) {
+            d.w[i] = lw.w[i];
+            d.s[i] = i8 ? (const __half *)lw.s[i] : nullptr;
+        }
+    }
+
+    int dev = 0;
+    rc = cuda_status(cudaGetDevice(&dev));
+    if (rc) return rc;
+    int major = 0, minor = 0, nsm = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) {
+        fprintf(stderr, "qw: device compute capability %d.%d; this library is built for sm_103a only\n", major, minor);
+        return QW_CUDA_ERROR;
+    }
+    const int group = cfg->n_heads / cfg->n_kv_heads;
+    int bps = 0;
+    rc = cuda_status(qw::decode_prepare(group, &bps));
+    if (rc) return rc;
+    if (bps < 1) {
+        fprintf(stderr, "qw: decode kernel does not fit on an SM\n");
+        return QW_CUDA_ERROR;
+    }
+    const int ncta = nsm < kMaxCtas ? nsm : kMaxCtas;
+    rc = cuda_status(qw::prefill_prepare());
+    if (rc) return rc;
+
+    qw_model *m = new (std::nothrow) qw_model();
+    if (!m) return QW_OUT_OF_MEMORY;
+    m->cfg = *cfg;
+    m->group = group;
+    m->ncta = ncta;
+    m->nsm = nsm;
+    m->device = dev;
+    m->stream = (cudaStream_t)cuda_stream;
+    m->ws = (uint8_t *)workspace;
+    m->lay = L;
+    uint8_t *ws = m->ws;
+
+    // RoPE table: cos/sin of pos * theta^(-2i/d), i < d/2, in double, rounded to f32.
+    const int half = cfg->head_dim / 2;
+    std::vector<float2> rope((size_t)cfg->max_ctx * half);
+    for (int i = 0; i < half; ++i) {
+        const double inv_freq = std::pow(cfg->rope_theta, -2.0 * i / (double)cfg->head_dim);
+        for (int p = 0; p < cfg->max_ctx; ++p) {
+            const double ang = (double)p * inv_freq;
+            rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    }
+    rc = cuda_status(cudaMemcpyAsync(ws + L.rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                                     m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemcpyAsync(ws + L.layers, host_layers.data(), host_layers.size() * sizeof(qw::DevLayer),
+                                         cudaMemcpyHostToDevice, m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.flags, 0, sizeof(qw::StepFlags), m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, qw::step_block_bytes(cfg->n_layers, cfg->n_kv_heads), m->stream));
+    if (!rc) rc = cuda_status(cudaStreamSynchronize(m->stream));  // host staging buffers go out of scope
+    if (rc) {
+        delete m;
+        return rc;
+    }
+
+    qw::DecodeArgs &a = m->args;
+    a.L = cfg->n_layers;
+    a.H = cfg->hidden;
+    a.Hq = cfg->n_heads;
+    a.Hkv = cfg->n_kv_heads;
+    a.I = cfg->intermediate;
+    a.V = cfg->vocab;
+    a.max_ctx = cfg->max_ctx;
+    a.fmt = cfg->weight_format;
+    a.eps = cfg->rms_eps;
+    a.layers = (const qw::DevLayer *)(ws + L.layers);
+    a.embed = (const __nv_bfloat16 *)w->embed;
+    a.lm_head = (const __nv_bfloat16 *)(w->lm_head ? w->lm_head : w->embed);
+    a.final_norm = (const __nv_bfloat16 *)w->final_norm;
+    a.kc = ws + L.kc;
+    a.vc = ws + L.vc;
+    a.kv_f32 = cfg->kv_format == QW_KV_F32 ? 1 : 0;
+    a.rope = (const float2 *)(ws + L.rope);
+    a.x = (float *)(ws + L.x);
+    a.qkv = (float *)(ws + L.qkv);
+    a.o = (float *)(ws + L.o);
+    a.act = (float *)(ws + L.act);
+    a.part = (float *)(ws + L.part);
+    a.logits = (float *)(ws + L.logits);
+    a.hidden = (float *)(ws + L.hidden);
+    a.sync = (unsigned *)(ws + L.step);
+    const size_t counters = (size_t)qw::kPhasesPerLayer * cfg->n_layers + 1 + (size_t)cfg->n_layers * cfg->n_kv_heads;
+    a.key = (unsigned long long *)(ws + L.step + ((counters * 4 + 7) / 8) * 8);
+    a.flags = (qw::StepFlags *)(ws + L.flags);
+    m->flags = a.flags;
+    m->step_block = ws + L.step;
+    m->step_bytes = qw::step_block_bytes(cfg->n_layers, cfg->n_kv_heads);
+    m->logits = a.logits;
+    m->hidden = a.hidden;
+    qw::prefill_init(&m->pf, a, ws + L.prefill, L.prefill_bytes,
+                     cfg->max_ctx < kPrefillRowsMax ? cfg->max_ctx : kPrefillRowsMax, nsm);
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        g_live.insert(m);
+    }
+    *out = m;
+    return QW_OK;
+}
+
+void qw_model_destroy(qw_model *m) {
+    if (!m) return;
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        if (!g_live.erase(m)) return;
+    }
+    cudaStreamSynchronize(m->stream);
+    delete m;
+}
+
+int qw_decode_step(qw_model *m, int32_t token, int32_t *next_token_host) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (m->failed) return m->failed;
+    if (token < -1 || token >= m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    if (token == -1 && !m->has_last) return QW_INVALID_ARGUMENT;
+    if (m->len + 1 > m->cfg.max_ctx) return QW_CONTEXT_EXCEEDED;
+    int rc = launch_step(m, token, nullptr);
+    if (rc) return rc;
+    if (next_token_host) return read_flags(m, next_token_host);
+    return QW_OK;
+}
+
+int qw_generate(qw_model *m, int32_t token, int32_t n, int32_t *tokens_dev) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (m->failed) return m->failed;
+    if (n < 0 || token < -1 || token >= m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    if (n == 0) return QW_OK;
+    if (token == -1 && !m->has_last) return QW_INVALID_ARGUMENT;
+    if ((int64_t)m->len + n > m->cfg.max_ctx) return QW_CONTEXT_EXCEEDED;
+    for (int32_t i = 0; i < n; ++i) {
+        int rc = launch_step(m, i == 0 ? token : -1, tokens_dev ? tokens_dev + i : nullptr);
+        if (rc) return rc;
+    }
+    return QW_OK;
+}
+
+int qw_prefill(qw_model *m, const int32_t *tokens_host, int32_t n, int32_t *next_token_host) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (m->failed) return m->failed;
+    if (n < 0 || (n > 0 && !tokens_host)) return QW_INVALID_ARGUMENT;
+    if (n == 0) return QW_OK;
+    if ((int64_t)m->len + n > m->cfg.max_ctx) return QW_CONTEXT_EXCEEDED;
+    for (int32_t i = 0; i < n; ++i)
+        if (tokens_host[i] < 0 || tokens_host[i] >= m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    int rc = QW_OK;
+    if ((m->debug & QW_DEBUG_PREFILL_BY_TOKEN) || !qw::prefill_supported(m->pf)) {
+        for (int32_t i = 0; i < n && !rc; ++i) rc = launch_step(m, tokens_host[i], nullptr);
+    } else {
+        rc = qw::prefill_run(&m->pf, m->args, m->len, tokens_host, n, m->stream);
+        if (!rc) {
+            m->len += n;
+            m->has_last = 1;
+        } else {
+            rc = QW_CUDA_ERROR;
+        }
+    }
+    if (rc) return rc;
+    if (next_token_host) return read_flags(m, next_token_host);
+    return QW_OK;
+}
+
+int qw_logits(qw_model *m, float *dst_dev, int64_t n) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (!dst_dev || n != m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    return cuda_status(cudaMemcpyAsync(dst_dev, m->logits, (size_t)n * 4, cudaMemcpyDeviceToDevice, m->stream));
+}
+
+int qw_kv_reset(qw_model *m) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    m->len = 0;
+    m->has_last = 0;
+    m->failed = 0;
+    return cuda_status(cudaMemsetAsync(m->flags, 0, sizeof(qw::StepFlags), m->stream));
+}
+
+int qw_kv_length(const qw_model *m, int32_t *out) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (!out) return QW_INVALID_ARGUMENT;
+    *out = m->len;
+    return QW_OK;
+}
+
+int qw_sync(qw_model *m) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    return read_flags(m, nullptr);
+}
+
+static int kv_copy(qw_model *m, const void *k_src, const void *v_src, void *k_dst, void *v_dst, int32_t n_pos,
+                   bool import) {
+    const qw_config &c = m->cfg;
+    const bool f32 = c.kv_format == QW_KV_F32;
+    const size_t row = (size_t)c.head_dim * (f32 ? 4 : 2);
+    const size_t width = (size_t)n_pos * row, pitch_cache = (size_t)c.max_ctx * row;
+    const size_t height = (size_t)c.n_layers * c.n_kv_heads;
+    uint8_t *kc = m->ws + m->lay.kc, *vc = m->ws + m->lay.vc;
+    cudaError_t e;
+    if (import && f32) {
+        e = qw::launch_kv_widen((const __nv_bfloat16 *)k_src, (float *)kc, (long long)height, n_pos, c.max_ctx,
+                                m->stream);
+        if (e == cudaSuccess)
+            e = qw::launch_kv_widen((const __nv_bfloat16 *)v_src, (float *)vc, (long long)height, n_pos, c.max_ctx,
+                                    m->stream);
+    } else if (import) {
+        e = cudaMemcpy2DAsync(kc, pitch_cache, k_src, width, width, height, cudaMemcpyDeviceToDevice, m->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(vc, pitch_cache, v_src, width, width, height, cudaMemcpyDeviceToDevice, m->stream);
+    } else {
+        e = cudaMemcpy2DAsync(k_dst, width, kc, pitch_cache, width, height, cudaMemcpyDeviceToDevice, m->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(v_dst, width, vc, pitch_cache, width, height, cudaMemcpyDeviceToDevice, m->stream);
+    }
+    return cuda_status(e);
+}
+
+int qw_kv_import(qw_model *m, const void *k_dev, const void *v_dev, int32_t n_pos) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (n_pos < 0 || (n_pos > 0 && (!k_dev || !v_dev))) return QW_INVALID_ARGUMENT;
+    if (n_pos > m->cfg.max_ctx) return QW_CONTEXT_EXCEEDED;
+    if (!aligned(k_dev, 16) || !aligned(v_dev, 16)) return n_pos ? QW_ALIGNMENT : QW_OK;
+    if (n_pos > 0) {
+        int rc = kv_copy(m, k_dev, v_dev, nullptr, nullptr, n_pos, true);
+        if (rc) return rc;
+    }
+    m->len = n_pos;
+    m->has_last = 0;
+    return QW_OK;
+}
+
+int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (n_pos < 0 || n_pos > m->len || (n_pos > 0 && (!k_dev || !v_dev))) return QW_INVALID_ARGUMENT;
+    if (n_pos == 0) return QW_OK;
+    return kv_copy(m, nullptr, nullptr, k_dev, v_dev, n_pos, false);
+}
+
+int qw_set_debug(qw_model *m, int32_t flags) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN)) return QW_INVALID_ARGUMENT;
+    m->debug = flags;
+    return QW_OK;
+}
+
+int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (!dst_dev || n != (int64_t)(m->cfg.n_layers + 1) * m->cfg.hidden) return QW_INVALID_ARGUMENT;
+    return cuda_status(cudaMemcpyAsync(dst_dev, m->hidden, (size_t)n * 4, cudaMemcpyDeviceToDevice, m->stream));
+}
+
+}  // extern "C"

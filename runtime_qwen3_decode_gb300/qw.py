@@ -1,0 +1,266 @@
+"""ctypes binding of libqw.so (include/qw.h): argument marshalling only.
+
+Every step of the decoder runs in the library's CUDA kernels; PyTorch provides the
+device memory (weights, workspace) and the stream.  Importing this module does not
+need a GPU; creating a model does, and there is no fallback: if the library is not
+built or the device cannot run it, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libqw.so")
+
+OK = 0
+INVALID_ARGUMENT = 1
+INVALID_HANDLE = 4
+ALIGNMENT = 7
+INTEGER_OVERFLOW = 8
+OUT_OF_MEMORY = 9
+UNSUPPORTED_QUANTIZATION = 12
+UNSUPPORTED_SHAPE = 13
+CONTEXT_EXCEEDED = 14
+NUMERICAL_FAILURE = 18
+INTERNAL_INVARIANT = 20
+CUDA_ERROR = 21
+
+W_BF16 = 0
+W_INT8_G32 = 1
+KV_F32 = 0
+KV_BF16 = 1
+DEBUG_HIDDEN = 1
+DEBUG_PREFILL_BY_TOKEN = 2
+MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
+
+# every symbol include/qw.h declares
+EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_step", "qw_generate", "qw_logits",
+           "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
+           "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version")
+
+
+class QwError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = _lib().qw_status_string(code).decode() if _LIB is not None else str(code)
+        super().__init__(f"{what}: {msg} (status {code})")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double),
+                ("max_ctx", ctypes.c_int32), ("weight_format", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("input_norm", ctypes.c_void_p), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+                ("post_norm", ctypes.c_void_p), ("w", ctypes.c_void_p * 7), ("s", ctypes.c_void_p * 7)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libqw.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            L.qw_workspace_bytes.argtypes = [ctypes.POINTER(Config)]
+            L.qw_workspace_bytes.restype = ctypes.c_size_t
+            L.qw_model_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, ctypes.c_size_t, vp,
+                                          ctypes.POINTER(vp)]
+            L.qw_prefill.argtypes = [vp, i32p, i32, i32p]
+            L.qw_decode_step.argtypes = [vp, i32, i32p]
+            L.qw_generate.argtypes = [vp, i32, i32, vp]
+            L.qw_logits.argtypes = [vp, vp, i64]
+            L.qw_kv_reset.argtypes = [vp]
+            L.qw_kv_length.argtypes = [vp, i32p]
+            L.qw_sync.argtypes = [vp]
+            L.qw_model_destroy.argtypes = [vp]
+            L.qw_model_destroy.restype = None
+            L.qw_kv_import.argtypes = [vp, vp, vp, i32]
+            L.qw_kv_export.argtypes = [vp, vp, vp, i32]
+            L.qw_set_debug.argtypes = [vp, i32]
+            L.qw_debug_hidden.argtypes = [vp, vp, i64]
+            L.qw_status_string.argtypes = [ctypes.c_int]
+            L.qw_status_string.restype = ctypes.c_char_p
+            L.qw_abi_version.argtypes = []
+            L.qw_abi_version.restype = i32
+            _LIB = L
+    return _LIB
+
+
+def lib():
+    return _lib()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise QwError(rc, what)
+
+
+def make_config(dims, max_ctx: int | None = None) -> Config:
+    """dims: any object with the Qwen3 dimension attributes (n_layers, hidden, ...)."""
+    fmt = {"bf16": W_BF16, "int8_g32": W_INT8_G32}.get(getattr(dims, "weight_format", "bf16"), -1)
+    kvf = {"f32": KV_F32, "bf16": KV_BF16}.get(getattr(dims, "kv_format", "f32"), -1)
+    return Config(dims.n_layers, dims.hidden, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.intermediate,
+                  dims.vocab, dims.rms_eps, dims.rope_theta, int(max_ctx or dims.max_ctx), fmt, kvf)
+
+
+def workspace_bytes(cfg: Config) -> int:
+    return int(_lib().qw_workspace_bytes(ctypes.byref(cfg)))
+
+
+def weights_to_device(host_weights: dict, int8: bool, device="cuda"):
+    """Copy a {embed, final_norm, layers[...]} dict of numpy arrays to device tensors.
+
+    bf16 tensors travel as int16 bit patterns (the library reads raw bytes).  For the
+    int8 format, each matrix m comes as "<m>_q8" (int8) and "<m>_s" (fp16 bits).
+    """
+    import torch
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(device)
+
+    out = {"embed": dev(host_weights["embed"]), "final_norm": dev(host_weights["final_norm"]), "layers": []}
+    for lw in host_weights["layers"]:
+        d = {k: dev(lw[k]) for k in ("input_norm", "q_norm", "k_norm", "post_norm")}
+        for m in MATRICES:
+            if int8:
+                d[m + "_q8"] = dev(lw[m + "_q8"])
+                d[m + "_s"] = dev(lw[m + "_s"])
+            else:
+                d[m] = dev(lw[m])
+        out["layers"].append(d)
+    return out
+
+
+class Model:
+    """One decoder instance on the current CUDA device and stream."""
+
+    def __init__(self, dims, dev_weights: dict, max_ctx: int | None = None, stream=None):
+        import torch
+
+        self.dims = dims
+        self.cfg = make_config(dims, max_ctx)
+        self.int8 = self.cfg.weight_format == W_INT8_G32
+        nbytes = workspace_bytes(self.cfg)
+        if nbytes == 0:
+            raise QwError(UNSUPPORTED_SHAPE, "workspace_bytes")
+        self._w = dev_weights
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        layers = (LayerWeights * self.cfg.n_layers)()
+        for l, lw in enumerate(dev_weights["layers"]):
+            L = layers[l]
+            L.input_norm = lw["input_norm"].data_ptr()
+            L.q_norm = lw["q_norm"].data_ptr()
+            L.k_norm = lw["k_norm"].data_ptr()
+            L.post_norm = lw["post_norm"].data_ptr()
+            for j, m in enumerate(MATRICES):
+                if self.int8:
+                    L.w[j] = lw[m + "_q8"].data_ptr()
+                    L.s[j] = lw[m + "_s"].data_ptr()
+                else:
+                    L.w[j] = lw[m].data_ptr()
+        self._layers = layers
+        w = Weights(dev_weights["embed"].data_ptr(), dev_weights["final_norm"].data_ptr(), None, layers)
+        h = ctypes.c_void_p()
+        _check(_lib().qw_model_create(ctypes.byref(self.cfg), ctypes.byref(w), self.workspace.data_ptr(), nbytes,
+                                      self.stream.cuda_stream, ctypes.byref(h)), "qw_model_create")
+        self._h = h
+
+    # ---------------------------------------------------------------- lifecycle
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().qw_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    # ------------------------------------------------------------------- calls
+    def prefill(self, tokens, want_token: bool = True):
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = ctypes.c_int32(-1)
+        _check(_lib().qw_prefill(self._h, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), t.size,
+                                 ctypes.byref(out) if want_token else None), "qw_prefill")
+        return int(out.value) if want_token else None
+
+    def decode_step(self, token: int = -1, want_token: bool = True):
+        out = ctypes.c_int32(-1)
+        _check(_lib().qw_decode_step(self._h, int(token), ctypes.byref(out) if want_token else None),
+               "qw_decode_step")
+        return int(out.value) if want_token else None
+
+    def generate(self, n: int, token: int = -1, tokens_out=None):
+        """Greedy n steps with no host sync; tokens_out: device int32 tensor [n] or None."""
+        _check(_lib().qw_generate(self._h, int(token), int(n),
+                                  tokens_out.data_ptr() if tokens_out is not None else None), "qw_generate")
+
+    def logits(self, out=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.cfg.vocab, dtype=torch.float32, device="cuda")
+        _check(_lib().qw_logits(self._h, out.data_ptr(), out.numel()), "qw_logits")
+        return out
+
+    def sync(self):
+        _check(_lib().qw_sync(self._h), "qw_sync")
+
+    def kv_reset(self):
+        _check(_lib().qw_kv_reset(self._h), "qw_kv_reset")
+
+    @property
+    def kv_length(self) -> int:
+        n = ctypes.c_int32(-1)
+        _check(_lib().qw_kv_length(self._h, ctypes.byref(n)), "qw_kv_length")
+        return int(n.value)
+
+    def kv_import(self, k, v, n_pos: int):
+        _check(_lib().qw_kv_import(self._h, k.data_ptr(), v.data_ptr(), int(n_pos)), "qw_kv_import")
+
+    def kv_export(self, n_pos: int):
+        import torch
+        c = self.cfg
+        shape = (c.n_layers, c.n_kv_heads, n_pos, c.head_dim)
+        dt = torch.float32 if c.kv_format == KV_F32 else torch.bfloat16
+        k = torch.empty(shape, dtype=dt, device="cuda")
+        v = torch.empty(shape, dtype=dt, device="cuda")
+        _check(_lib().qw_kv_export(self._h, k.data_ptr(), v.data_ptr(), int(n_pos)), "qw_kv_export")
+        return k, v
+
+    def set_debug(self, flags: int):
+        _check(_lib().qw_set_debug(self._h, int(flags)), "qw_set_debug")
+
+    def debug_hidden(self):
+        import torch
+        c = self.cfg
+        out = torch.empty((c.n_layers + 1, c.hidden), dtype=torch.float32, device="cuda")
+        _check(_lib().qw_debug_hidden(self._h, out.data_ptr(), out.numel()), "qw_debug_hidden")
+        return out
