@@ -217,11 +217,24 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos);
  * QW_DEBUG_PREFILL_BY_TOKEN: qw_prefill runs the prompt through the decode
  * path one token at a time (the differential baseline of the batched prefill).
  */
-enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2 };
+enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2, QW_DEBUG_TRACE = 4 };
 int qw_set_debug(qw_model *m, int32_t flags);
 
 /* f32 [n_layers+1][hidden] residual stream of the last decode step (needs QW_DEBUG_HIDDEN). */
 int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
+
+/*
+ * Timeline of the last decode step (needs QW_DEBUG_TRACE): uint64 %globaltimer
+ * nanoseconds [phase][cta][8], phase = 5*layer + {0 QKV, 1 attention, 2 o_proj,
+ * 3 gate/up, 4 down} and 5*n_layers for the head; stamps 0..3 = consumer before
+ * its wait, after the wait, after its work, after its arrival; 4, 5 = producer's
+ * first and last copy issue of the phase.  n must equal QW_QUERY_TRACE_LEN.
+ */
+int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n);
+
+/* Integer facts about a created model. */
+enum { QW_QUERY_DECODE_CTAS = 1, QW_QUERY_TRACE_LEN = 2, QW_QUERY_WORKSPACE_BYTES = 3 };
+int qw_query(const qw_model *m, int32_t what, int64_t *out);
 
 /* Static text for a status code. */
 const char *qw_status_string(int status);

@@ -5,48 +5,80 @@
 // section 2 steps 1-7; the decode schedule of "Portable WebAssembly Runtime
 // Architecture for TinyRustLM", section "Prefill versus decode") is split into
 // 5 phases per layer plus one head phase:
-//   QKV     h = RMSNorm(x) (folded into the activation load), q|k|v = W h
-//   ATTN    per (KV head, split): QK-Norm + RoPE of the head's queries and of
-//           the new key, append k,v at this position, online-softmax attention
-//           over a slice of the cache; the last split to finish merges
-//   OPROJ   x = x + Wo o
+//   QKV     h = RMSNorm(x) (folded into the activation staging), q|k|v = W h
+//   ATTN    per (KV head, split): QK-Norm + RoPE of the group's queries and of the
+//           new key, append k,v at this position, online softmax over a slice of
+//           the cache, a partial (acc, max, sum) per query head
+//   OPROJ   merge the partials, x = x + Wo o
 //   GATEUP  h2 = RMSNorm(x), a = silu(Wg h2) * (Wu h2)
 //   DOWN    x = x + Wd a
 //   LMHEAD  logits = E RMSNorm(x), packed-key atomicMax argmax (ties -> lowest id)
 //
 // Layout on the GPU: one CTA per SM (cooperative launch, so all CTAs are
-// resident).  Warp 8 of each CTA is a producer that streams, with bulk async
-// copies (cp.async.bulk + mbarrier transaction counts), every weight row and
-// cached K/V row this CTA will consume during the whole step into a ring of
-// shared-memory slots.  Weights do not depend on the step's data, so the ring
-// keeps HBM busy across phase boundaries while the 8 consumer warps wait for
-// the previous phase's outputs.  Phase order between CTAs is a set of global
-// arrival counters (release add / acquire load).  Every output row is owned by
-// one warp, so results do not depend on timing.  Every wait is bounded in time:
-// on expiry the kernel records QW_INTERNAL_INVARIANT, raises an abort flag that
-// every other wait also watches, drains its own copies in flight and returns.
+// resident), 7 consumer warps and 1 producer warp.  The producer streams, with
+// bulk async copies (cp.async.bulk + mbarrier transaction counts), every weight
+// row and cached K/V row its CTA will consume during the whole step into a ring
+// of shared-memory slots.  Weights do not depend on the step's data, so the ring
+// keeps HBM busy across phase boundaries while consumers wait for the previous
+// phase.  Every output row is owned by one warp, so results do not depend on
+// timing.  Every wait is bounded in time: on expiry the kernel records
+// QW_INTERNAL_INVARIANT, raises an abort flag that every other wait also
+// watches, drains its own copies in flight and returns.
+//
+// Data between phases travels as tagged words: 64-bit stores of (tag << 32 |
+// f32 bits), tag = step sequence * 512 + producing phase + 1.  One thread per
+// CTA waits on a per-phase arrival counter, then the CTA reads the words it needs
+// and re-polls any whose tag does not match yet; a naturally aligned 64-bit
+// access is single-copy atomic, so a matching tag guarantees the value and the
+// producer needs no release fence before its arrival.  Buffers are reused every
+// layer; a writer never overwrites words a reader still needs, because every
+// phase reads the whole output of the phase before it: e.g. down(l) rewrites xa
+// only after reading all of gate/up(l), which every CTA produces after its own
+// qkv(l) read of xa.  The residual stream alternates between xa (written by down,
+// read by qkv and the head) and xb (written by o_proj, read by gate/up).
+//
+// The kernel arguments are copied to shared memory at start, so phase bodies read
+// them with shared loads; each lane keeps its columns of the phase's activation in
+// registers while it streams rows.
+#include <cstddef>
+
 #include "qw_internal.h"
 
 namespace qw {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxVec = 3072;  // longest activation vector staged in shared memory
 
-struct __align__(128) Smem {
-    uint8_t slot[kSlots][kSlotBytes];
-    unsigned long long full[kSlots];
-    unsigned long long empty[kSlots];
-    float wacc[kConsumerWarps][2][kHeadDim];  // attention: per-warp accumulators (group <= 2)
-    float wml[kConsumerWarps][2][2];          // attention: per-warp running max, sum
-    float sq[2][kHeadDim];                    // attention: normalised, rotated queries
-    float sk[kHeadDim];                       // attention: this position's key (cache element type)
-    float sv[kHeadDim];                       // attention: this position's value (cache element type)
-    unsigned long long best[kConsumerWarps];  // head: per-warp argmax keys
+// Every array member is 16-byte aligned: slots are bulk-copy destinations, vec, sk and
+// sv are read with 16-byte vector loads.
+struct __align__(16) Smem {
+    alignas(16) uint8_t slot[kSlots][kSlotBytes];
+    alignas(16) float wacc[kConsumerWarps][2][kHeadDim];  // attention: per-warp accumulators (group <= 2)
+    alignas(16) float wml[kConsumerWarps][2][2];          // attention: per-warp running max, sum
+    alignas(16) float sq[2][kHeadDim];                    // attention: normalised, rotated queries
+    alignas(16) float sk[kHeadDim];                       // attention: this position's key (cache element type)
+    alignas(16) float sv[kHeadDim];                       // attention: this position's value (cache element type)
+    alignas(16) float vec[kMaxVec];                       // the phase's activation vector (staged once per CTA)
+    alignas(16) float xown[kMaxOwnRows];                  // this CTA's residual rows, kept for the whole step
+    alignas(16) unsigned long long full[kSlots];
+    alignas(16) unsigned long long empty[kSlots];
+    alignas(16) unsigned long long best[kConsumerWarps];  // head: per-warp argmax keys
+    alignas(16) float red[kConsumerWarps];                // block reductions
+    int fail;                                             // a consumer thread's poll gave up
     int flag;
     int tok;
-    int merge;
     int bad;
+    alignas(16) DecodeArgs args;                          // this launch's arguments
 };
+static_assert(offsetof(Smem, vec) % 16 == 0 && offsetof(Smem, sk) % 16 == 0 && offsetof(Smem, sv) % 16 == 0,
+              "vector-accessed shared arrays must be 16-byte aligned");
+static_assert(sizeof(Smem) <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ Smem &smem() {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    return *reinterpret_cast<Smem *>(smem_raw);
+}
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -107,55 +139,44 @@ __device__ __forceinline__ void bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+// Polls use relaxed loads at gpu scope: the data and flags live in this GPU's memory, and
+// system-scope (volatile) loads would also have to stay coherent with the host side.
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
     unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_add(unsigned *p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-
-__device__ __forceinline__ unsigned ld_volatile(const unsigned *p) { return *(volatile const unsigned *)p; }
 
 __device__ __forceinline__ void raise_error(StepFlags *f, unsigned code, bool abort) {
     atomicCAS(&f->err, 0u, code);
     if (abort) atomicExch(&f->abort, 1u);
 }
 
-// Bounded wait for a phase counter; false on abort or timeout (timeout raises the error).
-__device__ bool wait_count(const unsigned *ctr, unsigned target, StepFlags *f) {
-    unsigned long long t0 = 0;
-    for (unsigned i = 0;; ++i) {
-        if (ld_acquire(ctr) >= target) return true;
-        if ((i & 31u) == 31u) {
-            if (ld_volatile(&f->abort)) return false;
-            unsigned long long t = gtime();
-            if (t0 == 0) {
-                t0 = t;
-            } else if (t - t0 > kWaitLimitNs) {
-                raise_error(f, kErrInvariant, true);
-                return false;
-            }
-        }
+// Bounded poll bookkeeping: true to keep polling, false on abort or timeout.
+__device__ __forceinline__ bool poll_more(unsigned i, unsigned long long &t0, StepFlags *f, bool watch_abort = true) {
+    if ((i & 15u) != 15u) return true;
+    if (watch_abort && ld_relaxed(&f->abort)) return false;
+    const unsigned long long t = gtime();
+    if (t0 == 0) {
+        t0 = t;
+    } else if (t - t0 > kWaitLimitNs) {
+        raise_error(f, kErrInvariant, true);
+        return false;
     }
+    return true;
 }
 
 // Bounded wait for an mbarrier phase; watch_abort = false only while draining.
-__device__ bool mbar_wait(unsigned long long *b, unsigned parity, StepFlags *f, bool watch_abort = true) {
-    if (mbar_test(b, parity)) return true;
-    unsigned long long t0 = gtime();
-    for (unsigned i = 0;; ++i) {
-        if (mbar_test(b, parity)) return true;
-        if ((i & 15u) == 15u) {
-            if (watch_abort && ld_volatile(&f->abort)) return false;
-            if (gtime() - t0 > kWaitLimitNs) {
-                raise_error(f, kErrInvariant, true);
-                return false;
-            }
-        }
-    }
+__device__ __forceinline__ bool mbar_wait(unsigned long long *b, unsigned parity, StepFlags *f,
+                                          bool watch_abort = true) {
+    unsigned long long t0 = 0;
+    for (unsigned i = 0; !mbar_test(b, parity); ++i)
+        if (!poll_more(i, t0, f, watch_abort)) return false;
+    return true;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -167,29 +188,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ float dot8_bf16(uint4 v, const float (&a)[8], float acc) {
-    acc = fmaf(bf_lo(v.x), a[0], acc);
-    acc = fmaf(bf_hi(v.x), a[1], acc);
-    acc = fmaf(bf_lo(v.y), a[2], acc);
-    acc = fmaf(bf_hi(v.y), a[3], acc);
-    acc = fmaf(bf_lo(v.z), a[4], acc);
-    acc = fmaf(bf_hi(v.z), a[5], acc);
-    acc = fmaf(bf_lo(v.w), a[6], acc);
-    acc = fmaf(bf_hi(v.w), a[7], acc);
-    return acc;
-}
-
 __device__ __forceinline__ float i8f(uint32_t word, int byte) {
     return (float)((int)(word << (24 - 8 * byte)) >> 24);
-}
-
-// int8 group-32 dequantisation in registers: w = f32(q) * f32(s) (an exact product).
-__device__ __forceinline__ float dot8_i8(uint2 v, float s, const float (&a)[8], float acc) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc = fmaf(a[e], i8f(v.x, e) * s, acc);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc = fmaf(a[4 + e], i8f(v.y, e) * s, acc);
-    return acc;
 }
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
@@ -198,6 +198,28 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
 }
+
+// ----------------------------------------------------------------- tagged words
+
+__device__ __forceinline__ unsigned phase_tag(const DecodeArgs &a, int ph) { return a.tag_base + (unsigned)ph + 1u; }
+
+__device__ __forceinline__ void st_tag(unsigned long long *p, float v, unsigned tag) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ void ld_tag2(const unsigned long long *p, unsigned long long &x, unsigned long long &y) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_tag(const unsigned long long *p) {
+    unsigned long long x;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
+    return x;
+}
+
+__device__ __forceinline__ bool tag_is(unsigned long long w, unsigned tag) { return (unsigned)(w >> 32) == tag; }
+__device__ __forceinline__ float tag_val(unsigned long long w) { return __uint_as_float((unsigned)w); }
 
 // --------------------------------------------------------------- phase geometry
 
@@ -212,10 +234,14 @@ struct Phase {
     int nchunks;
 };
 
+__device__ __forceinline__ int phase_type(const DecodeArgs &a, int ph) {
+    return ph / kPhasesPerLayer >= a.L ? T_LMHEAD : ph % kPhasesPerLayer;
+}
+
 __device__ __forceinline__ Phase describe(const DecodeArgs &a, int ph, int cta, int ncta) {
     Phase p;
     p.l = ph / kPhasesPerLayer;
-    p.type = (p.l >= a.L) ? T_LMHEAD : ph % kPhasesPerLayer;
+    p.type = phase_type(a, ph);
     p.i8 = 0;
     p.pair = 0;
     p.nchunks = 0;
@@ -228,7 +254,7 @@ __device__ __forceinline__ Phase describe(const DecodeArgs &a, int ph, int cta, 
             p.s = cta % S;
             p.p0 = (int)((long long)a.pos * p.s / S);
             p.p1 = (int)((long long)a.pos * (p.s + 1) / S);
-            const int ch = kSlotBytes / (2 * kHeadDim * (a.kv_f32 ? 4 : 2));
+            const int ch = kv_chunk_rows(a.kv_f32 ? 4 : 2);
             p.nchunks = (p.p1 - p.p0 + ch - 1) / ch;
         } else {
             p.kvh = -1;
@@ -243,9 +269,13 @@ __device__ __forceinline__ Phase describe(const DecodeArgs &a, int ph, int cta, 
         default: p.R = a.V; p.K = a.H; break;
     }
     p.i8 = (p.type != T_LMHEAD) && a.fmt == 1;
-    int bpr = (p.pair ? 2 : 1) * (p.i8 ? p.K + p.K / 16 : 2 * p.K);
+    // output rows per slot; a multiple of 2 x the consumer warps when possible, as each
+    // warp takes two rows per pass
+    const int bpr = (p.pair ? 2 : 1) * (p.i8 ? p.K + p.K / 16 : 2 * p.K);
     p.rpc = kSlotBytes / bpr;
     if (p.rpc > 32) p.rpc = 32;
+    if (p.rpc >= 2 * kConsumerWarps) p.rpc -= p.rpc % (2 * kConsumerWarps);
+    else if (p.rpc >= kConsumerWarps) p.rpc = kConsumerWarps;
     p.r0 = (int)((long long)p.R * cta / ncta);
     p.r1 = (int)((long long)p.R * (cta + 1) / ncta);
     p.nchunks = (p.r1 - p.r0 + p.rpc - 1) / p.rpc;
@@ -279,32 +309,33 @@ __device__ __forceinline__ void copy_rows(Issuer &is, const Phase &p, int ns, in
     }
 }
 
-__device__ void issue_chunk(Issuer &is, const DecodeArgs &a, const Phase &p, int c) {
+__device__ __forceinline__ void issue_chunk(Issuer &is, const DecodeArgs &a, const Phase &p, int c) {
     if (p.type == T_ATTN) {
-        const int esz = a.kv_f32 ? 4 : 2, ch = kSlotBytes / (2 * kHeadDim * esz);
-        int q0 = p.p0 + c * ch;
-        int n = min(ch, p.p1 - q0);
-        size_t off = ((((size_t)p.l * a.Hkv + p.kvh) * a.max_ctx + q0) * kHeadDim) * esz;
+        const int esz = a.kv_f32 ? 4 : 2, ch = kv_chunk_rows(esz);
+        const int q0 = p.p0 + c * ch;
+        const int n = min(ch, p.p1 - q0);
+        const size_t off = ((((size_t)p.l * a.Hkv + p.kvh) * a.max_ctx + q0) * kHeadDim) * esz;
         is.copy(is.slot, (const uint8_t *)a.kc + off, (unsigned)(n * kHeadDim * esz));
         is.copy(is.slot + kSlotBytes / 2, (const uint8_t *)a.vc + off, (unsigned)(n * kHeadDim * esz));
         return;
     }
-    int a0 = p.r0 + c * p.rpc;
-    int n = min(p.rpc, p.r1 - a0);
+    const int a0 = p.r0 + c * p.rpc;
+    const int n = min(p.rpc, p.r1 - a0);
     if (p.type == T_LMHEAD) {
         copy_rows(is, p, n, 0, a.lm_head, nullptr, a0, n);
         return;
     }
     const DevLayer &Ly = a.layers[p.l];
     if (p.type == T_QKV) {
-        int qr = a.Hq * kHeadDim, kr = a.Hkv * kHeadDim;
-        int b = a0 + n;
+        const int qr = a.Hq * kHeadDim, kr = a.Hkv * kHeadDim, b = a0 + n;
         // q rows [0, qr), k rows [qr, qr+kr), v rows [qr+kr, qr+2kr)
         int lo = a0, hi = min(b, qr);
         if (hi > lo) copy_rows(is, p, n, lo - a0, Ly.w[0], Ly.s[0], lo, hi - lo);
-        lo = max(a0, qr); hi = min(b, qr + kr);
+        lo = max(a0, qr);
+        hi = min(b, qr + kr);
         if (hi > lo) copy_rows(is, p, n, lo - a0, Ly.w[1], Ly.s[1], lo - qr, hi - lo);
-        lo = max(a0, qr + kr); hi = b;
+        lo = max(a0, qr + kr);
+        hi = b;
         if (hi > lo) copy_rows(is, p, n, lo - a0, Ly.w[2], Ly.s[2], lo - qr - kr, hi - lo);
     } else if (p.type == T_OPROJ) {
         copy_rows(is, p, n, 0, Ly.w[3], Ly.s[3], a0, n);
@@ -316,19 +347,27 @@ __device__ void issue_chunk(Issuer &is, const DecodeArgs &a, const Phase &p, int
     }
 }
 
-__device__ void producer(const DecodeArgs &a, Smem &sm) {
+__device__ __noinline__ void producer() {
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
     const int cta = blockIdx.x, ncta = gridDim.x;
     const unsigned long long pol_w = policy_evict_first();
     const unsigned long long pol_kv = policy_evict_normal();
     unsigned it = 0;
     bool ok = true;
-    for (int ph = a.phase_begin; ph < a.phase_end && ok; ++ph) {
-        Phase p = describe(a, ph, cta, ncta);
+    const int nph = kPhasesPerLayer * a.L + 1;
+    for (int ph = 0; ph < nph && ok; ++ph) {
+        const Phase p = describe(a, ph, cta, ncta);
+        unsigned long long *tr = a.trace ? a.trace + ((size_t)ph * ncta + cta) * kTraceStamps : nullptr;
         for (int c = 0; c < p.nchunks; ++c) {
-            unsigned slot = it % kSlots, par = ((it / kSlots) & 1u) ^ 1u;
+            const unsigned slot = it % kSlots, par = ((it / kSlots) & 1u) ^ 1u;
             if (!mbar_wait(&sm.empty[slot], par, a.flags)) {
                 ok = false;
                 break;
+            }
+            if (tr) {
+                if (c == 0) tr[4] = gtime();
+                if (c == p.nchunks - 1) tr[5] = gtime();
             }
             Issuer is{sm.slot[slot], &sm.full[slot], p.type == T_ATTN ? pol_kv : pol_w, 0u, false};
             issue_chunk(is, a, p, c);
@@ -341,7 +380,7 @@ __device__ void producer(const DecodeArgs &a, Smem &sm) {
     if (!ok) {
         // drain: the last chunk issued into each slot must land before the CTA exits
         for (unsigned s = 0; s < (unsigned)kSlots && s < it; ++s) {
-            unsigned last = ((it - 1 - s) / kSlots) * kSlots + s;
+            const unsigned last = ((it - 1 - s) / kSlots) * kSlots + s;
             mbar_wait(&sm.full[s], (last / kSlots) & 1u, a.flags, false);
         }
     }
@@ -349,149 +388,364 @@ __device__ void producer(const DecodeArgs &a, Smem &sm) {
 
 // ---------------------------------------------------------------------- consumer
 
-// Activation for lanes' columns 8*(lane + 32 m) + e, m < 4*KM.
-template <int KM>
-__device__ __forceinline__ void load_plain(const float *src, int lane, float (&v)[4 * KM][8]) {
-#pragma unroll
-    for (int m = 0; m < 4 * KM; ++m) {
-        const float4 *p = reinterpret_cast<const float4 *>(src + 8 * (lane + 32 * m));
-        float4 lo = __ldcg(p), hi = __ldcg(p + 1);
-        v[m][0] = lo.x; v[m][1] = lo.y; v[m][2] = lo.z; v[m][3] = lo.w;
-        v[m][4] = hi.x; v[m][5] = hi.y; v[m][6] = hi.z; v[m][7] = hi.w;
-    }
-}
+constexpr int kFailed = -1;                 // uniform: the step is aborting
+constexpr unsigned kDeadBit = 0x80000000u;  // this warp gave up inside a chunk loop
 
-template <int KM>
-__device__ __forceinline__ void load_bf16_row(const __nv_bfloat16 *src, int lane, float (&v)[4 * KM][8]) {
-#pragma unroll
-    for (int m = 0; m < 4 * KM; ++m) {
-        uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + 8 * (lane + 32 * m)));
-        v[m][0] = bf_lo(u.x); v[m][1] = bf_hi(u.x); v[m][2] = bf_lo(u.y); v[m][3] = bf_hi(u.y);
-        v[m][4] = bf_lo(u.z); v[m][5] = bf_hi(u.z); v[m][6] = bf_lo(u.w); v[m][7] = bf_hi(u.w);
-    }
-}
+__device__ __forceinline__ int ctid() { return threadIdx.x; }
+__device__ __forceinline__ int cwarp() { return threadIdx.x >> 5; }
+__device__ __forceinline__ int clane() { return threadIdx.x & 31; }
 
-// In-place RMSNorm over the warp's full vector (each lane holds 32*KM of the K = 1024*KM entries).
-template <int KM>
-__device__ __forceinline__ void rmsnorm_regs(float (&v)[4 * KM][8], const __nv_bfloat16 *w, int lane, float eps) {
-    float ss = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4 * KM; ++m)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[m][e], v[m][e], ss);
-    ss = warp_sum(ss);
-    const float r = rsqrtf(ss * (1.0f / (1024.0f * KM)) + eps);
-#pragma unroll
-    for (int m = 0; m < 4 * KM; ++m) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(w + 8 * (lane + 32 * m)));
-        const float wv[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
-                             bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[m][e] = wv[e] * (v[m][e] * r);
-    }
+__device__ __forceinline__ unsigned long long *trace_of(const DecodeArgs &a, int ph) {
+    return a.trace ? a.trace + ((size_t)ph * gridDim.x + blockIdx.x) * kTraceStamps : nullptr;
 }
-
-template <int KM, bool I8>
-__device__ __forceinline__ float row_dot(const uint8_t *slot, int ns, int j, int lane, const float (&a)[4 * KM][8]) {
-    float acc = 0.f;
-    if constexpr (!I8) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(slot + (size_t)j * (2048 * KM));
-#pragma unroll
-        for (int m = 0; m < 4 * KM; ++m) acc = dot8_bf16(row[lane + 32 * m], a[m], acc);
-    } else {
-        const uint2 *row = reinterpret_cast<const uint2 *>(slot + (size_t)j * (1024 * KM));
-        const __half *sc = reinterpret_cast<const __half *>(slot + (size_t)ns * (1024 * KM) + (size_t)j * (64 * KM));
-#pragma unroll
-        for (int m = 0; m < 4 * KM; ++m) acc = dot8_i8(row[lane + 32 * m], __half2float(sc[(lane + 32 * m) >> 2]), a[m], acc);
-    }
-    return warp_sum(acc);
-}
-
-struct Ctx {
-    const DecodeArgs &a;
-    Smem &sm;
-    int tid, warp, lane, cta, ncta;
-    unsigned it;
-    bool dead;  // this warp saw an abort inside a chunk loop
-};
 
 // Wait for a slot to fill; warp-uniform result.
-__device__ __forceinline__ bool take_slot(Ctx &c, unsigned slot, unsigned par) {
-    bool ok = mbar_wait(&c.sm.full[slot], par, c.a.flags);
+__device__ __forceinline__ bool take_slot(unsigned slot, unsigned par) {
+    Smem &sm = smem();
+    const bool ok = mbar_wait(&sm.full[slot], par, sm.args.flags);
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void release_slot(Ctx &c, unsigned slot) {
+__device__ __forceinline__ void release_slot(unsigned slot) {
     __syncwarp();
-    if (c.lane == 0) mbar_arrive(&c.sm.empty[slot]);
+    if (clane() == 0) mbar_arrive(&smem().empty[slot]);
 }
 
-// Row-streaming phase: each warp owns whole rows of each chunk (row j -> warp j % 8).
+// Thread 0 polls (bounded) until every CTA has arrived at phase ph - 1 of this step;
+// the data itself is then read with tag checks, so the arrival needs no release fence.
+__device__ __forceinline__ bool phase_wait(int ph) {
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
+    if (ctid() == 0) {
+        bool ok = !ld_relaxed(&a.flags->abort);
+        if (ok && ph > 0) {
+            const unsigned *ctr = a.sync + ph - 1;
+            unsigned long long t0 = 0;
+            for (unsigned i = 0; ld_relaxed(ctr) < a.target; ++i)
+                if (!poll_more(i, t0, a.flags)) {
+                    ok = false;
+                    break;
+                }
+        }
+        sm.flag = ok;
+    }
+    bar_consumers();
+    return sm.flag != 0;
+}
+
+// Make a per-thread poll result uniform over the consumer threads (one barrier).
+__device__ __forceinline__ bool all_ok(bool ok) {
+    Smem &sm = smem();
+    if (!ok) sm.fail = 1;
+    bar_consumers();
+    return sm.fail == 0;
+}
+
+// Float4 slots per consumer thread for a vector of 1024*KM floats (index tid + NT*i).
+template <int KM>
+__host__ __device__ constexpr int vec_iters() { return (256 * KM + kConsumerThreads - 1) / kConsumerThreads; }
+
+// Poll the thread's float4 slots tid + NT*i (< 256 KM) of a tagged vector of 1024*KM words.
+template <int KM>
+__device__ __forceinline__ bool poll_vec(const unsigned long long *src, unsigned tag, float4 (&v)[vec_iters<KM>()],
+                                         StepFlags *f) {
+    constexpr int NI = vec_iters<KM>();
+    unsigned long long w[NI][4];
+    unsigned long long t0 = 0;
+    for (unsigned i = 0;; ++i) {
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int idx = ctid() + kConsumerThreads * k;
+            if (idx < 256 * KM) {
+                const unsigned long long *p = src + 4 * idx;
+                ld_tag2(p, w[k][0], w[k][1]);
+                ld_tag2(p + 2, w[k][2], w[k][3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ok &= tag_is(w[k][e], tag);
+            }
+        }
+        if (ok) break;
+        if (!poll_more(i, t0, f)) return false;
+    }
+#pragma unroll
+    for (int k = 0; k < NI; ++k)
+        v[k] = make_float4(tag_val(w[k][0]), tag_val(w[k][1]), tag_val(w[k][2]), tag_val(w[k][3]));
+    return true;
+}
+
+// sm.vec[h*128 + d] = attention output of query head h: the exact merge of the S
+// split partials (acc, running max m, running sum l; log2 domain) written by the
+// attention phase, o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s,
+// accumulated with online rescaling.  Thread t merges 16 dims of one head; two
+// splits are polled per round.
+constexpr int kMergeDims = 16;
+constexpr int kMergeWords = 2 + kMergeDims;
+
+__device__ __forceinline__ void merge_split(const unsigned long long (&w)[kMergeWords], float &mx, float &ls,
+                                            float (&acc)[kMergeDims]) {
+    const float ms = tag_val(w[0]);
+    if (ms == -INFINITY) return;
+    const float mn = fmaxf(mx, ms);
+    const float sa = (mx == -INFINITY) ? 0.f : exp2f(mx - mn), sb = exp2f(ms - mn);
+    ls = ls * sa + tag_val(w[1]) * sb;
+#pragma unroll
+    for (int e = 0; e < kMergeDims; ++e) acc[e] = acc[e] * sa + tag_val(w[2 + e]) * sb;
+    mx = mn;
+}
+
+__device__ __forceinline__ bool load_split(const unsigned long long *pp, int d0, unsigned tag,
+                                           unsigned long long (&w)[kMergeWords]) {
+    ld_tag2(pp + kHeadDim, w[0], w[1]);
+#pragma unroll
+    for (int e = 0; e < kMergeDims; e += 2) ld_tag2(pp + d0 + e, w[2 + e], w[3 + e]);
+    bool ok = true;
+#pragma unroll
+    for (int e = 0; e < kMergeWords; ++e) ok &= tag_is(w[e], tag);
+    return ok;
+}
+
+template <int G>
+__device__ __forceinline__ bool stage_attn_merge(unsigned tag) {
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
+    const int S = a.n_split;
+    const int base = ctid() * kMergeDims;
+    if (base >= a.Hq * kHeadDim) return true;
+    const int h = base / kHeadDim, d0 = base % kHeadDim;
+    const unsigned long long *p0 = a.partt + ((size_t)(h / G) * S * G + (h % G)) * kPartStride;
+    const size_t sstride = (size_t)G * kPartStride;
+    float mx = -INFINITY, ls = 0.f, acc[kMergeDims];
+#pragma unroll
+    for (int e = 0; e < kMergeDims; ++e) acc[e] = 0.f;
+    for (int s = 0; s < S; s += 2) {
+        const bool two = s + 1 < S;
+        unsigned long long w0[kMergeWords], w1[kMergeWords];
+        unsigned long long t0 = 0;
+        for (unsigned i = 0;; ++i) {
+            bool ok = load_split(p0 + s * sstride, d0, tag, w0);
+            if (two) ok &= load_split(p0 + (s + 1) * sstride, d0, tag, w1);
+            if (ok) break;
+            if (!poll_more(i, t0, a.flags)) return false;
+        }
+        merge_split(w0, mx, ls, acc);
+        if (two) merge_split(w1, mx, ls, acc);
+    }
+    float4 *d = reinterpret_cast<float4 *>(sm.vec + base);
+#pragma unroll
+    for (int e = 0; e < kMergeDims; e += 4)
+        d[e / 4] = make_float4(acc[e] / ls, acc[e + 1] / ls, acc[e + 2] / ls, acc[e + 3] / ls);
+    return true;
+}
+
+// Raw weight piece m (8 columns 8*(lane + 32 m) ..) of stored row j of a slot holding ns
+// rows: 16 bytes of bf16, or 8 bytes of int8 codes plus their group's fp16 scale.
 template <int KM, bool I8>
-__device__ void gemv_phase(Ctx &c, const Phase &p) {
-    const DecodeArgs &a = c.a;
-    float act[4 * KM][8];
-    const DevLayer *Ly = p.type == T_LMHEAD ? nullptr : &a.layers[p.l];
-    // activation of this phase, every warp holds the whole vector across its lanes
-    if (p.type == T_QKV || p.type == T_GATEUP || p.type == T_LMHEAD) {
-        if (p.type == T_QKV && p.l == 0) {
-            load_bf16_row<KM>(a.embed + (size_t)c.sm.tok * a.H, c.lane, act);
-            if ((a.debug & 1) && c.cta == 0 && c.warp == 0) {
+struct WPiece;
+template <int KM>
+struct WPiece<KM, false> {
+    uint4 v;
+    __device__ __forceinline__ void load(const uint8_t *sp, int, int j, int lane, int m) {
+        v = reinterpret_cast<const uint4 *>(sp + (size_t)j * (2048 * KM))[lane + 32 * m];
+    }
+    __device__ __forceinline__ void unpack(float (&w)[8]) const {
+        w[0] = bf_lo(v.x); w[1] = bf_hi(v.x); w[2] = bf_lo(v.y); w[3] = bf_hi(v.y);
+        w[4] = bf_lo(v.z); w[5] = bf_hi(v.z); w[6] = bf_lo(v.w); w[7] = bf_hi(v.w);
+    }
+};
+template <int KM>
+struct WPiece<KM, true> {
+    uint2 v;
+    __half s;
+    __device__ __forceinline__ void load(const uint8_t *sp, int ns, int j, int lane, int m) {
+        v = reinterpret_cast<const uint2 *>(sp + (size_t)j * (1024 * KM))[lane + 32 * m];
+        s = reinterpret_cast<const __half *>(sp + (size_t)ns * (1024 * KM) + (size_t)j * (64 * KM))[(lane + 32 * m) >> 2];
+    }
+    // int8 group-32 codes dequantised in registers: w = f32(q) * f32(s), an exact product
+    __device__ __forceinline__ void unpack(float (&w)[8]) const {
+        const float sf = __half2float(s);
 #pragma unroll
-                for (int m = 0; m < 4 * KM; ++m)
+        for (int e = 0; e < 4; ++e) w[e] = i8f(v.x, e) * sf;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) a.hidden[8 * (c.lane + 32 * m) + e] = act[m][e];
+        for (int e = 0; e < 4; ++e) w[4 + e] = i8f(v.y, e) * sf;
+    }
+};
+
+// Dot products of NR stored rows with the activation held in registers
+// (act[8 m + e] = activation column 8*(lane + 32 m) + e).  All weight loads of the
+// row group are issued before any arithmetic, and the accumulation chains of the
+// rows are interleaved; rows must be valid slot rows (callers clamp unused ones).
+template <int KM, bool I8, int NR>
+__device__ __forceinline__ void dot_rows(const uint8_t *sp, int ns, const int (&rows)[NR], int lane,
+                                         const float *act, float (&out)[NR]) {
+    WPiece<KM, I8> wp[NR][4 * KM];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int m = 0; m < 4 * KM; ++m) wp[r][m].load(sp, ns, rows[r], lane, m);
+    float acc[NR][2];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc[r][0] = acc[r][1] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4 * KM; ++m) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float w[8];
+            wp[r][m].unpack(w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[r][0] = fmaf(w[e], act[8 * m + e], acc[r][0]);
+#pragma unroll
+            for (int e = 4; e < 8; ++e) acc[r][1] = fmaf(w[e], act[8 * m + e], acc[r][1]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) out[r] = acc[r][0] + acc[r][1];
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) out[r] += __shfl_xor_sync(0xffffffffu, out[r], o);
+}
+
+// Row-streaming phase PT: stage the activation vector in shared memory once per CTA
+// (RMSNorm folded in where the phase normalises), then each warp owns whole rows
+// (two at a time) of each chunk.  Thread t stages float4 slots t + NT*i.
+// Returns the new ring position (kDeadBit set if this warp gave up) or kFailed.
+template <int PT, int KM, bool I8, int G>
+__device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
+    constexpr bool norm = PT == T_QKV || PT == T_GATEUP || PT == T_LMHEAD;
+    constexpr bool pair = PT == T_GATEUP;
+    constexpr int NI = vec_iters<KM>();
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
+    const int tid = ctid(), warp = cwarp(), lane = clane();
+    const Phase p = describe(a, ph, blockIdx.x, gridDim.x);
+    const bool embed = PT == T_QKV && p.l == 0;
+    const int own0 = (int)((long long)a.H * blockIdx.x / gridDim.x);
+    const unsigned in_tag = ph ? phase_tag(a, ph - 1) : 0u, out_tag = phase_tag(a, ph);
+    unsigned long long *tr = trace_of(a, ph);
+    // read-only inputs first: they do not depend on the previous phase, so their
+    // latency overlaps the wait
+    float4 nw[NI], v[NI];
+    if constexpr (norm) {
+        const __nv_bfloat16 *w = PT == T_QKV    ? a.layers[p.l].input_norm
+                                 : PT == T_GATEUP ? a.layers[p.l].post_norm
+                                                  : a.final_norm;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int idx = tid + kConsumerThreads * i;
+            if (idx < 256 * KM) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(w) + idx);
+                nw[i] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+            }
+        }
+    }
+    if (tr && tid == 0) tr[0] = gtime();
+    if (!phase_wait(ph)) return kFailed;
+    bool ok = true;
+    float4 *vec4 = reinterpret_cast<float4 *>(sm.vec);
+    if constexpr (PT == T_OPROJ) {
+        ok = stage_attn_merge<G>(in_tag);
+    } else {
+        if (embed) {
+            const uint2 *row = reinterpret_cast<const uint2 *>(a.embed + (size_t)sm.tok * a.H);
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int idx = tid + kConsumerThreads * i;
+                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (idx < 256 * KM) {
+                    const uint2 u = __ldg(row + idx);
+                    v[i] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+                    if ((a.debug & 1) && blockIdx.x == 0) reinterpret_cast<float4 *>(a.hidden)[idx] = v[i];
+                }
             }
         } else {
-            load_plain<KM>(a.x, c.lane, act);
+            const unsigned long long *src = PT == T_GATEUP ? a.xb : PT == T_DOWN ? a.actt : a.xa;
+            ok = poll_vec<KM>(src, in_tag, v, a.flags);
         }
-        const __nv_bfloat16 *nw =
-            p.type == T_QKV ? Ly->input_norm : (p.type == T_GATEUP ? Ly->post_norm : a.final_norm);
-        rmsnorm_regs<KM>(act, nw, c.lane, a.eps);
-    } else if (p.type == T_OPROJ) {
-        load_plain<KM>(a.o, c.lane, act);
-    } else {
-        load_plain<KM>(a.act, c.lane, act);
+    }
+    if (tr && tid == 0) tr[1] = gtime();
+    if constexpr (norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+            if (tid + kConsumerThreads * i < 256 * KM)
+                ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        ss = warp_sum(ss);
+        if (lane == 0) sm.red[warp] = ss;
+        if (!all_ok(ok)) return kFailed;
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) tot += sm.red[w];
+        const float r = rsqrtf(tot * (1.0f / (1024.0f * KM)) + a.eps);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int idx = tid + kConsumerThreads * i;
+            if (idx < 256 * KM)
+                vec4[idx] = make_float4(nw[i].x * (v[i].x * r), nw[i].y * (v[i].y * r), nw[i].z * (v[i].z * r),
+                                        nw[i].w * (v[i].w * r));
+        }
+    } else if constexpr (PT != T_OPROJ) {
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int idx = tid + kConsumerThreads * i;
+            if (idx < 256 * KM) vec4[idx] = v[i];
+        }
+    }
+    if (!all_ok(ok)) return kFailed;
+    // each lane keeps its 32*KM activation columns in registers for the whole phase
+    float areg[8 * 4 * KM];
+#pragma unroll
+    for (int m = 0; m < 4 * KM; ++m) {
+        reinterpret_cast<float4 *>(areg)[2 * m] = reinterpret_cast<const float4 *>(sm.vec + 8 * (lane + 32 * m))[0];
+        reinterpret_cast<float4 *>(areg)[2 * m + 1] = reinterpret_cast<const float4 *>(sm.vec + 8 * (lane + 32 * m))[1];
     }
     unsigned long long best = 0;
-    bool bad = false;
+    bool bad = false, dead = false;
     for (int ch = 0; ch < p.nchunks; ++ch) {
-        const unsigned slot = c.it % kSlots, par = (c.it / kSlots) & 1u;
-        ++c.it;
-        if (!take_slot(c, slot, par)) {
-            c.dead = true;
+        const unsigned slot = it % kSlots, par = (it / kSlots) & 1u;
+        ++it;
+        if (!take_slot(slot, par)) {
+            dead = true;
             break;
         }
-        const uint8_t *sp = c.sm.slot[slot];
+        const uint8_t *sp = sm.slot[slot];
         const int a0 = p.r0 + ch * p.rpc;
         const int n = min(p.rpc, p.r1 - a0);
-        const int ns = p.pair ? 2 * n : n;
-        for (int j = c.warp; j < n; j += kConsumerWarps) {
-            const int row = a0 + j;
-            if (p.pair) {
-                float g = row_dot<KM, I8>(sp, ns, j, c.lane, act);
-                float u = row_dot<KM, I8>(sp, ns, j + n, c.lane, act);
-                if (c.lane == 0) a.act[row] = (g / (1.0f + __expf(-g))) * u;
+        const int ns = pair ? 2 * n : n;
+        for (int j = warp; j < n; j += 2 * kConsumerWarps) {
+            const int j2 = j + kConsumerWarps;
+            const int cnt = j2 < n ? 2 : 1;
+            const int j2c = cnt == 2 ? j2 : j;  // an unused second row repeats the first
+            if constexpr (pair) {
+                // gate row j, up row j (stored at n + j), and the same for j2
+                const int rows[4] = {j, n + j, j2c, n + j2c};
+                float o[4];
+                dot_rows<KM, I8, 4>(sp, ns, rows, lane, areg, o);
+                if (lane == 0) {
+                    st_tag(a.actt + a0 + j, (o[0] / (1.0f + __expf(-o[0]))) * o[1], out_tag);
+                    if (cnt == 2) st_tag(a.actt + a0 + j2, (o[2] / (1.0f + __expf(-o[2]))) * o[3], out_tag);
+                }
             } else {
-                float v = row_dot<KM, I8>(sp, ns, j, c.lane, act);
-                if (c.lane == 0) {
-                    switch (p.type) {
-                        case T_QKV: a.qkv[row] = v; break;
-                        case T_OPROJ: {
-                            float r = p.l == 0 ? __bfloat162float(a.embed[(size_t)c.sm.tok * a.H + row]) : __ldcg(a.x + row);
-                            a.x[row] = r + v;
-                            break;
-                        }
-                        case T_DOWN: {
-                            float nx = __ldcg(a.x + row) + v;
-                            a.x[row] = nx;
-                            if (a.debug & 1) a.hidden[(size_t)(p.l + 1) * a.H + row] = nx;
-                            break;
-                        }
-                        default: {
-                            a.logits[row] = v;
-                            if (isfinite(v)) {
-                                unsigned long long k = argmax_key(v, row);
+                const int rows[2] = {j, j2c};
+                float o[2];
+                dot_rows<KM, I8, 2>(sp, ns, rows, lane, areg, o);
+                if (lane == 0) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        if (r >= cnt) break;
+                        const int row = a0 + (r ? j2 : j);
+                        if constexpr (PT == T_QKV) {
+                            st_tag(a.qkvt + row, o[r], out_tag);
+                        } else if constexpr (PT == T_OPROJ || PT == T_DOWN) {
+                            // the residual rows of this CTA live in shared memory for the whole step
+                            const float nx = sm.xown[row - own0] + o[r];
+                            sm.xown[row - own0] = nx;
+                            st_tag((PT == T_OPROJ ? a.xb : a.xa) + row, nx, out_tag);
+                            if (PT == T_DOWN && (a.debug & 1)) a.hidden[(size_t)(p.l + 1) * a.H + row] = nx;
+                        } else {
+                            a.logits[row] = o[r];
+                            if (isfinite(o[r])) {
+                                const unsigned long long k = argmax_key(o[r], row);
                                 best = k > best ? k : best;
                             } else {
                                 bad = true;
@@ -501,28 +755,46 @@ __device__ void gemv_phase(Ctx &c, const Phase &p) {
                 }
             }
         }
-        release_slot(c, slot);
+        release_slot(slot);
     }
-    if (p.type == T_LMHEAD && c.lane == 0) {
-        c.sm.best[c.warp] = best;
-        if (bad) atomicOr(&c.sm.bad, 1);
+    if constexpr (PT == T_LMHEAD) {
+        if (lane == 0) {
+            sm.best[warp] = best;
+            if (bad) atomicOr(&sm.bad, 1);
+        }
     }
+    return (int)(it | (dead ? kDeadBit : 0u));
 }
 
-// QK-Norm then RoPE of one head held as dims (lane, lane+32, lane+64, lane+96).
-__device__ __forceinline__ void qk_norm_rope(float (&v)[4], const __nv_bfloat16 *w, const float2 *rope, int lane,
-                                             float eps) {
+// QK-Norm then RoPE of one head held as dims (lane, lane+32, lane+64, lane+96);
+// w and cs are the lane's norm weights and (cos, sin) for dims lane and lane+32.
+__device__ __forceinline__ void qk_norm_rope(float (&v)[4], const float (&w)[4], const float2 (&cs)[2], float eps) {
     float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
     ss = warp_sum(ss);
     const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __bfloat162float(w[lane + 32 * i]) * (v[i] * r);
-    const float2 cs0 = rope[lane], cs1 = rope[lane + 32];
+    for (int i = 0; i < 4; ++i) v[i] = w[i] * (v[i] * r);
     const float a0 = v[0], a1 = v[1], b0 = v[2], b1 = v[3];
-    v[0] = a0 * cs0.x - b0 * cs0.y;
-    v[2] = b0 * cs0.x + a0 * cs0.y;
-    v[1] = a1 * cs1.x - b1 * cs1.y;
-    v[3] = b1 * cs1.x + a1 * cs1.y;
+    v[0] = a0 * cs[0].x - b0 * cs[0].y;
+    v[2] = b0 * cs[0].x + a0 * cs[0].y;
+    v[1] = a1 * cs[1].x - b1 * cs[1].y;
+    v[3] = b1 * cs[1].x + a1 * cs[1].y;
+}
+
+// Poll a head's 128 tagged values as dims (lane, lane+32, lane+64, lane+96).
+__device__ __forceinline__ bool poll_head(const unsigned long long *src, int lane, unsigned tag, float (&v)[4],
+                                          StepFlags *f) {
+    unsigned long long w[4];
+    unsigned long long t0 = 0;
+    for (unsigned i = 0;; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = ld_tag(src + lane + 32 * k);
+        if (tag_is(w[0], tag) && tag_is(w[1], tag) && tag_is(w[2], tag) && tag_is(w[3], tag)) break;
+        if (!poll_more(i, t0, f)) return false;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = tag_val(w[k]);
+    return true;
 }
 
 // K/V element type of the cache: f32 (default) or bf16.
@@ -550,12 +822,9 @@ struct KvTraits<__nv_bfloat16> {
     __device__ static __forceinline__ __nv_bfloat16 store(float v) { return __float2bfloat16_rn(v); }
 };
 
-template <typename KT>
-constexpr int attn_chunk() { return kSlotBytes / (2 * kHeadDim * (int)sizeof(KT)); }
-
 // Online-softmax update over n positions whose K and V rows (128 elements of KT each)
 // sit at kb and vb.  Eight lanes share a position: lane (jj = lane/8, o8 = lane%8)
-// takes dims [16*o8, 16*o8 + 16) of positions base + 4*warp + jj for base = 0, 32, ...
+// takes dims [16*o8, 16*o8 + 16) of positions base + 4*warp + jj for base = 0, 4*NCW, ...
 // Each lane visits its 16-byte pieces in an order rotated by f(o8), so the eight
 // lanes of a shared-memory phase hit distinct banks; lanes with equal o8 share f,
 // which keeps their accumulators aligned for the reduction over jj.
@@ -621,52 +890,73 @@ __device__ __forceinline__ void attn_block(const uint8_t *kb, const uint8_t *vb,
     }
 }
 
+// One (KV head, split) item: QK-Norm + RoPE of the group's queries and of the new key,
+// append k, v at this position (the last split owns it), online softmax over the
+// split's cached positions (+ the new one), and the split's tagged partial (acc, max,
+// sum) for each query head of the group.  The o_proj phase merges the partials.
 template <int G, typename KT>
-__device__ void attn_phase(Ctx &c, const Phase &p) {
+__device__ __forceinline__ int attn_phase(int ph, unsigned it) {
     using T = KvTraits<KT>;
-    constexpr int NP = T::kPieces, PER = T::kPer, CH = attn_chunk<KT>();
-    const DecodeArgs &a = c.a;
-    Smem &sm = c.sm;
-    if (p.kvh < 0) return;
+    constexpr int NP = T::kPieces, PER = T::kPer, CH = kv_chunk_rows((int)sizeof(KT));
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
+    const int tid = ctid(), warp = cwarp(), lane = clane();
+    const Phase p = describe(a, ph, blockIdx.x, gridDim.x);
+    unsigned long long *tr = trace_of(a, ph);
+    if (p.kvh < 0) {  // no attention item on this CTA
+        if (tr && tid == 0) tr[0] = tr[1] = gtime();
+        return (int)it;
+    }
     const int S = a.n_split, P = a.pos, kvh = p.kvh, l = p.l;
     const bool owner = (p.s == S - 1);
     const DevLayer &Ly = a.layers[l];
-    const float2 *rope = a.rope + (size_t)P * (kHeadDim / 2);
-    const int warp = c.warp, lane = c.lane;
+    const unsigned in_tag = phase_tag(a, ph - 1), out_tag = phase_tag(a, ph);
+    // read-only inputs before the wait: norm weights and this position's rotation
+    float w4[4];
+    float2 cs[2];
+    if (warp <= G) {
+        const __nv_bfloat16 *nw = warp < G ? Ly.q_norm : Ly.k_norm;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w4[i] = __bfloat162float(nw[lane + 32 * i]);
+        const float2 *rope = a.rope + (size_t)P * (kHeadDim / 2);
+        cs[0] = rope[lane];
+        cs[1] = rope[lane + 32];
+    }
+    if (tr && tid == 0) tr[0] = gtime();
+    if (!phase_wait(ph)) return kFailed;
     KT *snew_k = reinterpret_cast<KT *>(sm.sk), *snew_v = reinterpret_cast<KT *>(sm.sv);
     const size_t row_off = (((size_t)l * a.Hkv + kvh) * a.max_ctx + P) * kHeadDim;
+    bool ok = true;
     if (warp < G) {
-        const float *src = a.qkv + (size_t)(kvh * G + warp) * kHeadDim;
         float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + lane + 32 * i);
-        qk_norm_rope(v, Ly.q_norm, rope, lane, a.eps);
+        ok = poll_head(a.qkvt + (size_t)(kvh * G + warp) * kHeadDim, lane, in_tag, v, a.flags);
+        qk_norm_rope(v, w4, cs, a.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) sm.sq[warp][lane + 32 * i] = v[i];
     } else if (warp == G) {
-        const float *src = a.qkv + (size_t)(a.Hq + kvh) * kHeadDim;
         float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + lane + 32 * i);
-        qk_norm_rope(v, Ly.k_norm, rope, lane, a.eps);
+        ok = poll_head(a.qkvt + (size_t)(a.Hq + kvh) * kHeadDim, lane, in_tag, v, a.flags);
+        qk_norm_rope(v, w4, cs, a.eps);
         KT *dst = reinterpret_cast<KT *>(a.kc) + row_off;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const KT b = T::store(v[i]);
             snew_k[lane + 32 * i] = b;
-            if (owner) dst[lane + 32 * i] = b;
+            if (owner && ok) dst[lane + 32 * i] = b;
         }
     } else if (warp == G + 1) {
-        const float *src = a.qkv + (size_t)(a.Hq + a.Hkv + kvh) * kHeadDim;
+        float v[4];
+        ok = poll_head(a.qkvt + (size_t)(a.Hq + a.Hkv + kvh) * kHeadDim, lane, in_tag, v, a.flags);
         KT *dst = reinterpret_cast<KT *>(a.vc) + row_off;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const KT b = T::store(__ldcg(src + lane + 32 * i));
+            const KT b = T::store(v[i]);
             snew_v[lane + 32 * i] = b;
-            if (owner) dst[lane + 32 * i] = b;
+            if (owner && ok) dst[lane + 32 * i] = b;
         }
     }
-    bar_consumers();
+    if (tr && tid == 0) tr[1] = gtime();
+    if (!all_ok(ok)) return kFailed;
 
     const int jj = lane >> 3, o8 = lane & 7, f = (o8 / (8 / NP)) % NP;
     const float qscale = 0.08838834764831845f * kLog2e;  // 1/sqrt(128), log2 domain
@@ -683,17 +973,20 @@ __device__ void attn_phase(Ctx &c, const Phase &p) {
                 acc[h][r][e] = 0.f;
             }
     }
+    bool dead = false;
     for (int ch = 0; ch < p.nchunks; ++ch) {
-        const unsigned slot = c.it % kSlots, par = (c.it / kSlots) & 1u;
-        ++c.it;
-        if (!c.dead && !take_slot(c, slot, par)) c.dead = true;
-        if (c.dead) break;
+        const unsigned slot = it % kSlots, par = (it / kSlots) & 1u;
+        ++it;
+        if (!take_slot(slot, par)) {
+            dead = true;
+            break;
+        }
         const uint8_t *sp = sm.slot[slot];
         const int n = min(CH, p.p1 - (p.p0 + ch * CH));
         attn_block<G, KT>(sp, sp + kSlotBytes / 2, n, warp, lane, qr, acc, M, Ls);
-        release_slot(c, slot);
+        release_slot(slot);
     }
-    if (owner && !c.dead)
+    if (owner && !dead)
         attn_block<G, KT>(reinterpret_cast<const uint8_t *>(snew_k), reinterpret_cast<const uint8_t *>(snew_v), 1,
                           warp, lane, qr, acc, M, Ls);
     // combine the four positions of each warp (lanes with equal o8 share a dim order)
@@ -727,8 +1020,8 @@ __device__ void attn_phase(Ctx &c, const Phase &p) {
         }
     }
     bar_consumers();
-    // combine the eight warps: exact split-softmax merge
-    for (int t = c.tid; t < G * kHeadDim; t += kConsumerThreads) {
+    // combine the warps into this split's tagged partial (exact rescaling to the common max)
+    for (int t = tid; t < G * kHeadDim; t += kConsumerThreads) {
         const int h = t / kHeadDim, dim = t % kHeadDim;
         float mx = -INFINITY;
         for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, sm.wml[w][h][0]);
@@ -742,111 +1035,105 @@ __device__ void attn_phase(Ctx &c, const Phase &p) {
                 ls = fmaf(sm.wml[w][h][1], sc, ls);
             }
         }
-        if (S == 1) {
-            a.o[(size_t)(kvh * G + h) * kHeadDim + dim] = av / ls;
-        } else {
-            float *pp = a.part + ((size_t)(kvh * S + p.s) * G + h) * kPartStride;
-            pp[dim] = av;
-            if (dim == 0) {
-                pp[kHeadDim] = mx;
-                pp[kHeadDim + 1] = ls;
-            }
+        unsigned long long *pp = a.partt + ((size_t)(kvh * S + p.s) * G + h) * kPartStride;
+        st_tag(pp + dim, av, out_tag);
+        if (dim == 0) {
+            st_tag(pp + kHeadDim, mx, out_tag);
+            st_tag(pp + kHeadDim + 1, ls, out_tag);
         }
     }
-    if (S == 1) return;
-    __threadfence();
-    bar_consumers();
-    if (c.tid == 0) {
-        const unsigned old = atomicAdd(&a.sync[kPhasesPerLayer * a.L + 1 + l * a.Hkv + kvh], 1u);
-        __threadfence();
-        sm.merge = (old == (unsigned)(S - 1));
-    }
-    bar_consumers();
-    if (!sm.merge) return;
-    for (int t = c.tid; t < G * kHeadDim; t += kConsumerThreads) {
-        const int h = t / kHeadDim, dim = t % kHeadDim;
-        float mx = -INFINITY;
-        for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldcg(a.part + ((size_t)(kvh * S + s) * G + h) * kPartStride + kHeadDim));
-        float av = 0.f, ls = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float *pp = a.part + ((size_t)(kvh * S + s) * G + h) * kPartStride;
-            const float ms = __ldcg(pp + kHeadDim);
-            if (ms == -INFINITY) continue;
-            const float sc = exp2f(ms - mx);
-            av = fmaf(__ldcg(pp + dim), sc, av);
-            ls = fmaf(__ldcg(pp + kHeadDim + 1), sc, ls);
-        }
-        a.o[(size_t)(kvh * G + h) * kHeadDim + dim] = av / ls;
+    return (int)(it | (dead ? kDeadBit : 0u));
+}
+
+template <int PT, bool I8, int G>
+__device__ __forceinline__ int gemv_km(int K, int ph, unsigned it) {
+    switch (K >> 10) {
+        case 1: return gemv_phase<PT, 1, I8, G>(ph, it);
+        case 2: return gemv_phase<PT, 2, I8, G>(ph, it);
+        default: return gemv_phase<PT, 3, I8, G>(ph, it);
     }
 }
 
-template <bool I8>
-__device__ void gemv_dispatch(Ctx &c, const Phase &p) {
-    switch (p.K >> 10) {
-        case 1: gemv_phase<1, I8>(c, p); break;
-        case 2: gemv_phase<2, I8>(c, p); break;
-        default: gemv_phase<3, I8>(c, p); break;
+template <bool I8, int G>
+__device__ __forceinline__ int gemv_dispatch(const DecodeArgs &a, int type, int ph, unsigned it) {
+    switch (type) {
+        case T_QKV: return gemv_km<T_QKV, I8, G>(a.H, ph, it);
+        case T_OPROJ: return gemv_km<T_OPROJ, I8, G>(a.Hq * kHeadDim, ph, it);
+        case T_GATEUP: return gemv_km<T_GATEUP, I8, G>(a.H, ph, it);
+        case T_DOWN: return gemv_km<T_DOWN, I8, G>(a.I, ph, it);
+        default: return gemv_km<T_LMHEAD, false, G>(a.H, ph, it);
     }
 }
 
 template <int G>
-__device__ void consumer(const DecodeArgs &a, Smem &sm) {
-    Ctx c{a, sm, (int)threadIdx.x, (int)threadIdx.x >> 5, (int)threadIdx.x & 31, (int)blockIdx.x, (int)gridDim.x, 0u,
-          false};
-    if (c.tid == 0) {
-        int tok = a.token >= 0 ? a.token : a.flags->next_tok;
+__device__ void consumer() {
+    Smem &sm = smem();
+    const DecodeArgs &a = sm.args;
+    const int tid = ctid();
+    if (tid == 0) {
+        const int tok = a.token >= 0 ? a.token : a.flags->next_tok;
         sm.tok = tok;
         sm.bad = 0;
-        sm.flag = (tok >= 0 && tok < a.V) ? 1 : 0;
-        if (!sm.flag) raise_error(a.flags, kErrInvalidArgument, true);
+        sm.fail = 0;
+        const bool valid = tok >= 0 && tok < a.V;
+        sm.flag = valid && !ld_relaxed(&a.flags->abort);
+        if (!valid) raise_error(a.flags, kErrInvalidArgument, true);
     }
     bar_consumers();
     if (!sm.flag) return;
-    for (int ph = a.phase_begin; ph < a.phase_end; ++ph) {
-        if (c.tid == 0) sm.flag = (ph == 0) ? !ld_volatile(&a.flags->abort) : wait_count(&a.sync[ph - 1], c.ncta, a.flags);
+    // residual rows owned by this CTA start as the embedding of the input token
+    const int own0 = (int)((long long)a.H * blockIdx.x / gridDim.x);
+    const int own1 = (int)((long long)a.H * (blockIdx.x + 1) / gridDim.x);
+    for (int j = tid; j < own1 - own0; j += kConsumerThreads)
+        sm.xown[j] = __bfloat162float(a.embed[(size_t)sm.tok * a.H + own0 + j]);
+    unsigned it = 0;
+    const int nph = kPhasesPerLayer * a.L + 1;
+    for (int ph = 0; ph < nph; ++ph) {
+        const int type = phase_type(a, ph);
+        int r;
+        if (type == T_ATTN)
+            r = a.kv_f32 ? attn_phase<G, float>(ph, it) : attn_phase<G, __nv_bfloat16>(ph, it);
+        else if (a.fmt == 1)
+            r = gemv_dispatch<true, G>(a, type, ph, it);
+        else
+            r = gemv_dispatch<false, G>(a, type, ph, it);
+        unsigned long long *tr = trace_of(a, ph);
+        if (tr && tid == 0) tr[2] = gtime();
+        if (r == kFailed) return;  // uniform: decided at a barrier
+        if (((unsigned)r & kDeadBit) && clane() == 0) raise_error(a.flags, kErrInvariant, true);
+        it = (unsigned)r & ~kDeadBit;
+        // arrive; the barrier also guards the shared activation vector the next phase restages
         bar_consumers();
-        if (!sm.flag) return;
-        const Phase p = describe(a, ph, c.cta, c.ncta);
-        if (!c.dead) {
-            if (p.type == T_ATTN) {
-                if (a.kv_f32) attn_phase<G, float>(c, p);
-                else attn_phase<G, __nv_bfloat16>(c, p);
-            }
-            else if (p.i8) gemv_dispatch<true>(c, p);
-            else gemv_dispatch<false>(c, p);
-        }
-        __threadfence();
-        bar_consumers();
-        if (c.tid == 0) {
-            if (p.type == T_LMHEAD) {
+        if (tid == 0) {
+            if (type != T_LMHEAD) {
+                red_add(a.sync + ph, 1u);
+            } else {
                 unsigned long long b = 0;
                 for (int w = 0; w < kConsumerWarps; ++w) b = sm.best[w] > b ? sm.best[w] : b;
                 if (sm.bad) raise_error(a.flags, kErrNumerical, false);
-                if (b) atomicMax(a.key, b);
+                unsigned long long *key = a.key + (a.step & 1u);
+                if (b) atomicMax(key, b);
                 __threadfence();
-                const unsigned old = atomicAdd(&a.sync[ph], 1u);
-                if (old == (unsigned)(c.ncta - 1)) {
+                const unsigned old = atomicAdd(a.sync + ph, 1u);
+                if (old + 1u == a.target) {  // the last CTA of this step
                     __threadfence();
-                    const unsigned long long k = atomicAdd(a.key, 0ull);
+                    const unsigned long long k = atomicAdd(key, 0ull);
                     const int tok = k ? (int)(0xffffffffu - (unsigned)(k & 0xffffffffull)) : 0;
                     a.flags->next_tok = tok;
                     if (a.tok_out) *a.tok_out = tok;
+                    a.key[(a.step + 1u) & 1u] = 0ull;  // ready for the next step
                 }
-            } else {
-                red_release_add(&a.sync[ph], 1u);
             }
-        }
-        if (c.dead) {
-            if (c.lane == 0) raise_error(a.flags, kErrInvariant, true);
+            if (tr) tr[3] = gtime();
         }
     }
 }
 
 template <int G>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    Smem &sm = smem();
     if (threadIdx.x == 0) {
+        sm.args = a;
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
@@ -855,10 +1142,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     }
     __syncthreads();
     if (threadIdx.x >= kConsumerThreads) {
-        if (threadIdx.x == kConsumerThreads) producer(a, sm);
+        if (threadIdx.x == kConsumerThreads) producer();
         return;
     }
-    consumer<G>(a, sm);
+    consumer<G>();
 }
 
 __global__ void kv_widen_kernel(const __nv_bfloat16 *__restrict__ src, float *__restrict__ dst, long long heads,
@@ -888,7 +1175,7 @@ cudaError_t launch_kv_widen(const __nv_bfloat16 *src, float *dst, long long head
     return cudaGetLastError();
 }
 
-size_t decode_smem_bytes() { return sizeof(Smem) + 128; }
+size_t decode_smem_bytes() { return sizeof(Smem); }
 
 cudaError_t decode_prepare(int group, int *blocks_per_sm) {
     const int bytes = (int)decode_smem_bytes();

@@ -24,7 +24,8 @@ constexpr size_t kAlign = 256;
 constexpr int kPrefillRowsMax = 2048;
 
 struct Layout {
-    size_t kc, vc, rope, layers, x, qkv, o, act, part, logits, hidden, step, flags;
+    size_t kc, vc, rope, layers, xa, xb, qkvt, actt, partt, logits, hidden, step, flags, trace;
+    size_t tagged_begin, tagged_end;
     size_t prefill, prefill_bytes;
     size_t total;
 };
@@ -73,15 +74,18 @@ int make_layout(const qw_config *c, Layout *L) {
     L->vc = take(kv);
     L->rope = take((size_t)c->max_ctx * (c->head_dim / 2) * sizeof(float2));
     L->layers = take((size_t)c->n_layers * sizeof(qw::DevLayer));
-    L->x = take((size_t)c->hidden * 4);
-    L->qkv = take((size_t)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim * 4);
-    L->o = take((size_t)c->n_heads * c->head_dim * 4);
-    L->act = take((size_t)c->intermediate * 4);
-    L->part = take((size_t)kMaxCtas * g * qw::kPartStride * 4);
+    L->xa = take((size_t)c->hidden * 8);
+    L->tagged_begin = L->xa;
+    L->xb = take((size_t)c->hidden * 8);
+    L->qkvt = take((size_t)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim * 8);
+    L->actt = take((size_t)c->intermediate * 8);
+    L->partt = take((size_t)kMaxCtas * g * qw::kPartStride * 8);
+    L->tagged_end = off;
     L->logits = take((size_t)c->vocab * 4);
     L->hidden = take((size_t)(c->n_layers + 1) * c->hidden * 4);
-    L->step = take(qw::step_block_bytes(c->n_layers, c->n_kv_heads));
+    L->step = take(qw::step_block_bytes(c->n_layers));
     L->flags = take(sizeof(qw::StepFlags));
+    L->trace = take(((size_t)qw::kPhasesPerLayer * c->n_layers + 1) * kMaxCtas * qw::kTraceStamps * 8);
     const int rows = c->max_ctx < kPrefillRowsMax ? c->max_ctx : kPrefillRowsMax;
     L->prefill_bytes = qw::prefill_workspace_bytes(*c, rows);
     L->prefill = take(L->prefill_bytes);
@@ -109,6 +113,8 @@ struct qw_model {
     int has_last = 0;
     int debug = 0;
     int failed = 0;  // device error seen; cleared by qw_kv_reset
+    uint32_t step_seq = 0;  // decode steps launched so far (tags of step n use n * 512 + phase + 1)
+    uint32_t csteps = 0;    // steps since the arrival counters were last zeroed
     float *logits = nullptr;
     float *hidden = nullptr;
 };
@@ -128,8 +134,9 @@ int cuda_status(cudaError_t e) {
 
 bool aligned(const void *p, size_t a) { return p && ((uintptr_t)p % a) == 0; }
 
+// Attention splits per KV head: about 96 cached positions each, at most the CTAs per head.
 int split_for(const qw_model *m, int pos) {
-    int s = (pos + 127) / 128;
+    int s = (pos + 95) / 96;
     const int cap = m->ncta / m->cfg.n_kv_heads;
     if (s > cap) s = cap;
     if (s > pos) s = pos;
@@ -145,10 +152,19 @@ int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
     a.n_split = split_for(m, m->len);
     a.debug = m->debug;
     a.tok_out = tok_out_dev;
-    a.phase_begin = 0;
-    a.phase_end = qw::kPhasesPerLayer * m->cfg.n_layers + 1;
-    int rc = cuda_status(cudaMemsetAsync(m->step_block, 0, m->step_bytes, m->stream));
-    if (rc) return rc;
+    a.trace = (m->debug & QW_DEBUG_TRACE) ? (unsigned long long *)(m->ws + m->lay.trace) : nullptr;
+    m->step_seq += 1;
+    if (m->step_seq >= (1u << 23)) m->step_seq = 1;  // tag_base stays below 2^32
+    a.step = m->step_seq;
+    a.tag_base = m->step_seq * 512u;
+    int rc = QW_OK;
+    if ((uint64_t)(m->csteps + 1) * (uint64_t)m->ncta >= 0xffffffffull) {  // counters would overflow
+        rc = cuda_status(cudaMemsetAsync(m->step_block, 0, m->step_bytes, m->stream));
+        if (rc) return rc;
+        m->csteps = 0;
+    }
+    m->csteps += 1;
+    a.target = m->csteps * (uint32_t)m->ncta;
     rc = cuda_status(qw::launch_decode(a, m->group, m->ncta, m->stream));
     if (rc) return rc;
     m->len += 1;
@@ -260,6 +276,7 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
         return QW_CUDA_ERROR;
     }
     const int ncta = nsm < kMaxCtas ? nsm : kMaxCtas;
+    if ((cfg->hidden + ncta - 1) / ncta > qw::kMaxOwnRows) return QW_UNSUPPORTED_SHAPE;
     rc = cuda_status(qw::prefill_prepare());
     if (rc) return rc;
 
@@ -291,7 +308,9 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
         rc = cuda_status(cudaMemcpyAsync(ws + L.layers, host_layers.data(), host_layers.size() * sizeof(qw::DevLayer),
                                          cudaMemcpyHostToDevice, m->stream));
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.flags, 0, sizeof(qw::StepFlags), m->stream));
-    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, qw::step_block_bytes(cfg->n_layers, cfg->n_kv_heads), m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, qw::step_block_bytes(cfg->n_layers), m->stream));
+    // tagged exchange words start with tag 0, which no step ever uses
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.tagged_begin, 0, L.tagged_end - L.tagged_begin, m->stream));
     if (!rc) rc = cuda_status(cudaStreamSynchronize(m->stream));  // host staging buffers go out of scope
     if (rc) {
         delete m;
@@ -316,20 +335,19 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     a.vc = ws + L.vc;
     a.kv_f32 = cfg->kv_format == QW_KV_F32 ? 1 : 0;
     a.rope = (const float2 *)(ws + L.rope);
-    a.x = (float *)(ws + L.x);
-    a.qkv = (float *)(ws + L.qkv);
-    a.o = (float *)(ws + L.o);
-    a.act = (float *)(ws + L.act);
-    a.part = (float *)(ws + L.part);
+    a.xa = (unsigned long long *)(ws + L.xa);
+    a.xb = (unsigned long long *)(ws + L.xb);
+    a.qkvt = (unsigned long long *)(ws + L.qkvt);
+    a.actt = (unsigned long long *)(ws + L.actt);
+    a.partt = (unsigned long long *)(ws + L.partt);
     a.logits = (float *)(ws + L.logits);
     a.hidden = (float *)(ws + L.hidden);
-    a.sync = (unsigned *)(ws + L.step);
-    const size_t counters = (size_t)qw::kPhasesPerLayer * cfg->n_layers + 1 + (size_t)cfg->n_layers * cfg->n_kv_heads;
-    a.key = (unsigned long long *)(ws + L.step + ((counters * 4 + 7) / 8) * 8);
+    a.key = (unsigned long long *)(ws + L.step);
+    a.sync = (unsigned *)(ws + L.step + 16);
     a.flags = (qw::StepFlags *)(ws + L.flags);
     m->flags = a.flags;
     m->step_block = ws + L.step;
-    m->step_bytes = qw::step_block_bytes(cfg->n_layers, cfg->n_kv_heads);
+    m->step_bytes = qw::step_block_bytes(cfg->n_layers);
     m->logits = a.logits;
     m->hidden = a.hidden;
     qw::prefill_init(&m->pf, a, ws + L.prefill, L.prefill_bytes,
@@ -414,6 +432,9 @@ int qw_kv_reset(qw_model *m) {
     m->len = 0;
     m->has_last = 0;
     m->failed = 0;
+    m->csteps = 0;
+    int rc = cuda_status(cudaMemsetAsync(m->step_block, 0, m->step_bytes, m->stream));
+    if (rc) return rc;
     return cuda_status(cudaMemsetAsync(m->flags, 0, sizeof(qw::StepFlags), m->stream));
 }
 
@@ -479,7 +500,7 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos) {
 
 int qw_set_debug(qw_model *m, int32_t flags) {
     if (!live(m)) return QW_INVALID_HANDLE;
-    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN)) return QW_INVALID_ARGUMENT;
+    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN | QW_DEBUG_TRACE)) return QW_INVALID_ARGUMENT;
     m->debug = flags;
     return QW_OK;
 }
@@ -488,6 +509,27 @@ int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n) {
     if (!live(m)) return QW_INVALID_HANDLE;
     if (!dst_dev || n != (int64_t)(m->cfg.n_layers + 1) * m->cfg.hidden) return QW_INVALID_ARGUMENT;
     return cuda_status(cudaMemcpyAsync(dst_dev, m->hidden, (size_t)n * 4, cudaMemcpyDeviceToDevice, m->stream));
+}
+
+int qw_query(const qw_model *m, int32_t what, int64_t *out) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (!out) return QW_INVALID_ARGUMENT;
+    switch (what) {
+        case QW_QUERY_DECODE_CTAS: *out = m->ncta; return QW_OK;
+        case QW_QUERY_TRACE_LEN:
+            *out = ((int64_t)qw::kPhasesPerLayer * m->cfg.n_layers + 1) * m->ncta * qw::kTraceStamps;
+            return QW_OK;
+        case QW_QUERY_WORKSPACE_BYTES: *out = (int64_t)m->lay.total; return QW_OK;
+        default: return QW_INVALID_ARGUMENT;
+    }
+}
+
+int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    const int64_t len = ((int64_t)qw::kPhasesPerLayer * m->cfg.n_layers + 1) * m->ncta * qw::kTraceStamps;
+    if (!dst_dev || n != len) return QW_INVALID_ARGUMENT;
+    return cuda_status(cudaMemcpyAsync(dst_dev, m->ws + m->lay.trace, (size_t)n * 8, cudaMemcpyDeviceToDevice,
+                                       m->stream));
 }
 
 }  // extern "C"

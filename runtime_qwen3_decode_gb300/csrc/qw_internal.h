@@ -14,14 +14,23 @@ constexpr int kMaxLayers = 64;
 constexpr int kPhasesPerLayer = 5;  // QKV, ATTN, OPROJ, GATEUP, DOWN; then one LMHEAD phase per step
 enum { PH_QKV = 0, PH_ATTN = 1, PH_OPROJ = 2, PH_GATEUP = 3, PH_DOWN = 4 };
 
-// Persistent decode kernel geometry: 8 consumer warps + 1 producer warp per CTA,
-// one CTA per SM, a ring of shared-memory slots filled by bulk async copies.
-constexpr int kConsumerWarps = 8;
+// Persistent decode kernel geometry: 7 consumer warps + 1 producer warp per CTA (8
+// warps: two per SM sub-partition, so a thread may use up to 255 registers), one CTA
+// per SM, a ring of shared-memory slots filled by bulk async copies.
+constexpr int kConsumerWarps = 7;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kDecodeThreads = kConsumerThreads + 32;
 constexpr int kSlotBytes = 32768;
 constexpr int kSlots = 6;
-constexpr int kPartStride = kHeadDim + 2;    // split-attention partial: acc[128], max, sum
+// Cached positions per attention slot: one pass of 4 positions per consumer warp for
+// f32 rows (512 B), two passes for bf16 rows; K rows then V rows at half the slot.
+__host__ __device__ constexpr int kv_chunk_rows(int elem_bytes) { return 4 * kConsumerWarps * (4 / elem_bytes); }
+constexpr int kPartStride = kHeadDim + 4;    // split-attention partial: acc[128], max, sum, 2 pad (16-B rows)
+constexpr int kMaxOwnRows = 64;             // residual rows per CTA kept in shared memory
+
+// Debug timeline stamps per (phase, CTA): consumer before wait, after wait, after
+// compute, after arrive; producer first issue, last issue of the phase.
+constexpr int kTraceStamps = 8;
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // every device-side wait gives up after 1 s
 
@@ -57,27 +66,29 @@ struct DecodeArgs {
     void *kc, *vc;                   // [L][Hkv][max_ctx][128] of f32 (kv_f32) or bf16
     int kv_f32;
     const float2 *rope;              // [max_ctx][64] (cos, sin)
-    float *x;                        // residual [H]
-    float *qkv;                      // [(Hq + 2 Hkv) * 128]
-    float *o;                        // attention output [Hq * 128]
-    float *act;                      // SwiGLU output [I]
-    float *part;                     // split partials [Hkv][S][G][kPartStride]
+    // tagged exchange words (tag << 32 | f32 bits) between phases
+    unsigned long long *xa;          // residual after down [H]
+    unsigned long long *xb;          // residual after o_proj [H]
+    unsigned long long *qkvt;        // [(Hq + 2 Hkv) * 128]
+    unsigned long long *actt;        // SwiGLU output [I]
+    unsigned long long *partt;       // split-attention partials [Hkv][S][G][kPartStride]
     float *logits;                   // [V]
     float *hidden;                   // [(L + 1) H] debug dump
-    unsigned *sync;                  // per-step counters: phases [5L+1], attention merges [L*Hkv], zeroed per step
-    unsigned long long *key;         // packed argmax key, zeroed per step
+    unsigned *sync;                  // arrivals per phase [5L+1]; each step adds the CTA count
+    unsigned target;                 // arrivals that mean "this step's phase is done" (steps * CTAs)
+    unsigned long long *key;         // packed argmax keys [2], one per step parity
     StepFlags *flags;
     int *tok_out;                    // optional device slot for this step's greedy pick
+    unsigned long long *trace;       // debug timeline [phase][cta][kTraceStamps] (%globaltimer ns) or null
     // step
     int pos, token, n_split, debug;
-    int phase_begin, phase_end;
+    unsigned step;                   // step sequence number (never 0 after creation)
+    unsigned tag_base;               // step * 512: tags of this step are tag_base + phase + 1
 };
 
-// Size of the per-step bookkeeping block (counters + key), zeroed before each decode step.
-inline size_t step_block_bytes(int L, int Hkv) {
-    size_t counters = (size_t)kPhasesPerLayer * L + 1 + (size_t)L * Hkv;
-    return ((counters * 4 + 7) / 8) * 8 + 8;
-}
+// Step bookkeeping: two argmax keys then the per-phase arrival counters (zeroed at
+// creation, by qw_kv_reset and when the counters would overflow).
+inline size_t step_block_bytes(int L) { return 16 + 4 * ((size_t)kPhasesPerLayer * L + 1); }
 
 size_t decode_smem_bytes();
 cudaError_t decode_prepare(int group, int *blocks_per_sm);

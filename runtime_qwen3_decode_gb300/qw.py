@@ -35,12 +35,16 @@ KV_F32 = 0
 KV_BF16 = 1
 DEBUG_HIDDEN = 1
 DEBUG_PREFILL_BY_TOKEN = 2
+DEBUG_TRACE = 4
+QUERY_DECODE_CTAS = 1
+QUERY_TRACE_LEN = 2
+QUERY_WORKSPACE_BYTES = 3
 MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 
 # every symbol include/qw.h declares
 EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_step", "qw_generate", "qw_logits",
            "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
-           "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version")
+           "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query")
 
 
 class QwError(RuntimeError):
@@ -97,6 +101,8 @@ def _lib():
             L.qw_kv_export.argtypes = [vp, vp, vp, i32]
             L.qw_set_debug.argtypes = [vp, i32]
             L.qw_debug_hidden.argtypes = [vp, vp, i64]
+            L.qw_debug_trace.argtypes = [vp, vp, i64]
+            L.qw_query.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -257,6 +263,20 @@ class Model:
 
     def set_debug(self, flags: int):
         _check(_lib().qw_set_debug(self._h, int(flags)), "qw_set_debug")
+
+    def query(self, what: int) -> int:
+        v = ctypes.c_int64(-1)
+        _check(_lib().qw_query(self._h, int(what), ctypes.byref(v)), "qw_query")
+        return int(v.value)
+
+    def debug_trace(self):
+        """[phase, cta, 8] uint64 ns timeline of the last decode step (needs DEBUG_TRACE)."""
+        import torch
+        n = self.query(QUERY_TRACE_LEN)
+        ncta = self.query(QUERY_DECODE_CTAS)
+        out = torch.zeros(n, dtype=torch.int64, device="cuda")
+        _check(_lib().qw_debug_trace(self._h, out.data_ptr(), n), "qw_debug_trace")
+        return out.view(-1, ncta, 8)
 
     def debug_hidden(self):
         import torch
