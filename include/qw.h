@@ -236,6 +236,30 @@ int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n);
 enum { QW_QUERY_DECODE_CTAS = 1, QW_QUERY_TRACE_LEN = 2, QW_QUERY_WORKSPACE_BYTES = 3 };
 int qw_query(const qw_model *m, int32_t what, int64_t *out);
 
+/*
+ * One decode step with no device allocation (the reference pages have no
+ * counterpart; this entry point exists for callers that cannot allocate device
+ * memory when they decode, e.g. code running inside another framework's memory
+ * pool or under a fixed memory budget, where a cudaMalloc would fail or stall the
+ * device).  No handle and no workspace: the caller passes the config, the weight
+ * table, the K/V cache planes (device, [n_layers][n_kv_heads][max_ctx][head_dim]
+ * in cfg->kv_format; rows [0, pos) hold earlier positions, row pos is written),
+ * the position pos, the input token id, and device outputs logits_dev (f32
+ * [vocab]) and next_token_dev (int32, the greedy pick).  Every other buffer lives
+ * in one fixed 1 MiB array in the library's device memory, which holds configs of
+ * up to 64 layers on GPUs of up to 256 SMs; larger needs return QW_OUT_OF_MEMORY
+ * with a message on stderr.  The library calls no allocating routine here.
+ * The first call on a device sets the array up (looks up its device address and
+ * zeroes it) and must come before any stream capture.  The array is shared by all
+ * calls on a device and keeps the last call's contents (counters and flags are
+ * zeroed by every call), so calls that overlap on the GPU race: serialise them.
+ * The call waits for the stream after copying the layer table and the RoPE row;
+ * with wait != 0 it also waits for the step and returns any device-side error.
+ */
+int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *weights, void *k_cache, void *v_cache,
+                           int32_t pos, int32_t token, float *logits_dev, int32_t *next_token_dev,
+                           void *cuda_stream, int32_t wait);
+
 /* Static text for a status code. */
 const char *qw_status_string(int status);
 

@@ -1,0 +1,246 @@
+// noalloc.cu - one decode step that needs no device allocation at all.
+//
+// Some callers cannot allocate device memory when they want to decode: code that
+// runs inside another framework's memory pool or a fixed memory budget, or a host
+// that must not call cudaMalloc after start-up (its allocations would
+// synchronise the device or fail under a cap).  qw_decode_step_noalloc serves them: the
+// caller passes the weights, the K/V cache, the input token and the output
+// buffers, and every other buffer the decode kernel needs (the tagged exchange
+// words between phases, split-attention partials, arrival counters, argmax keys,
+// the layer pointer table and this position's RoPE row) lives in one file-scope
+// device array of fixed size, kScratchBytes.  The kernel itself is the unchanged
+// decode kernel of decode.cu.
+//
+// The array is shared by every call in the process on a given device and keeps the
+// last call's contents, so calls whose work overlaps on the GPU (different streams,
+// or other threads) race on it and must be serialised by the caller.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "qw.h"
+#include "qw_internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = 1u << 20;  // 1 MiB per device
+constexpr int kMaxDevices = 64;
+constexpr int kMaxNoallocCtas = 256;
+
+// Scratch regions (bytes, 256-aligned offsets inside the array)
+constexpr size_t kOffFlags = 0;         // StepFlags
+constexpr size_t kOffStep = 256;        // argmax keys [2] + arrival counters [5 L + 1]
+constexpr size_t kOffLayers = 2048;     // DevLayer [n_layers]
+constexpr size_t kOffRope = 12288;      // float2 [head_dim / 2], this call's position
+constexpr size_t kOffTagged = 16384;    // tagged words: xa, xb, qkvt, actt, partt
+
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void *g_ptr[kMaxDevices];        // device address of g_scratch, per device (set-up done when non-null)
+uint32_t g_seq[kMaxDevices];     // tag sequence of the last call on each device
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct TaggedLayout {
+    size_t xa, xb, qkvt, actt, partt, end;
+};
+
+TaggedLayout tagged_layout(const qw_config &c, int ncta) {
+    TaggedLayout t;
+    const int g = c.n_heads / c.n_kv_heads;
+    size_t off = kOffTagged;
+    t.xa = off;
+    off += align256((size_t)c.hidden * 8);
+    t.xb = off;
+    off += align256((size_t)c.hidden * 8);
+    t.qkvt = off;
+    off += align256((size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim * 8);
+    t.actt = off;
+    off += align256((size_t)c.intermediate * 8);
+    t.partt = off;
+    off += align256((size_t)ncta * g * qw::kPartStride * 8);
+    t.end = off;
+    return t;
+}
+
+int cuda_rc(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return QW_OK;
+    fprintf(stderr, "qw_decode_step_noalloc: %s failed: %s\n", what, cudaGetErrorString(e));
+    return QW_CUDA_ERROR;
+}
+
+bool aligned16(const void *p) { return p && ((uintptr_t)p % 16) == 0; }
+
+}  // namespace
+
+extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w, void *k_cache, void *v_cache,
+                                      int32_t pos, int32_t token, float *logits_dev, int32_t *next_token_dev,
+                                      void *cuda_stream, int32_t wait) {
+    // configuration and arguments, checked before anything touches the device
+    if (!cfg || !w || !w->layers || !k_cache || !v_cache || !logits_dev || !next_token_dev) return QW_INVALID_ARGUMENT;
+    if (qw_workspace_bytes(cfg) == 0) return QW_UNSUPPORTED_SHAPE;  // same validation as qw_model_create
+    if (token < 0 || token >= cfg->vocab) return QW_INVALID_ARGUMENT;
+    if (pos < 0) return QW_INVALID_ARGUMENT;
+    if (pos >= cfg->max_ctx) return QW_CONTEXT_EXCEEDED;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(logits_dev) || ((uintptr_t)next_token_dev % 4))
+        return QW_ALIGNMENT;
+    const bool i8 = cfg->weight_format == QW_W_INT8_G32;
+    if (!aligned16(w->embed) || !aligned16(w->final_norm) || (w->lm_head && !aligned16(w->lm_head)))
+        return QW_ALIGNMENT;
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const qw_layer_weights &lw = w->layers[l];
+        const void *norms[4] = {lw.input_norm, lw.q_norm, lw.k_norm, lw.post_norm};
+        for (const void *p : norms)
+            if (!aligned16(p)) return p ? QW_ALIGNMENT : QW_INVALID_ARGUMENT;
+        for (int i = 0; i < 7; ++i) {
+            if (!lw.w[i] || (i8 && !lw.s[i])) return QW_INVALID_ARGUMENT;
+            if (!aligned16(lw.w[i]) || (i8 && !aligned16(lw.s[i]))) return QW_ALIGNMENT;
+        }
+    }
+
+    int dev = 0, major = 0, minor = 0, nsm = 0;
+    int rc = cuda_rc(cudaGetDevice(&dev), "cudaGetDevice");
+    if (rc) return rc;
+    if (dev < 0 || dev >= kMaxDevices) return QW_INVALID_ARGUMENT;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) {
+        fprintf(stderr, "qw_decode_step_noalloc: device compute capability %d.%d; built for sm_103a only\n", major, minor);
+        return QW_CUDA_ERROR;
+    }
+    const int ncta = nsm;
+    const int group = cfg->n_heads / cfg->n_kv_heads;
+
+    // everything must fit the fixed array; say so plainly when it does not
+    const TaggedLayout t = tagged_layout(*cfg, ncta);
+    const size_t step_bytes = 16 + 4 * ((size_t)qw::kPhasesPerLayer * cfg->n_layers + 1);
+    if (ncta > kMaxNoallocCtas || t.end > kScratchBytes || kOffStep + step_bytes > kOffLayers ||
+        kOffLayers + (size_t)cfg->n_layers * sizeof(qw::DevLayer) > kOffRope ||
+        kOffRope + (size_t)cfg->head_dim / 2 * sizeof(float2) > kOffTagged ||
+        (cfg->hidden + ncta - 1) / ncta > qw::kMaxOwnRows) {
+        fprintf(stderr,
+                "qw_decode_step_noalloc: this config needs %zu bytes of fixed scratch (%d CTAs); the static array "
+                "holds %zu bytes for at most %d CTAs\n",
+                t.end, ncta, kScratchBytes, kMaxNoallocCtas);
+        return QW_OUT_OF_MEMORY;
+    }
+
+    cudaStream_t stream = (cudaStream_t)cuda_stream;
+    int bps = 0;
+    rc = cuda_rc(qw::decode_prepare(group, &bps), "decode_prepare");  // shared-memory attribute of the kernel
+    if (rc) return rc;
+    if (bps < 1) return QW_CUDA_ERROR;
+    unsigned char *base = nullptr;
+    uint32_t seq = 0;
+    {
+        std::lock_guard<std::mutex> g(g_mu);
+        if (!g_ptr[dev]) {
+            // Once per device, with that device current: find the array's device
+            // address (in host code g_scratch is only a stand-in symbol, not an address
+            // the GPU can use) and zero the array.  This first call on a device therefore
+            // enqueues a memset and must come before any stream capture.
+            void *p = nullptr;
+            rc = cuda_rc(cudaGetSymbolAddress(&p, g_scratch), "cudaGetSymbolAddress");
+            if (rc) return rc;
+            rc = cuda_rc(cudaMemsetAsync(p, 0, kScratchBytes, stream), "cudaMemsetAsync");
+            if (rc) return rc;
+            g_ptr[dev] = p;
+            g_seq[dev] = 0;
+        }
+        base = (unsigned char *)g_ptr[dev];
+        g_seq[dev] += 1;
+        if (g_seq[dev] >= (1u << 23)) g_seq[dev] = 1;
+        seq = g_seq[dev];
+    }
+    if (seq == 1) {
+        // tags restart: clear the tagged words so no stale word carries a live tag
+        rc = cuda_rc(cudaMemsetAsync(base + kOffTagged, 0, kScratchBytes - kOffTagged, stream), "cudaMemsetAsync");
+        if (rc) return rc;
+    }
+
+    // per call: the layer pointer table and this position's RoPE row (both copied from
+    // host memory into the array), and zeroed flags, keys and arrival counters
+    std::vector<qw::DevLayer> layers((size_t)cfg->n_layers);
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const qw_layer_weights &lw = w->layers[l];
+        qw::DevLayer &d = layers[(size_t)l];
+        d.input_norm = (const __nv_bfloat16 *)lw.input_norm;
+        d.q_norm = (const __nv_bfloat16 *)lw.q_norm;
+        d.k_norm = (const __nv_bfloat16 *)lw.k_norm;
+        d.post_norm = (const __nv_bfloat16 *)lw.post_norm;
+        for (int i = 0; i < 7; ++i) {
+            d.w[i] = lw.w[i];
+            d.s[i] = i8 ? (const __half *)lw.s[i] : nullptr;
+        }
+    }
+    const int half = cfg->head_dim / 2;
+    std::vector<float2> rope((size_t)half);
+    for (int i = 0; i < half; ++i) {
+        const double ang = (double)pos * std::pow(cfg->rope_theta, -2.0 * i / (double)cfg->head_dim);
+        rope[(size_t)i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+    rc = cuda_rc(cudaMemcpyAsync(base + kOffLayers, layers.data(), layers.size() * sizeof(qw::DevLayer),
+                                 cudaMemcpyHostToDevice, stream), "cudaMemcpyAsync");
+    if (!rc)
+        rc = cuda_rc(cudaMemcpyAsync(base + kOffRope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                                     stream), "cudaMemcpyAsync");
+    if (!rc) rc = cuda_rc(cudaMemsetAsync(base + kOffFlags, 0, kOffLayers, stream), "cudaMemsetAsync");
+    if (rc) return rc;
+    // the two host sources are locals of this call: wait until the copies have run
+    rc = cuda_rc(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+    if (rc) return rc;
+
+    qw::DecodeArgs a{};
+    a.L = cfg->n_layers;
+    a.H = cfg->hidden;
+    a.Hq = cfg->n_heads;
+    a.Hkv = cfg->n_kv_heads;
+    a.I = cfg->intermediate;
+    a.V = cfg->vocab;
+    a.max_ctx = cfg->max_ctx;
+    a.fmt = cfg->weight_format;
+    a.eps = cfg->rms_eps;
+    a.layers = (const qw::DevLayer *)(base + kOffLayers);
+    a.embed = (const __nv_bfloat16 *)w->embed;
+    a.lm_head = (const __nv_bfloat16 *)(w->lm_head ? w->lm_head : w->embed);
+    a.final_norm = (const __nv_bfloat16 *)w->final_norm;
+    a.kc = k_cache;
+    a.vc = v_cache;
+    a.kv_f32 = cfg->kv_format == QW_KV_F32 ? 1 : 0;
+    // the kernel reads row `pos` of a [max_ctx][head_dim/2] table; point that row at the copy
+    a.rope = (const float2 *)((uintptr_t)(base + kOffRope) - (uintptr_t)pos * half * sizeof(float2));
+    a.xa = (unsigned long long *)(base + t.xa);
+    a.xb = (unsigned long long *)(base + t.xb);
+    a.qkvt = (unsigned long long *)(base + t.qkvt);
+    a.actt = (unsigned long long *)(base + t.actt);
+    a.partt = (unsigned long long *)(base + t.partt);
+    a.logits = logits_dev;
+    a.hidden = nullptr;
+    a.key = (unsigned long long *)(base + kOffStep);
+    a.sync = (unsigned *)(base + kOffStep + 16);
+    a.flags = (qw::StepFlags *)(base + kOffFlags);
+    a.tok_out = next_token_dev;
+    a.trace = nullptr;
+    a.pos = pos;
+    a.token = token;
+    int s = (pos + 95) / 96;
+    if (s > ncta / cfg->n_kv_heads) s = ncta / cfg->n_kv_heads;
+    if (s > pos) s = pos;
+    if (s < 1) s = 1;
+    a.n_split = s;
+    a.debug = 0;
+    a.step = 1;          // counters and keys were zeroed for this call
+    a.target = (unsigned)ncta;
+    a.tag_base = seq * 512u;
+    rc = cuda_rc(qw::launch_decode(a, group, ncta, stream), "decode launch");
+    if (rc || !wait) return rc;
+    qw::StepFlags f;
+    rc = cuda_rc(cudaMemcpyAsync(&f, base + kOffFlags, sizeof(f), cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync");
+    if (!rc) rc = cuda_rc(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+    if (rc) return rc;
+    return f.err ? (int)f.err : QW_OK;
+}

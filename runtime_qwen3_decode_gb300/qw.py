@@ -44,7 +44,8 @@ MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 # every symbol include/qw.h declares
 EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_step", "qw_generate", "qw_logits",
            "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
-           "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query")
+           "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query",
+           "qw_decode_step_noalloc")
 
 
 class QwError(RuntimeError):
@@ -103,6 +104,8 @@ def _lib():
             L.qw_debug_hidden.argtypes = [vp, vp, i64]
             L.qw_debug_trace.argtypes = [vp, vp, i64]
             L.qw_query.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
+            L.qw_decode_step_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, i32, i32, vp,
+                                                 vp, vp, i32]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -157,6 +160,37 @@ def weights_to_device(host_weights: dict, int8: bool, device="cuda"):
                 d[m] = dev(lw[m])
         out["layers"].append(d)
     return out
+
+
+def weight_table(dev_weights: dict, int8: bool):
+    """(Weights struct, layer array) for device weights from ``weights_to_device``; keep both alive."""
+    n = len(dev_weights["layers"])
+    layers = (LayerWeights * n)()
+    for l, lw in enumerate(dev_weights["layers"]):
+        L = layers[l]
+        L.input_norm = lw["input_norm"].data_ptr()
+        L.q_norm = lw["q_norm"].data_ptr()
+        L.k_norm = lw["k_norm"].data_ptr()
+        L.post_norm = lw["post_norm"].data_ptr()
+        for j, m in enumerate(MATRICES):
+            if int8:
+                L.w[j] = lw[m + "_q8"].data_ptr()
+                L.s[j] = lw[m + "_s"].data_ptr()
+            else:
+                L.w[j] = lw[m].data_ptr()
+    w = Weights(dev_weights["embed"].data_ptr(), dev_weights["final_norm"].data_ptr(), None, layers)
+    return w, layers
+
+
+def decode_step_noalloc(cfg: Config, dev_weights: dict, k_cache, v_cache, pos: int, token: int, logits_out,
+                        next_token_out, stream=None, wait: bool = True):
+    """qw_decode_step_noalloc: one step over caller-owned K/V planes; no device allocation."""
+    import torch
+    w, layers = weight_table(dev_weights, cfg.weight_format == W_INT8_G32)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(_lib().qw_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         int(pos), int(token), logits_out.data_ptr(), next_token_out.data_ptr(),
+                                         st.cuda_stream, 1 if wait else 0), "qw_decode_step_noalloc")
 
 
 class Model:
