@@ -129,6 +129,26 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense 16-bit tensor-core peak in TFLOP/s (burst: the prefill is timed on its own).
+    fp16 and bf16 share kind::f16 and its nominal rate, so the bf16 figure applies."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured bf16 burst (fp16 runs at the same nominal rate)"
+    return 1900.0, "fallback"
+
+
+def prefill_flops(wl, T: int) -> int:
+    """Algorithmic flops of a T-row prefill: the projections and MLP of every row, the
+    causal QK^T and PV over non-masked (query, key) pairs, and the head of the last row."""
+    H, d, Hq, Hkv, I, V = wl.hidden, wl.head_dim, wl.n_heads, wl.n_kv_heads, wl.intermediate, wl.vocab
+    per_layer = Hq * d * H + 2 * Hkv * d * H + H * Hq * d + 3 * I * H
+    gemm = 2 * T * wl.n_layers * per_layer
+    attn = wl.n_layers * 4 * Hq * d * (T * (T + 1) // 2)
+    return gemm + attn + 2 * V * H
+
+
 def kernel_traffic():
     """Per-launch DRAM bytes from the committed ncu capture, if the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
@@ -192,6 +212,55 @@ def run_reference(args, wl):
     return 0
 
 
+def measure_prefill(qw, wl, reps: int, warmup: int, gpu: int):
+    """Batched prefill of the workload's whole prompt: median device time over reps
+    (CUDA events on the model's stream, after warm-up), plus one host-synchronous call."""
+    import torch
+
+    host = qi.make_weights(wl)
+    dev = qw.weights_to_device(host, int8=wl.weight_format == "int8_g32")
+    prompt = qi.prompt(wl)
+    T = len(prompt)
+    model = qw.Model(wl, dev, max_ctx=T + 1)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        model.kv_reset()
+        model.prefill(prompt, want_token=False)
+    model.sync()
+    clocks = ClockSampler(gpu)
+    clocks.start()
+    times = []
+    for _ in range(reps):
+        model.kv_reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        model.prefill(prompt, want_token=False)
+        e1.record(stream)
+        model.sync()
+        times.append(e0.elapsed_time(e1))
+    clk = clocks.stop()
+    model.kv_reset()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    model.prefill(prompt)  # host token ids in, greedy pick back to the host
+    e2e_s = time.perf_counter() - t
+    model.close()
+    del dev
+    ms = statistics.median(times)
+    flops = prefill_flops(wl, T)
+    tf = flops / (ms / 1e3) / 1e12
+    peak, kind = measured_tensor_peak()
+    return {"workload": wl.name, "tokens": T, "ms": ms, "ms_all": times, "tokens_per_s": T / (ms / 1e3),
+            "dtype": "fp16 operands, f32 accumulation (tcgen05 kind::f16)",
+            "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": kind, "traffic": None,
+                         "note": "whole prefill (GEMMs, attention, row kernels, head) against the GEMM peak"},
+            "e2e": {"value": T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T, "d2h_bytes_per_step": 16,
+                    "how": "qw_prefill(tokens_host, &next_token_host), host-synchronous"},
+            "clocks": clk}
+
+
 def run_ours(args, wl):
     import torch
 
@@ -209,44 +278,50 @@ def run_ours(args, wl):
     prompt = qi.prompt(wl)
     W, K = args.warmup, args.steps
     per_seq = wl.decode_steps
-    max_ctx = wl.prompt_len + max(per_seq, min(W + K, per_seq)) + 1
+    n0 = wl.kv_prefill + wl.prompt_len  # positions in the cache when decoding starts
+    max_ctx = n0 + per_seq + 1
     model = qw.Model(wl, dev, max_ctx=max_ctx)
     stream = torch.cuda.current_stream()
+    if wl.kv_prefill:
+        kh, vh = qi.kv_fill(wl, wl.kv_prefill)
+        kd = torch.from_numpy(kh.view(np.int16)).cuda()
+        vd = torch.from_numpy(vh.view(np.int16)).cuda()
+        del kh, vh
+
+    def start_sequence():
+        """Fresh cache for a new sequence; returns the first decode input (-1: the prefill's pick)."""
+        model.kv_reset()
+        if wl.kv_prefill:
+            model.kv_import(kd, vd, wl.kv_prefill)
+        if wl.prompt_len:
+            model.prefill(prompt, want_token=False)
+            return -1
+        return qi.first_decode_token(wl)
 
     def barrier():
         if ws > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # prefill of the workload's prompt (timed on its own, reported beside the headline)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    model.prefill(prompt, want_token=False)  # warm
-    model.kv_reset()
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    model.prefill(prompt, want_token=False)
-    ev1.record(stream)
-    model.sync()
-    prefill_ms = ev0.elapsed_time(ev1)
-
     # decode: W warm-up tokens, then exactly K timed tokens; a new sequence starts (reset +
-    # prefill, inside the timed region) whenever the workload's decode budget is used up
+    # prefill or K/V import, inside the timed region) whenever the decode budget is used up
     toks = torch.zeros(max(K, 1), dtype=torch.int32, device="cuda")
     positions = []
+    next_in = start_sequence()
     done_in_seq = 0
 
     def run_tokens(n, out=None, record=False):
-        nonlocal done_in_seq
+        nonlocal done_in_seq, next_in
         i = 0
         while i < n:
             if done_in_seq == per_seq:
-                model.kv_reset()
-                model.prefill(prompt, want_token=False)
+                next_in = start_sequence()
                 done_in_seq = 0
             m = min(n - i, per_seq - done_in_seq)
             if record:
                 positions.extend(range(model.kv_length, model.kv_length + m))
-            model.generate(m, -1, out[i:i + m] if out is not None else None)
+            model.generate(m, next_in, out[i:i + m] if out is not None else None)
+            next_in = -1
             done_in_seq += m
             i += m
 
@@ -275,7 +350,11 @@ def run_ours(args, wl):
 
     # end to end through the public call: host token in, host token out, every step
     model.kv_reset()
-    tok = model.prefill(prompt)
+    tok = qi.first_decode_token(wl)
+    if wl.kv_prefill:
+        model.kv_import(kd, vd, wl.kv_prefill)
+    if wl.prompt_len:
+        tok = model.prefill(prompt)
     n_e2e = min(K, per_seq)
     torch.cuda.synchronize()
     t_e = time.perf_counter()
@@ -311,14 +390,18 @@ def run_ours(args, wl):
                 "how": "qw_decode_step(token_from_host, &next_token_host) per token, host-synchronous"},
         "gpu_launches": K,
         "clocks": clk,
-        "prefill": {"tokens": wl.prompt_len, "ms": prefill_ms, "tokens_per_s": wl.prompt_len / (prefill_ms / 1e3)},
     }
     model.close()
+    if wl.kv_prefill:
+        del kd, vd
+    if not args.no_prefill:
+        line["prefill"] = measure_prefill(qw, qi.WORKLOADS[args.prefill_workload], args.prefill_reps,
+                                          max(3, min(W, 5)), local)
     if not args.no_cpu_baseline and ws == 1:
         n = args.cpu_steps
-        rate, dt, cores = oracle_decode_rate(wl, host, wl.prompt_len, n)
+        rate, dt, cores = oracle_decode_rate(wl, host, n0, n)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{n} oracle decode steps after a {wl.prompt_len}-position synthetic "
+                                "sample": f"{n} oracle decode steps after a {n0}-position synthetic "
                                           f"K/V import, full shape ({dt:.1f} s of CPU)"}
     print(json.dumps(line), flush=True)
     return 0
@@ -327,16 +410,22 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=376)
+    ap.add_argument("--steps", type=int, default=None, help="timed decode tokens (default: the workload's "
+                    "decode budget minus the warm-up)")
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_decode", choices=sorted(qi.WORKLOADS))
     ap.add_argument("--cpu-steps", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-workload", default="qwen3_0p6b_prefill2048", choices=sorted(qi.WORKLOADS))
+    ap.add_argument("--prefill-reps", type=int, default=5)
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = qi.WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = max(1, wl.decode_steps - args.warmup)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -163,6 +163,12 @@ int qw_model_create(const qw_config *cfg, const qw_weights *weights, void *works
  * token that qw_decode_step(-1) consumes).  If next_token_host is not NULL the
  * call waits and writes the greedy pick there.  n == 0 is a no-op.
  * QW_CONTEXT_EXCEEDED if len + n > max_ctx, with nothing changed.
+ * The prompt runs in chunks of up to 2048 rows through tensor-core GEMMs and a
+ * causal tensor-core attention ("Portable WebAssembly Runtime Architecture for
+ * TinyRustLM", section "Prefill versus decode"), with fp16 operands and f32
+ * accumulation; the weights were converted to fp16 in the workspace at creation.
+ * If a weight does not fit fp16 the model falls back to the decode path, one
+ * token at a time (a message on stderr says so).
  */
 int qw_prefill(qw_model *m, const int32_t *tokens_host, int32_t n, int32_t *next_token_host);
 
@@ -220,7 +226,10 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos);
 enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2, QW_DEBUG_TRACE = 4 };
 int qw_set_debug(qw_model *m, int32_t flags);
 
-/* f32 [n_layers+1][hidden] residual stream of the last decode step (needs QW_DEBUG_HIDDEN). */
+/*
+ * f32 [n_layers+1][hidden] residual stream of the last processed position (needs
+ * QW_DEBUG_HIDDEN): the last decode step, or the last row of the last prefill.
+ */
 int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
 
 /*
@@ -259,6 +268,16 @@ int qw_query(const qw_model *m, int32_t what, int64_t *out);
 int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *weights, void *k_cache, void *v_cache,
                            int32_t pos, int32_t token, float *logits_dev, int32_t *next_token_dev,
                            void *cuda_stream, int32_t wait);
+
+/*
+ * Test entry of the tensor-core GEMM the prefill uses: C = A B^T with A fp16
+ * [M, K], B fp16 [N, K] (row-major, K contiguous) and C f32 [M, N], all device
+ * pointers, 16-byte aligned.  K must be a multiple of 64, N of the tile width bn
+ * (128 or 256).  Waits for cuda_stream and returns QW_OK, QW_INTERNAL_INVARIANT
+ * (a bounded wait inside the kernel expired) or QW_CUDA_ERROR.
+ */
+int qw_debug_gemm_f16(const void *a_dev, const void *b_dev, float *c_dev, int32_t M, int32_t N, int32_t K,
+                      int32_t bn, void *cuda_stream);
 
 /* Static text for a status code. */
 const char *qw_status_string(int status);

@@ -1,20 +1,1050 @@
-// prefill.cu - batched prefill of a prompt chunk.
+// prefill.cu - batched prefill of a prompt chunk on the sm_103a tensor cores.
+//
+// The prompt's T rows go through every layer together ("Portable WebAssembly Runtime
+// Architecture for TinyRustLM", section "Prefill versus decode": prefill is the
+// matrix-matrix form of the same decoder; "Scalar-Native Qwen3 Reference Runtime As
+// The Numerical Authority", section 2 steps 1-7 give the per-row arithmetic):
+//
+//   embed+norm   x = f32(E[tok]), h = fp16(RMSNorm(x) * w_in)            row kernel
+//   QKV GEMM     qkv = h Wqkv^T                    (f32 out)              tcgen05
+//   qk/rope      QK-Norm + RoPE of q (fp16 out) and k, K/V rows -> cache  row kernel
+//   attention    causal GQA, S = Q K^T, online softmax, O += P V          tcgen05
+//   O GEMM       x += o Wo^T                       (residual epilogue)    tcgen05
+//   norm         h = fp16(RMSNorm(x) * w_post)                            row kernel
+//   GU GEMM      a = fp16(silu(h Wg^T) * (h Wu^T)) (SwiGLU epilogue)      tcgen05
+//   down GEMM    x += a Wd^T                       (residual epilogue)    tcgen05
+//   head         last row only: final RMSNorm, logits = E hf, argmax      GEMV kernel
+//
+// Operands of the tensor-core steps are fp16 with f32 accumulation (kind::f16); the
+// weights are converted to fp16 once, when the model is created (exact for every
+// bf16 value of magnitude >= 2^-14; smaller ones round to fp16 subnormals).  Gate and
+// up rows are interleaved in blocks of 128 so that one 256-wide output tile holds a
+// gate block and its matching up block and the SwiGLU product happens in the epilogue.
+//
+// GEMM kernel: persistent, one CTA per SM, warp-specialised: warp 0 issues TMA tile
+// loads into a ring of shared-memory stages, warp 1 owns the TMEM allocation and
+// issues tcgen05.mma from one thread, warps 2-5 drain the double-buffered TMEM
+// accumulator (tcgen05.ld) and apply the epilogue while the next tile accumulates.
+// Every wait is bounded: on expiry the CTA records QW_INTERNAL_INVARIANT, raises a
+// shared abort flag, waits (bounded) for its own copies and MMAs in flight, frees
+// TMEM and returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdio>
+#include <vector>
+
 #include "qw_prefill.h"
+#include "tc.cuh"
 
 namespace qw {
+namespace {
 
-size_t prefill_workspace_bytes(const qw_config &, int) { return 256; }
+using namespace tc;
 
-cudaError_t prefill_prepare() { return cudaSuccess; }
+constexpr int BM = 128;  // GEMM tile rows (prompt rows) = TMEM lanes
+constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle span of fp16
+constexpr int kGemmThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
 
-void prefill_init(PrefillState *st, const DecodeArgs &, uint8_t *buf, size_t bytes, int rows_max, int nsm) {
+enum { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+
+struct GemmParams {
+    int M, N, K;       // rows, output columns, reduction length
+    float *out;        // EPI_STORE: out[M][ldo] = acc; EPI_ADD: out[M][ldo] += acc
+    int ldo;
+    __half *act;       // EPI_SWIGLU: act[M][ldh], column block nt * BN/2
+    int ldh;
+    StepFlags *flags;
+};
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = BM * BK * 2;
+    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+    static constexpr int kBarBytes = 256;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+    static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void raise(StepFlags *f, unsigned code) {
+    atomicCAS(&f->err, 0u, code);
+    atomicExch(&f->abort, 1u);
+}
+
+// 1024-byte aligned start of dynamic shared memory (swizzled tiles need it).
+__device__ __forceinline__ uint8_t *smem_base1024() {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t off = (1024u - (su32(smem_raw) & 1023u)) & 1023u;
+    return smem_raw + off;
+}
+
+__device__ __forceinline__ uint4 pack_half8(const float *v) {
+    uint4 u;
+    __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+    __half2 h2 = __floats2half2_rn(v[4], v[5]), h3 = __floats2half2_rn(v[6], v[7]);
+    u.x = *reinterpret_cast<uint32_t *>(&h0);
+    u.y = *reinterpret_cast<uint32_t *>(&h1);
+    u.z = *reinterpret_cast<uint32_t *>(&h2);
+    u.w = *reinterpret_cast<uint32_t *>(&h3);
+    return u;
+}
+
+// ------------------------------------------------------------------ GEMM epilogues
+
+template <int BN, int EPI>
+__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int row, int nt) {
+    const bool live = row < p.M;
+    if constexpr (EPI == EPI_SWIGLU) {
+        constexpr int HB = BN / 2;  // gate columns [0, HB), matching up columns [HB, BN)
+#pragma unroll 1
+        for (int c = 0; c < HB; c += 32) {
+            float g[32], u[32];
+            tmem_ld32(tacc + c, g);
+            tmem_ld32(tacc + HB + c, u);
+            if (live) {
+                float a[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = (g[i] * (1.0f / (1.0f + expf(-g[i])))) * u[i];
+                uint4 *dst = reinterpret_cast<uint4 *>(p.act + (size_t)row * p.ldh + (size_t)nt * HB + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = pack_half8(a + 8 * i);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            tmem_ld32(tacc + c, v);
+            if (live) {
+                float4 *dst = reinterpret_cast<float4 *>(p.out + (size_t)row * p.ldo + (size_t)nt * BN + c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    if constexpr (EPI == EPI_ADD) {
+                        const float4 x = dst[i];
+                        o.x += x.x;
+                        o.y += x.y;
+                        o.z += x.z;
+                        o.w += x.w;
+                    }
+                    dst[i] = o;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ GEMM kernel
+//
+// C[M, N] = A[M, K] * B[N, K]^T, A and B fp16 row-major (K contiguous), read by TMA
+// with 128-byte swizzle.  Tiles BM x BN, tile index -> (m tile fastest, n tile).
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                const GemmParams p) {
+    using C = GemmCfg<BN>;
+    uint8_t *base = smem_base1024();
+    uint8_t *sa = base;
+    uint8_t *sb = base + C::kStages * C::kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sb + C::kStages * C::kBBytes);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (p.M + BM - 1) / BM;
+    const int ntiles = tiles_m * (p.N / BN);
+    const int nkb = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            int s = 0;
+            unsigned ph = 0;
+            int last_par[C::kStages];
+            for (int i = 0; i < C::kStages; ++i) last_par[i] = -1;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort, true, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[s], C::kStageBytes);
+                    tma_load_2d(sa + s * C::kABytes, &tma, kb * BK, m0, &full[s]);
+                    tma_load_2d(sb + s * C::kBBytes, &tmb, kb * BK, n0, &full[s]);
+                    last_par[s] = (int)ph;
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                raise(p.flags, kErrInvariant);
+                // no copy may land in shared memory after this CTA has exited
+                for (int i = 0; i < C::kStages; ++i)
+                    if (last_par[i] >= 0) mbar_wait(&full[i], (unsigned)last_par[i], abort, false, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            int s = 0, acc = 0;
+            unsigned ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort, true, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort, true, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(su32(sa + s * C::kABytes));
+                    const uint64_t bd = desc_sw128(su32(sb + s * C::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step (address field >> 4)
+                        mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0);
+                    mma_commit(&empty[s]);
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                raise(p.flags, kErrInvariant);
+            }
+            // every MMA this thread issued completes before TMEM is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, abort, false, kWaitLimitNs);
+        }
+    } else {
+        // ---- epilogue warps 2..5: TMEM lane quarter = warp % 4
+        const int q = warp & 3;
+        int acc = 0;
+        unsigned aph = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort, true, kWaitLimitNs);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort = 1;
+                    raise(p.flags, kErrInvariant);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int mt = tile % tiles_m, nt = tile / tiles_m;
+            const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32 + lane, nt);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ row kernels
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red may still be read by a previous call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+    return t;
+}
+
+// h[t] = fp16(w * (x[t] * rsqrt(mean(x[t]^2) + eps))); with tokens, x[t] = f32(E[tok[t]]) first.
+__global__ void __launch_bounds__(kRowThreads) norm_rows_kernel(float *x, const int32_t *tokens,
+                                                                const __nv_bfloat16 *embed,
+                                                                const __nv_bfloat16 *w, __half *h, int H,
+                                                                float eps) {
+    __shared__ float red[kRowThreads / 32];
+    const int t = blockIdx.x;
+    float *xr = x + (size_t)t * H;
+    float v[12];  // H <= 3072
+    const int per = H / kRowThreads;
+    float ss = 0.f;
+    if (tokens) {
+        const __nv_bfloat16 *er = embed + (size_t)tokens[t] * H;
+        for (int i = 0; i < per; ++i) {
+            v[i] = __bfloat162float(er[threadIdx.x + kRowThreads * i]);
+            xr[threadIdx.x + kRowThreads * i] = v[i];
+        }
+    } else {
+        for (int i = 0; i < per; ++i) v[i] = xr[threadIdx.x + kRowThreads * i];
+    }
+    for (int i = 0; i < per; ++i) ss += v[i] * v[i];
+    const float r = rsqrtf(block_sum(ss, red) / (float)H + eps);
+    __half *hr = h + (size_t)t * H;
+    for (int i = 0; i < per; ++i) {
+        const int c = threadIdx.x + kRowThreads * i;
+        hr[c] = __float2half_rn(__bfloat162float(w[c]) * (v[i] * r));
+    }
+}
+
+// One warp per (row, head slot): slots [0, Hq) query heads, [Hq, Hq+Hkv) key heads,
+// [Hq+Hkv, Hq+2Hkv) value heads.  A lane holds dims (lane, lane+32, lane+64, lane+96);
+// RoPE pairs dim i with i + 64.
+template <typename KT>
+__global__ void qk_rope_kernel(const float *qkv, int n, int Hq, int Hkv, const __nv_bfloat16 *q_norm,
+                               const __nv_bfloat16 *k_norm, const float2 *rope, int pos0, float eps,
+                               __half *q16, int q_rows, KT *kc, KT *vc, int max_ctx) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = blockIdx.y * (blockDim.x >> 5) + warp;
+    const int t = blockIdx.x;
+    const int nslot = Hq + 2 * Hkv;
+    if (slot >= nslot || t >= n) return;
+    const float *src = qkv + (size_t)t * nslot * kHeadDim + (size_t)slot * kHeadDim;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
+    const int P = pos0 + t;
+    if (slot < Hq + Hkv) {
+        const __nv_bfloat16 *nw = slot < Hq ? q_norm : k_norm;
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __bfloat162float(nw[lane + 32 * i]) * (v[i] * r);
+        const float2 c0 = rope[(size_t)P * (kHeadDim / 2) + lane];
+        const float2 c1 = rope[(size_t)P * (kHeadDim / 2) + lane + 32];
+        const float a0 = v[0], a1 = v[1], b0 = v[2], b1 = v[3];
+        v[0] = a0 * c0.x - b0 * c0.y;
+        v[2] = b0 * c0.x + a0 * c0.y;
+        v[1] = a1 * c1.x - b1 * c1.y;
+        v[3] = b1 * c1.x + a1 * c1.y;
+    }
+    if (slot < Hq) {
+        __half *dst = q16 + ((size_t)slot * q_rows + t) * kHeadDim;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = __float2half_rn(v[i]);
+    } else {
+        const bool is_k = slot < Hq + Hkv;
+        const int kvh = is_k ? slot - Hq : slot - Hq - Hkv;
+        KT *dst = (is_k ? kc : vc) + ((size_t)kvh * max_ctx + P) * kHeadDim;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (sizeof(KT) == 4)
+                dst[lane + 32 * i] = v[i];
+            else
+                dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ causal attention
+//
+// CTA = (query tile, KV head).  The 128 MMA rows are the G query heads of the KV
+// head stacked over 128/G positions: row r -> head kvh*G + r/(128/G), position
+// t0 + r%(128/G), so both heads of a group share every K/V tile.  Per 64-key block:
+// S = Q K^T (TMEM), the thread owning row r applies the causal mask and the online
+// softmax in the log2 domain, writes P (fp16) to shared memory, and O += P V
+// accumulates in TMEM.  O is rescaled only when the running max grows by more than 8
+// (factor 256): the final O / l uses one consistent reference max either way, and
+// p <= 2^8 stays well inside fp16.
+
+constexpr int kAttnThreads = 128;
+constexpr int kAttnKeys = 64;
+
+struct AttnParams {
+    const __half *q16;  // [Hq][q_rows][128]
+    int q_rows;
+    const void *kc, *vc;  // this layer's cache planes [Hkv][max_ctx][128]
+    int max_ctx;
+    __half *o16;        // [n][Hq * 128]
+    int n, pos0, Hq, G;
+    float scale_log2;   // log2(e) / sqrt(128)
+    StepFlags *flags;
+};
+
+struct AttnSmem {
+    static constexpr int kQ = 0;                   // 2 regions x [128 rows][128 B]
+    static constexpr int kK = kQ + 2 * 128 * 128;  // 2 regions x [64 keys][128 B]
+    static constexpr int kV = kK + 2 * 64 * 128;   // [128 dims][64 keys] fp16
+    static constexpr int kP = kV + 128 * 128;      // [128 rows][64 keys] fp16
+    static constexpr int kBar = kP + 128 * 128;
+    static constexpr int kBytes = kBar + 64;
+    static constexpr size_t kDyn = 1024 + kBytes;
+};
+// Two CTAs per SM at most (shared memory), each holding 256 TMEM columns.
+static_assert(3 * AttnSmem::kDyn > 228 * 1024, "a third attention CTA per SM would exceed TMEM");
+
+template <typename KT>
+__device__ __forceinline__ float kv_load(const KT *p) {
+    if constexpr (sizeof(KT) == 4)
+        return *p;
+    else
+        return __bfloat162float(*p);
+}
+
+template <typename KT>
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnParams p) {
+    uint8_t *base = smem_base1024();
+    uint8_t *sQ = base + AttnSmem::kQ, *sK = base + AttnSmem::kK, *sV = base + AttnSmem::kV,
+            *sP = base + AttnSmem::kP;
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(base + AttnSmem::kBar);
+    uint64_t *bar_o = bar_s + 1;
+    uint64_t *bar_d = bar_s + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_s + 3);
+    volatile int *sh_ok = reinterpret_cast<volatile int *>(tslot + 1);
+    volatile int *abort = sh_ok + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int QT = kAttnThreads / p.G;  // positions per tile
+    const int ntq = (p.n + QT - 1) / QT;
+    const int qt = ntq - 1 - (int)blockIdx.x;  // longest (latest) tiles first
+    const int g = blockIdx.y;
+    const int t0 = qt * QT;
+    const int head = g * p.G + tid / QT;
+    const int t = t0 + tid % QT;
+    const int pr = p.pos0 + t;
+    const bool valid = t < p.n;
+    const int kv_len = p.pos0 + p.n;
+    const int last = p.pos0 + min(t0 + QT, p.n) - 1;
+    const int nkb = last / kAttnKeys + 1;
+    const KT *kc = reinterpret_cast<const KT *>(p.kc) + (size_t)g * p.max_ctx * kHeadDim;
+    const KT *vc = reinterpret_cast<const KT *>(p.vc) + (size_t)g * p.max_ctx * kHeadDim;
+
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_d, 1);
+        *sh_ok = 1;
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    // this thread's query row -> swizzled Q tile (zeros past the prompt)
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q16 + ((size_t)head * p.q_rows + t) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sQ + (c >> 3) * (128 * 128) + swz128(tid, c & 7)) = v;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    constexpr uint32_t idesc_s = idesc_f16_f32(128, kAttnKeys);
+    constexpr uint32_t idesc_o = idesc_f16_f32(128, kHeadDim);
+
+    float m_used = -INFINITY, l = 0.f;
+    unsigned phs = 0, pho = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int k0 = kb * kAttnKeys;
+        // K block: thread -> key tid/2, dims 64*(tid&1) .. +63 (one swizzle region row)
+        {
+            const int j = tid >> 1, reg = tid & 1, key = k0 + j;
+            uint8_t *dst = sK + reg * (64 * 128);
+            const KT *src = kc + (size_t)key * kHeadDim + reg * 64;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = key < kv_len ? kv_load(src + 8 * c + i) : 0.f;
+                *reinterpret_cast<uint4 *>(dst + swz128(j, c)) = pack_half8(f);
+            }
+        }
+        // V block transposed: thread -> dim tid, 8 keys per 16-byte chunk
+        {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int key = k0 + 8 * c + i;
+                    f[i] = key < kv_len ? kv_load(vc + (size_t)key * kHeadDim + tid) : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(sV + swz128(tid, c)) = pack_half8(f);
+            }
+        }
+        fence_async_shared();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+                const uint64_t ad = desc_sw128(su32(sQ + (k >> 2) * (128 * 128))) + 2u * (k & 3);
+                const uint64_t bd = desc_sw128(su32(sK + (k >> 2) * (64 * 128))) + 2u * (k & 3);
+                mma_f16(tS, ad, bd, idesc_s, k != 0);
+            }
+            mma_commit(bar_s);
+            if (!mbar_wait(bar_s, phs, abort, false, kWaitLimitNs)) *sh_ok = 0;
+        }
+        phs ^= 1u;
+        __syncthreads();
+        tc_fence_after();
+        if (!*sh_ok) {
+            ok = false;
+            break;
+        }
+        float s[2][32];
+        tmem_ld32(tS + lane_base, s[0]);
+        tmem_ld32(tS + lane_base + 32, s[1]);
+        float mb = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kAttnKeys; ++j) {
+            float &sj = s[j >> 5][j & 31];
+            sj = (k0 + j <= pr) ? sj * p.scale_log2 : -INFINITY;
+            mb = fmaxf(mb, sj);
+        }
+        const bool resc = mb > m_used + 8.f;
+        const float m_new = resc ? mb : m_used;
+        const float factor = resc ? exp2f(m_used - m_new) : 1.f;
+        if (kb > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim; c += 32) {
+                float o[32];
+                tmem_ld32(tO + lane_base + c, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= factor;
+                tmem_st32(tO + lane_base + c, o);
+            }
+        }
+        l *= factor;
+        m_used = m_new;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float e[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __half h = __float2half_rn(exp2f(s[c >> 2][8 * (c & 3) + i] - m_used));
+                e[i] = __half2float(h);
+                l += e[i];
+            }
+            *reinterpret_cast<uint4 *>(sP + swz128(tid, c)) = pack_half8(e);
+        }
+        fence_async_shared();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < kAttnKeys / 16; ++k) {
+                const uint64_t ad = desc_sw128(su32(sP)) + 2u * k;
+                const uint64_t bd = desc_sw128(su32(sV)) + 2u * k;
+                mma_f16(tO, ad, bd, idesc_o, kb > 0 || k > 0);
+            }
+            mma_commit(bar_o);
+            if (!mbar_wait(bar_o, pho, abort, false, kWaitLimitNs)) *sh_ok = 0;
+        }
+        pho ^= 1u;
+        __syncthreads();
+        tc_fence_after();
+        if (!*sh_ok) ok = false;
+    }
+    if (ok) {
+        const float inv = 1.0f / l;
+        __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim;
+#pragma unroll 1
+        for (int c = 0; c < kHeadDim; c += 32) {
+            float o[32];
+            tmem_ld32(tO + lane_base + c, o);
+            if (valid) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= inv;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + c)[i] = pack_half8(o + 8 * i);
+            }
+        }
+    } else if (tid == 0) {
+        raise(p.flags, kErrInvariant);
+        mma_commit(bar_d);  // every MMA issued completes before TMEM is released
+        mbar_wait(bar_d, 0, abort, false, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ------------------------------------------------------------------ head (last row)
+
+constexpr int kHeadThreads = 256;
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
+    const uint32_t u = __float_as_uint(v);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (0xffffffffu - (uint32_t)id);
+}
+
+// logits[v] = E[v] . (final_norm * RMSNorm(x)), packed-key argmax (ties -> lowest id);
+// the last CTA to finish publishes the token and re-arms the key for the next call.
+__global__ void __launch_bounds__(kHeadThreads) head_kernel(const float *x, const __nv_bfloat16 *final_norm,
+                                                            const __nv_bfloat16 *E, int V, int H, float eps,
+                                                            float *logits, unsigned long long *key,
+                                                            unsigned *count, StepFlags *flags) {
+    __shared__ __align__(16) float hf[3072];
+    __shared__ float red[kHeadThreads / 32];
+    __shared__ unsigned long long best[kHeadThreads / 32];
+    __shared__ int bad_any;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) bad_any = 0;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < H; c += kHeadThreads) ss += x[c] * x[c];
+    const float r = rsqrtf(block_sum(ss, red) / (float)H + eps);
+    for (int c = threadIdx.x; c < H; c += kHeadThreads) hf[c] = __bfloat162float(final_norm[c]) * (x[c] * r);
+    __syncthreads();
+    unsigned long long kbest = 0;
+    bool bad = false;
+    const int nchunk = H / 256;  // 16-byte chunks of 8 bf16 per lane
+    const int gw = blockIdx.x * (kHeadThreads / 32) + warp, nw = gridDim.x * (kHeadThreads / 32);
+    for (int v = gw; v < V; v += nw) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(E + (size_t)v * H);
+        float acc = 0.f;
+        for (int i = 0; i < nchunk; ++i) {
+            const int c = lane + 32 * i;
+            const uint4 u = __ldg(row + c);
+            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+            const float4 h0 = *reinterpret_cast<const float4 *>(hf + 8 * c);
+            const float4 h1 = *reinterpret_cast<const float4 *>(hf + 8 * c + 4);
+            float2 f;
+            f = __bfloat1622float2(b[0]);
+            acc += f.x * h0.x + f.y * h0.y;
+            f = __bfloat1622float2(b[1]);
+            acc += f.x * h0.z + f.y * h0.w;
+            f = __bfloat1622float2(b[2]);
+            acc += f.x * h1.x + f.y * h1.y;
+            f = __bfloat1622float2(b[3]);
+            acc += f.x * h1.z + f.y * h1.w;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            logits[v] = acc;
+            if (!isfinite(acc)) bad = true;
+            const unsigned long long k = argmax_key(acc, v);
+            kbest = k > kbest ? k : kbest;
+        }
+    }
+    if (lane == 0) {
+        best[warp] = kbest;
+        if (bad) bad_any = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long b = 0;
+        for (int w = 0; w < kHeadThreads / 32; ++w) b = best[w] > b ? best[w] : b;
+        if (bad_any) atomicCAS(&flags->err, 0u, kErrNumerical);
+        if (b) atomicMax(key, b);
+        __threadfence();
+        const unsigned old = atomicAdd(count, 1u);
+        if (old + 1u == gridDim.x) {
+            __threadfence();
+            const unsigned long long k = atomicAdd(key, 0ull);
+            flags->next_tok = k ? (int)(0xffffffffu - (unsigned)(k & 0xffffffffull)) : 0;
+            *key = 0ull;
+            *count = 0u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ weight conversion
+
+// dst row mapping of source row i: mode 0 -> off + i; mode 1 (gate) / 2 (up) ->
+// (i / 128) * 256 + (mode == 2 ? 128 : 0) + i % 128.
+__global__ void convert_kernel(const void *src, const __half *scales, int int8, int rows, int cols, __half *dst,
+                               int mode, int off, unsigned *overflow) {
+    const long long n = (long long)rows * cols;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(e / cols), c = (int)(e % cols);
+        float w;
+        if (int8) {
+            w = (float)reinterpret_cast<const int8_t *>(src)[e] * __half2float(scales[(size_t)i * (cols / 32) + c / 32]);
+        } else {
+            w = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[e]);
+        }
+        const int drow = mode == 0 ? off + i : (i / 128) * 256 + (mode == 2 ? 128 : 0) + i % 128;
+        const __half h = __float2half_rn(w);
+        if (__hisinf(h)) atomicAdd(overflow, 1u);
+        dst[(size_t)drow * cols + c] = h;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+cudaError_t load_encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = (EncodeTiledFn)fn;
+    return cudaSuccess;
+}
+
+// fp16 row-major [rows][cols] read in boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_rows) {
+    if (!g_encode || rows < 1 || cols % 64 || ((uintptr_t)ptr & 15)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t set_gemm_attr() {
+    return cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)GemmCfg<BN>::kSmem);
+}
+
+template <int BN, int EPI>
+cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int nsm,
+                        cudaStream_t st) {
+    const int tiles = (p.M + BM - 1) / BM * (p.N / BN);
+    const int grid = tiles < nsm ? tiles : nsm;
+    gemm_kernel<BN, EPI><<<grid, kGemmThreads, GemmCfg<BN>::kSmem, st>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+size_t align_up(size_t v) { return (v + 255) / 256 * 256; }
+
+struct PrefillLayout {
+    size_t w16, x, h, qkv, q16, o16, act, tok, misc, total;
+    size_t w_layer;  // fp16 weight elements per layer
+};
+
+PrefillLayout prefill_layout(const qw_config &c, int rows) {
+    PrefillLayout L{};
+    const size_t H = c.hidden, QD = (size_t)c.n_heads * c.head_dim, KD = (size_t)c.n_kv_heads * c.head_dim,
+                 I = c.intermediate;
+    L.w_layer = (QD + 2 * KD) * H + H * QD + 2 * I * H + H * I;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align_up(bytes);
+        return at;
+    };
+    L.w16 = take((size_t)c.n_layers * L.w_layer * 2);
+    L.x = take((size_t)rows * H * 4);
+    L.h = take((size_t)rows * (H > I ? H : I) * 2);
+    L.qkv = take((size_t)rows * (QD + 2 * KD) * 4);
+    L.q16 = take((size_t)rows * QD * 2);
+    L.o16 = take((size_t)rows * QD * 2);
+    L.act = take((size_t)rows * I * 2);
+    L.tok = take((size_t)rows * 4);
+    L.misc = take(64);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+struct PrefillImpl {
+    PrefillLayout lay;
+    qw_config cfg;
+    std::vector<DevLayer> host_layers;  // the model's layer table (device pointers)
+    std::vector<CUtensorMap> wmaps;     // per layer: qkv, o, gate/up, down
+};
+
+size_t prefill_workspace_bytes(const qw_config &c, int rows_max) { return prefill_layout(c, rows_max).total; }
+
+cudaError_t prefill_prepare() {
+    cudaError_t e = load_encoder();
+    if (e != cudaSuccess) return e;
+    if ((e = set_gemm_attr<256, EPI_STORE>()) != cudaSuccess) return e;
+    if ((e = set_gemm_attr<256, EPI_SWIGLU>()) != cudaSuccess) return e;
+    if ((e = set_gemm_attr<128, EPI_ADD>()) != cudaSuccess) return e;
+    if ((e = set_gemm_attr<128, EPI_STORE>()) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)AttnSmem::kDyn)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)AttnSmem::kDyn);
+}
+
+int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, uint8_t *buf, size_t bytes,
+                 int rows_max, int nsm, cudaStream_t stream) {
     st->buf = buf;
     st->bytes = bytes;
     st->rows_max = rows_max;
     st->nsm = nsm;
     st->ready = 0;
+    st->impl = nullptr;
+    PrefillImpl *im = new (std::nothrow) PrefillImpl();
+    if (!im) return 1;
+    im->cfg = c;
+    im->lay = prefill_layout(c, rows_max);
+    if (im->lay.total > bytes) {
+        delete im;
+        return 1;
+    }
+    st->impl = im;
+    im->host_layers.assign(host_layers, host_layers + c.n_layers);
+    const PrefillLayout &L = im->lay;
+    const int H = c.hidden, QD = c.n_heads * c.head_dim, KD = c.n_kv_heads * c.head_dim, I = c.intermediate;
+    unsigned *overflow = reinterpret_cast<unsigned *>(buf + L.misc + 16);
+    if (cudaMemsetAsync(buf + L.misc, 0, 64, stream) != cudaSuccess) return 1;
+    const int int8 = c.weight_format == QW_W_INT8_G32 ? 1 : 0;
+    im->wmaps.resize((size_t)c.n_layers * 4);
+    for (int l = 0; l < c.n_layers; ++l) {
+        __half *w = reinterpret_cast<__half *>(buf + L.w16) + (size_t)l * L.w_layer;
+        __half *wqkv = w, *wo = wqkv + (size_t)(QD + 2 * KD) * H, *wgu = wo + (size_t)H * QD,
+               *wd = wgu + (size_t)2 * I * H;
+        const DevLayer &Ly = host_layers[l];
+        struct Job {
+            int m, rows, cols, mode, off;
+            __half *dst;
+        } jobs[7] = {{0, QD, H, 0, 0, wqkv},  {1, KD, H, 0, QD, wqkv}, {2, KD, H, 0, QD + KD, wqkv},
+                     {3, H, QD, 0, 0, wo},     {4, I, H, 1, 0, wgu},    {5, I, H, 2, 0, wgu},
+                     {6, H, I, 0, 0, wd}};
+        for (const Job &j : jobs) {
+            convert_kernel<<<4 * nsm, 256, 0, stream>>>(Ly.w[j.m], Ly.s[j.m], int8, j.rows, j.cols, j.dst, j.mode,
+                                                        j.off, overflow);
+            if (cudaGetLastError() != cudaSuccess) return 1;
+        }
+        CUtensorMap *m = &im->wmaps[(size_t)l * 4];
+        if (!make_map(&m[0], wqkv, QD + 2 * KD, H, 256) || !make_map(&m[1], wo, H, QD, 128) ||
+            !make_map(&m[2], wgu, 2 * I, H, 256) || !make_map(&m[3], wd, H, I, 128))
+            return 1;
+    }
+    unsigned ovf = 0;
+    if (cudaMemcpyAsync(&ovf, overflow, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return 1;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return 1;
+    if (ovf) {
+        fprintf(stderr, "qw: %u weights exceed the fp16 range; prefill runs token by token\n", ovf);
+        return 0;
+    }
+    st->ready = 1;
+    return 0;
 }
 
-int prefill_run(PrefillState *, const DecodeArgs &, int, const int32_t *, int, cudaStream_t) { return 1; }
+void prefill_destroy(PrefillState *st) {
+    delete st->impl;
+    st->impl = nullptr;
+    st->ready = 0;
+}
+
+int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *tokens_host, int n, int debug,
+                cudaStream_t stream) {
+    PrefillImpl *im = st->impl;
+    if (!im || !st->ready) return 1;
+    const qw_config &c = im->cfg;
+    const PrefillLayout &L = im->lay;
+    uint8_t *buf = st->buf;
+    const int H = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, QD = Hq * kHeadDim, KD = Hkv * kHeadDim,
+              I = c.intermediate, G = Hq / Hkv;
+    const int nslot = Hq + 2 * Hkv;
+    float *x = reinterpret_cast<float *>(buf + L.x);
+    __half *h = reinterpret_cast<__half *>(buf + L.h);
+    float *qkv = reinterpret_cast<float *>(buf + L.qkv);
+    __half *q16 = reinterpret_cast<__half *>(buf + L.q16);
+    __half *o16 = reinterpret_cast<__half *>(buf + L.o16);
+    __half *act = reinterpret_cast<__half *>(buf + L.act);
+    int32_t *tok = reinterpret_cast<int32_t *>(buf + L.tok);
+    unsigned long long *key = reinterpret_cast<unsigned long long *>(buf + L.misc);
+    unsigned *count = reinterpret_cast<unsigned *>(buf + L.misc + 8);
+    const size_t kv_plane = (size_t)Hkv * a.max_ctx * kHeadDim * (a.kv_f32 ? 4 : 2);
+    const DevLayer *hl = im->host_layers.data();
+
+    // argmax key and finishing counter of the head kernel start at zero every call
+    if (cudaMemsetAsync(key, 0, 16, stream) != cudaSuccess) return 1;
+    for (int done = 0; done < n;) {
+        const int m = n - done < st->rows_max ? n - done : st->rows_max;
+        const int p0 = pos0 + done;
+        cudaError_t e = cudaMemcpyAsync(tok, tokens_host + done, (size_t)m * 4, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return 1;
+        CUtensorMap mh, mo, ma;
+        if (!make_map(&mh, h, m, H, BM) || !make_map(&mo, o16, m, QD, BM) || !make_map(&ma, act, m, I, BM))
+            return 1;
+        norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, tok, a.embed, hl[0].input_norm, h, H, a.eps);
+        if (debug & 1)
+            cudaMemcpyAsync(a.hidden, x + (size_t)(m - 1) * H, (size_t)H * 4, cudaMemcpyDeviceToDevice, stream);
+        for (int l = 0; l < c.n_layers; ++l) {
+            const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
+            GemmParams gp{};
+            gp.flags = a.flags;
+            gp.M = m;
+            // q | k | v
+            gp.N = QD + 2 * KD;
+            gp.K = H;
+            gp.out = qkv;
+            gp.ldo = QD + 2 * KD;
+            if (launch_gemm<256, EPI_STORE>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
+            uint8_t *kc = reinterpret_cast<uint8_t *>(a.kc) + (size_t)l * kv_plane;
+            uint8_t *vc = reinterpret_cast<uint8_t *>(a.vc) + (size_t)l * kv_plane;
+            const dim3 qg(m, (nslot + 7) / 8);
+            if (a.kv_f32)
+                qk_rope_kernel<float><<<qg, 256, 0, stream>>>(qkv, m, Hq, Hkv, hl[l].q_norm, hl[l].k_norm, a.rope,
+                                                              p0, a.eps, q16, st->rows_max,
+                                                              reinterpret_cast<float *>(kc),
+                                                              reinterpret_cast<float *>(vc), a.max_ctx);
+            else
+                qk_rope_kernel<__nv_bfloat16><<<qg, 256, 0, stream>>>(
+                    qkv, m, Hq, Hkv, hl[l].q_norm, hl[l].k_norm, a.rope, p0, a.eps, q16, st->rows_max,
+                    reinterpret_cast<__nv_bfloat16 *>(kc), reinterpret_cast<__nv_bfloat16 *>(vc), a.max_ctx);
+            // causal attention over the cache rows [0, p0 + m)
+            AttnParams ap{};
+            ap.q16 = q16;
+            ap.q_rows = st->rows_max;
+            ap.kc = kc;
+            ap.vc = vc;
+            ap.max_ctx = a.max_ctx;
+            ap.o16 = o16;
+            ap.n = m;
+            ap.pos0 = p0;
+            ap.Hq = Hq;
+            ap.G = G;
+            ap.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+            ap.flags = a.flags;
+            const dim3 ag((m + kAttnThreads / G - 1) / (kAttnThreads / G), Hkv);
+            if (a.kv_f32)
+                attn_kernel<float><<<ag, kAttnThreads, AttnSmem::kDyn, stream>>>(ap);
+            else
+                attn_kernel<__nv_bfloat16><<<ag, kAttnThreads, AttnSmem::kDyn, stream>>>(ap);
+            // x += o Wo^T
+            gp.N = H;
+            gp.K = QD;
+            gp.out = x;
+            gp.ldo = H;
+            if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
+            norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, nullptr, nullptr, hl[l].post_norm, h, H, a.eps);
+            // a = silu(h Wg^T) * (h Wu^T)
+            gp.N = 2 * I;
+            gp.K = H;
+            gp.act = act;
+            gp.ldh = I;
+            if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream) != cudaSuccess) return 1;
+            // x += a Wd^T
+            gp.N = H;
+            gp.K = I;
+            gp.out = x;
+            gp.ldo = H;
+            if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream) != cudaSuccess) return 1;
+            if (debug & 1)
+                cudaMemcpyAsync(a.hidden + (size_t)(l + 1) * H, x + (size_t)(m - 1) * H, (size_t)H * 4,
+                                cudaMemcpyDeviceToDevice, stream);
+            if (l + 1 < c.n_layers)
+                norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, nullptr, nullptr, hl[l + 1].input_norm, h, H,
+                                                                a.eps);
+        }
+        done += m;
+        if (done == n) {
+            head_kernel<<<4 * st->nsm, kHeadThreads, 0, stream>>>(x + (size_t)(m - 1) * H, a.final_norm, a.lm_head,
+                                                                  a.V, H, a.eps, a.logits, key, count, a.flags);
+        }
+        if (cudaGetLastError() != cudaSuccess) return 1;
+    }
+    return 0;
+}
+
+// ------------------------------------------------------------------ GEMM test entry
+
+namespace {
+__device__ StepFlags g_gemm_flags;  // status of the test GEMM entry point
+}
+
+int prefill_debug_gemm(const void *a, const void *b, float *c, int M, int N, int K, int bn, cudaStream_t stream) {
+    if (prefill_prepare() != cudaSuccess) return QW_CUDA_ERROR;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return QW_CUDA_ERROR;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, M, K, BM) || !make_map(&mb, b, N, K, bn)) return QW_INVALID_ARGUMENT;
+    StepFlags *flags = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&flags), g_gemm_flags) != cudaSuccess) return QW_CUDA_ERROR;
+    if (cudaMemsetAsync(flags, 0, sizeof(StepFlags), stream) != cudaSuccess) return QW_CUDA_ERROR;
+    GemmParams gp{};
+    gp.M = M;
+    gp.N = N;
+    gp.K = K;
+    gp.out = c;
+    gp.ldo = N;
+    gp.flags = flags;
+    cudaError_t e = bn == 256 ? launch_gemm<256, EPI_STORE>(ma, mb, gp, nsm, stream)
+                              : launch_gemm<128, EPI_STORE>(ma, mb, gp, nsm, stream);
+    if (e != cudaSuccess) return QW_CUDA_ERROR;
+    StepFlags f{};
+    if (cudaMemcpyAsync(&f, flags, sizeof(f), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return QW_CUDA_ERROR;
+    return f.err ? (int)f.err : QW_OK;
+}
 
 }  // namespace qw

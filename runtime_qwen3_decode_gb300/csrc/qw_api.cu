@@ -350,8 +350,13 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     m->step_bytes = qw::step_block_bytes(cfg->n_layers);
     m->logits = a.logits;
     m->hidden = a.hidden;
-    qw::prefill_init(&m->pf, a, ws + L.prefill, L.prefill_bytes,
-                     cfg->max_ctx < kPrefillRowsMax ? cfg->max_ctx : kPrefillRowsMax, nsm);
+    if (qw::prefill_init(&m->pf, *cfg, host_layers.data(), ws + L.prefill, L.prefill_bytes,
+                         cfg->max_ctx < kPrefillRowsMax ? cfg->max_ctx : kPrefillRowsMax, nsm, m->stream)) {
+        fprintf(stderr, "qw: preparing the batched prefill failed\n");
+        qw::prefill_destroy(&m->pf);
+        delete m;
+        return QW_CUDA_ERROR;
+    }
     {
         std::lock_guard<std::mutex> g(g_live_mu);
         g_live.insert(m);
@@ -367,6 +372,7 @@ void qw_model_destroy(qw_model *m) {
         if (!g_live.erase(m)) return;
     }
     cudaStreamSynchronize(m->stream);
+    qw::prefill_destroy(&m->pf);
     delete m;
 }
 
@@ -408,7 +414,7 @@ int qw_prefill(qw_model *m, const int32_t *tokens_host, int32_t n, int32_t *next
     if ((m->debug & QW_DEBUG_PREFILL_BY_TOKEN) || !qw::prefill_supported(m->pf)) {
         for (int32_t i = 0; i < n && !rc; ++i) rc = launch_step(m, tokens_host[i], nullptr);
     } else {
-        rc = qw::prefill_run(&m->pf, m->args, m->len, tokens_host, n, m->stream);
+        rc = qw::prefill_run(&m->pf, m->args, m->len, tokens_host, n, m->debug, m->stream);
         if (!rc) {
             m->len += n;
             m->has_last = 1;
@@ -530,6 +536,14 @@ int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n) {
     if (!dst_dev || n != len) return QW_INVALID_ARGUMENT;
     return cuda_status(cudaMemcpyAsync(dst_dev, m->ws + m->lay.trace, (size_t)n * 8, cudaMemcpyDeviceToDevice,
                                        m->stream));
+}
+
+int qw_debug_gemm_f16(const void *a_dev, const void *b_dev, float *c_dev, int32_t M, int32_t N, int32_t K,
+                      int32_t bn, void *cuda_stream) {
+    if (M < 1 || N < 1 || K < 64 || K % 64 || (bn != 128 && bn != 256) || N % bn) return QW_INVALID_ARGUMENT;
+    if (!a_dev || !b_dev || !c_dev) return QW_INVALID_ARGUMENT;
+    if (!aligned(a_dev, 16) || !aligned(b_dev, 16) || !aligned(c_dev, 16)) return QW_ALIGNMENT;
+    return qw::prefill_debug_gemm(a_dev, b_dev, c_dev, M, N, K, bn, (cudaStream_t)cuda_stream);
 }
 
 }  // extern "C"

@@ -45,7 +45,7 @@ MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_step", "qw_generate", "qw_logits",
            "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
            "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query",
-           "qw_decode_step_noalloc")
+           "qw_decode_step_noalloc", "qw_debug_gemm_f16")
 
 
 class QwError(RuntimeError):
@@ -106,6 +106,7 @@ def _lib():
             L.qw_query.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
             L.qw_decode_step_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, i32, i32, vp,
                                                  vp, vp, i32]
+            L.qw_debug_gemm_f16.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -191,6 +192,16 @@ def decode_step_noalloc(cfg: Config, dev_weights: dict, k_cache, v_cache, pos: i
     _check(_lib().qw_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), k_cache.data_ptr(), v_cache.data_ptr(),
                                          int(pos), int(token), logits_out.data_ptr(), next_token_out.data_ptr(),
                                          st.cuda_stream, 1 if wait else 0), "qw_decode_step_noalloc")
+
+
+def debug_gemm_f16(a, b, c, bn: int = 256, stream=None):
+    """qw_debug_gemm_f16: c[M,N] = a[M,K] @ b[N,K]^T on the prefill's tensor-core GEMM (fp16 in, f32 out)."""
+    import torch
+    st = stream if stream is not None else torch.cuda.current_stream()
+    M, K = a.shape
+    N = b.shape[0]
+    _check(_lib().qw_debug_gemm_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), int(M), int(N), int(K), int(bn),
+                                    st.cuda_stream), "qw_debug_gemm_f16")
 
 
 class Model:

@@ -10,6 +10,12 @@ import numpy as np
 HIDDEN_REL_L2 = 2e-3
 LOGITS_MAX_ABS = 5e-2
 MARGIN = 0.1
+# A bf16 K/V cache on both sides (not one of the workloads' prefill configurations): each
+# side rounds its own K/V rows to bf16, and an element whose two unrounded values straddle
+# a rounding boundary ends one bf16 ulp (2^-8 relative) apart.  With only one side rounding
+# the cache, the per-layer hidden error was measured at 2.6e-3 to 4.3e-3 on the tiny
+# model, so twice the bar bounds the case where both round.
+HIDDEN_REL_L2_BF16_KV = 4e-3
 
 
 def rel_l2(a, b) -> float:
@@ -24,7 +30,7 @@ def top2_margin(logits) -> float:
 
 
 def check_position(gpu_logits, ora_logits, gpu_hidden=None, ora_hidden=None, gpu_pick=None, ora_pick=None,
-                   what=""):
+                   what="", hidden_tol=HIDDEN_REL_L2):
     """Assert the parity bar at one position; returns a dict of the measured errors."""
     g = np.asarray(gpu_logits, np.float32)
     o = np.asarray(ora_logits, np.float32)
@@ -35,8 +41,8 @@ def check_position(gpu_logits, ora_logits, gpu_hidden=None, ora_hidden=None, gpu
     if gpu_hidden is not None and ora_hidden is not None:
         rels = [rel_l2(gh, oh) for gh, oh in zip(gpu_hidden, ora_hidden)]
         out["hidden_rel_l2_max"] = max(rels)
-        bad = [(i, r) for i, r in enumerate(rels) if r > HIDDEN_REL_L2]
-        assert not bad, f"{what}: hidden rel L2 above {HIDDEN_REL_L2} at (layer+1, value) {bad[:4]}"
+        bad = [(i, r) for i, r in enumerate(rels) if r > hidden_tol]
+        assert not bad, f"{what}: hidden rel L2 above {hidden_tol} at (layer+1, value) {bad[:4]}"
     m = top2_margin(o)
     out["margin"] = m
     if gpu_pick is not None and ora_pick is not None and m > MARGIN:

@@ -44,9 +44,12 @@ def test_workspace_bytes(qw):
     c = cfg_of(qw)
     n = qw.workspace_bytes(c)
     kv = 2 * 28 * 8 * c.max_ctx * 128 * 4  # f32 cache
-    assert n > kv
+    # fp16 copies of the seven projection matrices for the tensor-core prefill
+    H, QD, KD, I = 1024, 2048, 1024, 3072
+    w16 = 28 * 2 * ((QD + 2 * KD) * H + H * QD + 2 * I * H + H * I)
+    assert n > kv + w16
     assert qw.workspace_bytes(cfg_of(qw, kv_format="bf16")) < n - kv // 2 + 2 ** 20
-    assert n < kv + 200 * 2 ** 20  # activations, RoPE table, prefill buffers
+    assert n < kv + w16 + 200 * 2 ** 20  # activations, RoPE table, prefill buffers
     # unsupported or invalid configs report 0
     assert qw.workspace_bytes(cfg_of(qw, head_dim=64)) == 0
     assert qw.workspace_bytes(cfg_of(qw, hidden=1000)) == 0

@@ -1,0 +1,219 @@
+"""GPU parity of the batched tensor-core prefill (C ABI) against the CPU oracle.
+
+The prefill runs its projections, MLP and causal attention on the tensor cores with
+fp16 operands and f32 accumulation.  Its bar is the one the decode path meets:
+hidden-state relative L2 <= 2e-3 after every layer at the last prompt row, logits
+max-abs <= 5e-2, and the same greedy pick wherever the oracle's top-2 margin exceeds
+0.1.  The K/V rows the prefill appends are compared with the oracle's cache row by row,
+and decode steps after a batched prefill continue from that cache.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import qw_inputs as qi  # noqa: E402
+from _helpers import HIDDEN_REL_L2, HIDDEN_REL_L2_BF16_KV, check_position, rel_l2  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+# Per (layer, KV head) plane of appended K or V rows: the projections see fp16-rounded
+# activations (relative rounding 2^-11), so a plane agrees to a few 1e-4.
+KV_PLANE_REL_L2 = 2e-3
+
+
+@pytest.fixture(scope="module")
+def qw():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from runtime_qwen3_decode_gb300 import build, qw as binding
+    build.build()
+    return binding
+
+
+# --------------------------------------------------------------------------- GEMM
+
+
+@pytest.mark.parametrize("M,N,K,bn", [
+    (1, 256, 64, 256),        # one row, one k block
+    (128, 256, 128, 256),     # exactly one tile
+    (200, 512, 192, 256),     # ragged rows, 2 n tiles, 3 k blocks
+    (300, 256, 1024, 128),    # 3 m tiles (ragged), 2 n tiles of 128
+    (129, 1024, 3072, 128),   # down-projection shape, ragged by one row
+    (2048, 4096, 1024, 256),  # QKV shape of a 2048-row prompt: more tiles than SMs
+])
+def test_gemm_f16_matches_fp32(qw, M, N, K, bn):
+    torch.backends.cuda.matmul.allow_tf32 = False
+    g = torch.Generator().manual_seed(M * 1009 + N * 7 + K)
+    a = torch.randn(M, K, generator=g).half()
+    b = torch.randn(N, K, generator=g).half()
+    c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    qw.debug_gemm_f16(a.cuda(), b.cuda(), c, bn)
+    torch.cuda.synchronize()
+    ref = a.cuda().float() @ b.cuda().float().T  # plain fp32 product of the same fp16 values
+    assert bool(torch.isfinite(c).all())
+    # both sides accumulate exact fp16 products in f32, in different orders
+    err = (c - ref).abs().max().item()
+    assert err <= 2e-6 * K, f"max abs error {err:.3g}"
+
+
+def test_gemm_rejects_bad_shapes(qw):
+    a = torch.zeros(4, 64, dtype=torch.float16, device="cuda")
+    b = torch.zeros(256, 64, dtype=torch.float16, device="cuda")
+    c = torch.zeros(4, 256, device="cuda")
+    with pytest.raises(qw.QwError) as e:
+        qw.debug_gemm_f16(a, b, c, bn=96)
+    assert e.value.code == qw.INVALID_ARGUMENT
+    with pytest.raises(qw.QwError) as e:
+        qw.debug_gemm_f16(a[:, :48].contiguous(), b[:, :48].contiguous(), c, bn=256)
+    assert e.value.code == qw.INVALID_ARGUMENT
+
+
+# --------------------------------------------------------------------------- prefill
+
+
+def oracle_kv(ref, wl, n):
+    """Oracle cache rows [L][Hkv][n][d] for K and V."""
+    k = np.empty((wl.n_layers, wl.n_kv_heads, n, wl.head_dim), np.float32)
+    v = np.empty_like(k)
+    for l in range(wl.n_layers):
+        for h in range(wl.n_kv_heads):
+            for p in range(n):
+                k[l, h, p], v[l, h, p] = ref.kv_row(l, h, p)
+    return k, v
+
+
+def check_kv_planes(m, ref, wl, n):
+    ke, ve = m.kv_export(n)
+    ke, ve = ke.float().cpu().numpy(), ve.float().cpu().numpy()
+    ko, vo = oracle_kv(ref, wl, n)
+    worst = 0.0
+    for l in range(wl.n_layers):
+        for h in range(wl.n_kv_heads):
+            for got, want, what in ((ke, ko, "K"), (ve, vo, "V")):
+                r = rel_l2(got[l, h], want[l, h])
+                worst = max(worst, r)
+                assert r <= KV_PLANE_REL_L2, f"{what} layer {l} head {h}: rel L2 {r:.3g}"
+    return worst
+
+
+def run_prefill(qw, wl, chunks, host=None, kv_bf16_oracle=False, check_kv=True, decode_after=2):
+    """Prefill the workload's prompt in the given chunk sizes; compare with the oracle."""
+    n = sum(chunks)
+    wl = wl.with_(prompt_len=n, decode_steps=max(decode_after, 1))
+    host = host if host is not None else qi.make_weights(wl)
+    ref = oracle.OracleModel(wl, host)
+    if kv_bf16_oracle:
+        ref.set_kv_round_bf16(True)
+    dev = qw.weights_to_device(host, int8=wl.weight_format == "int8_g32")
+    m = qw.Model(wl, dev)
+    m.set_debug(qw.DEBUG_HIDDEN)
+    prompt = qi.prompt(wl)
+    ora = oracle.run_sequence(ref, prompt, 0, want_hidden=True)
+    pos = 0
+    for c in chunks:
+        pick = m.prefill(prompt[pos:pos + c])
+        pos += c
+    assert m.kv_length == n
+    tol = HIDDEN_REL_L2_BF16_KV if kv_bf16_oracle else HIDDEN_REL_L2
+    stats = check_position(m.logits().cpu().numpy(), ora["logits"][0], m.debug_hidden().cpu().numpy(),
+                           ora["hidden"][0], pick, ora["picks"][0], what=f"prefill {chunks} last row",
+                           hidden_tol=tol)
+    if check_kv:
+        stats["kv_plane_rel_l2_max"] = check_kv_planes(m, ref, wl, n)
+    # decode continues from the cache the prefill wrote (teacher-forced)
+    nxt = ora["picks"][0]
+    for s in range(decode_after):
+        ologits, ohid = ref.step(nxt, want_hidden=True)
+        gpick = m.decode_step(nxt)
+        check_position(m.logits().cpu().numpy(), ologits, m.debug_hidden().cpu().numpy(), ohid, gpick,
+                       oracle.argmax(ologits), what=f"decode {s} after prefill", hidden_tol=tol)
+        nxt = oracle.argmax(ologits)
+    m.close()
+    return stats
+
+
+@pytest.mark.parametrize("n", [1, 8, 63, 64, 65, 129, 300])
+def test_tiny_prefill_lengths(qw, n):
+    # 1 row; the tiny prompt; q tiles of 64 positions full, ragged and spanning key blocks
+    stats = run_prefill(qw, qi.WORKLOADS["tiny"], [n])
+    print(n, stats)
+
+
+def test_tiny_prefill_in_chunks(qw):
+    # later chunks attend to cache rows written by earlier ones (pos0 > 0)
+    run_prefill(qw, qi.WORKLOADS["tiny"], [100, 150, 50])
+
+
+def test_prefill_after_decode_steps(qw):
+    wl = qi.WORKLOADS["tiny"].with_(prompt_len=90, decode_steps=4)
+    host = qi.make_weights(wl)
+    ref = oracle.OracleModel(wl, host)
+    dev = qw.weights_to_device(host, int8=False)
+    m = qw.Model(wl, dev)
+    m.set_debug(qw.DEBUG_HIDDEN)
+    prompt = qi.prompt(wl)
+    first, second = prompt[:40], prompt[40:]
+    ora1 = oracle.run_sequence(ref, first, 0)
+    m.prefill(first)
+    nxt = ora1["picks"][0]
+    for _ in range(3):
+        ologits, _ = ref.step(nxt)
+        m.decode_step(nxt)
+        nxt = oracle.argmax(ologits)
+    ora2 = oracle.run_sequence(ref, second, 0, want_hidden=True)
+    pick = m.prefill(second)
+    check_position(m.logits().cpu().numpy(), ora2["logits"][0], m.debug_hidden().cpu().numpy(), ora2["hidden"][0],
+                   pick, ora2["picks"][0], what="prefill after decode")
+    check_kv_planes(m, ref, wl, 93)
+    m.close()
+
+
+def test_tiny_prefill_bf16_cache(qw):
+    # a bf16 cache rounds every appended row; the oracle rounds its rows the same way
+    run_prefill(qw, qi.WORKLOADS["tiny"].with_(kv_format="bf16"), [200], kv_bf16_oracle=True, check_kv=False)
+
+
+def test_full_shape_prefill_ragged(qw):
+    # full Qwen3-0.6B shape, 320 rows: 2.5 row tiles, 5 key blocks
+    stats = run_prefill(qw, qi.WORKLOADS["qwen3_0p6b_prefill2048"], [320], check_kv=False, decode_after=1)
+    print(stats)
+
+
+def test_full_shape_int8_prefill(qw):
+    # the int8 workload's own prompt length; weights dequantised to fp16 once at creation
+    wl = qi.WORKLOADS["qwen3_0p6b_int8"]
+    stats = run_prefill(qw, wl, [wl.prompt_len], check_kv=False, decode_after=1)
+    print(stats)
+
+
+def test_full_prompt_2048_matches_decode_path(qw):
+    # The 2048-row prompt of the prefill workload, in the launch configuration the bench
+    # times, against the same model run token by token through the decode path (itself
+    # held to the oracle by the decode tests): last-row hidden states and logits, every
+    # appended K/V row, and the greedy pick.
+    wl = qi.WORKLOADS["qwen3_0p6b_prefill2048"]
+    host = qi.make_weights(wl)
+    dev = qw.weights_to_device(host, int8=False)
+    prompt = qi.prompt(wl)
+    res = {}
+    for by_token in (False, True):
+        m = qw.Model(wl, dev)
+        m.set_debug(qw.DEBUG_HIDDEN | (qw.DEBUG_PREFILL_BY_TOKEN if by_token else 0))
+        pick = m.prefill(prompt)
+        k, v = m.kv_export(len(prompt))
+        res[by_token] = (pick, m.logits().cpu().numpy(), m.debug_hidden().cpu().numpy(), k.float(), v.float())
+        m.close()
+    (pb, lb, hb, kb, vb), (pt, lt, ht, kt, vt) = res[False], res[True]
+    assert np.all(np.isfinite(lb))
+    rels = [rel_l2(a, b) for a, b in zip(hb, ht)]
+    assert max(rels) <= HIDDEN_REL_L2, rels
+    assert float(np.abs(lb - lt).max()) <= 5e-2
+    top2 = np.sort(lt)[-2:]
+    if top2[1] - top2[0] > 0.1:
+        assert pb == pt
+    kr = ((kb - kt).norm(dim=(2, 3)) / kt.norm(dim=(2, 3))).max().item()
+    vr = ((vb - vt).norm(dim=(2, 3)) / vt.norm(dim=(2, 3))).max().item()
+    assert kr <= KV_PLANE_REL_L2 and vr <= KV_PLANE_REL_L2, (kr, vr)
+    print({"hidden_rel_l2_max": max(rels), "logits_max_abs": float(np.abs(lb - lt).max()), "k": kr, "v": vr})
