@@ -255,11 +255,14 @@ class OracleModel:
             raise OracleError(rc, "kv_row")
         return k, v
 
-    def step(self, token: int, want_hidden: bool = False):
-        """One decode step: (logits [V], hidden [L+1, H] or None)."""
-        logits = np.empty(self.cfg.vocab, np.float32)
+    def step(self, token: int, want_hidden: bool = False, want_logits: bool = True):
+        """One decode step: (logits [V] or None, hidden [L+1, H] or None).
+
+        want_logits=False skips the final norm and head (a prompt row before the last)."""
+        logits = np.empty(self.cfg.vocab, np.float32) if want_logits else None
         hidden = np.empty((self.cfg.n_layers + 1, self.cfg.hidden), np.float32) if want_hidden else None
-        rc = lib().ora_step(self._h, int(token), _fp(logits), None if hidden is None else hidden.ctypes.data)
+        rc = lib().ora_step(self._h, int(token), None if logits is None else _fp(logits),
+                            None if hidden is None else hidden.ctypes.data)
         if rc:
             raise OracleError(rc, "step")
         return logits, hidden
@@ -289,7 +292,8 @@ def run_sequence(model: OracleModel, prompt, n_decode: int, want_hidden: bool = 
     out = {"logits": [], "hidden": [], "inputs": [], "picks": []}
     last = None
     for i, tok in enumerate(prompt):
-        logits, hid = model.step(int(tok), want_hidden and i == len(prompt) - 1)
+        is_last = i == len(prompt) - 1
+        logits, hid = model.step(int(tok), want_hidden and is_last, want_logits=is_last)
         last = logits
     if len(prompt):
         out["logits"].append(last)

@@ -522,7 +522,11 @@ static int head_logits(const ora_model *md, const float *x, float *logits, float
 /*
  * Decode one token at position len: logits [V] and, if hidden != NULL, the
  * residual stream [L+1][H] (index 0 = embedding row, l+1 = after layer l).
- * On an error the cache length is unchanged.
+ * logits == NULL skips the final norm and head: a prompt row other than the
+ * last only has to leave its K/V in the cache (final norm, head and argmax act
+ * on the last prompt row, "Portable WebAssembly Runtime Architecture for
+ * TinyRustLM", section "Prefill versus decode").  On an error the cache length
+ * is unchanged.
  */
 int ora_step(ora_model *md, int32_t token, float *logits, float *hidden) {
     const ora_config *c = &md->cfg;
@@ -539,7 +543,7 @@ int ora_step(ora_model *md, int32_t token, float *logits, float *hidden) {
         rc = layer_step(md, l, x, pos, buf);
         if (hidden) memcpy(hidden + (size_t)(l + 1) * H, x, sizeof(float) * H);
     }
-    if (!rc) rc = head_logits(md, x, logits, x + H);
+    if (!rc && logits) rc = head_logits(md, x, logits, x + H);
     free(x);
     free(buf);
     if (!rc) md->len = pos + 1;
