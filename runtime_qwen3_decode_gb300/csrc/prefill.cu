@@ -399,238 +399,353 @@ __global__ void qk_rope_kernel(const float *qkv, int n, int Hq, int Hkv, const _
     }
 }
 
-// ------------------------------------------------------------------ causal attention
+// ------------------------------------------------------------------ K/V fp16 shadows
 //
-// CTA = (query tile, KV head).  The 128 MMA rows are the G query heads of the KV
-// head stacked over 128/G positions: row r -> head kvh*G + r/(128/G), position
-// t0 + r%(128/G), so both heads of a group share every K/V tile.  Per 64-key block:
-// S = Q K^T (TMEM), the thread owning row r applies the causal mask and the online
-// softmax in the log2 domain, writes P (fp16) to shared memory, and O += P V
-// accumulates in TMEM.  O is rescaled only when the running max grows by more than 8
-// (factor 256): the final O / l uses one consistent reference max either way, and
-// p <= 2^8 stays well inside fp16.
+// The attention reads K as fp16 [Hkv][kv_rows][128] and V transposed, V^T fp16
+// [Hkv][128][kv_rows], both with TMA.  kv_shadow_kernel fills positions [0, n_pos) of
+// one layer from the cache (f32 or bf16) and zeroes [n_pos, n_fill), so every key a
+// 128-key block can touch holds a finite value (a masked key still meets p = 0 in P V).
 
-constexpr int kAttnThreads = 128;
-constexpr int kAttnKeys = 64;
-
-struct AttnParams {
-    const __half *q16;  // [Hq][q_rows][128]
-    int q_rows;
-    const void *kc, *vc;  // this layer's cache planes [Hkv][max_ctx][128]
-    int max_ctx;
-    __half *o16;        // [n][Hq * 128]
-    int n, pos0, Hq, G;
-    float scale_log2;   // log2(e) / sqrt(128)
-    StepFlags *flags;
-};
-
-struct AttnSmem {
-    static constexpr int kQ = 0;                   // 2 regions x [128 rows][128 B]
-    static constexpr int kK = kQ + 2 * 128 * 128;  // 2 regions x [64 keys][128 B]
-    static constexpr int kV = kK + 2 * 64 * 128;   // [128 dims][64 keys] fp16
-    static constexpr int kP = kV + 128 * 128;      // [128 rows][64 keys] fp16
-    static constexpr int kBar = kP + 128 * 128;
-    static constexpr int kBytes = kBar + 64;
-    static constexpr size_t kDyn = 1024 + kBytes;
-};
-// Two CTAs per SM at most (shared memory), each holding 256 TMEM columns.
-static_assert(3 * AttnSmem::kDyn > 228 * 1024, "a third attention CTA per SM would exceed TMEM");
+constexpr int kShadowPos = 64;
 
 template <typename KT>
-__device__ __forceinline__ float kv_load(const KT *p) {
-    if constexpr (sizeof(KT) == 4)
-        return *p;
-    else
-        return __bfloat162float(*p);
+__device__ __forceinline__ void load8(const KT *src, float (&f)[8]) {
+    if constexpr (sizeof(KT) == 4) {
+        const float4 a = reinterpret_cast<const float4 *>(src)[0], b = reinterpret_cast<const float4 *>(src)[1];
+        f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 v = __bfloat1622float2(h[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
 }
 
 template <typename KT>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnParams p) {
-    uint8_t *base = smem_base1024();
-    uint8_t *sQ = base + AttnSmem::kQ, *sK = base + AttnSmem::kK, *sV = base + AttnSmem::kV,
-            *sP = base + AttnSmem::kP;
-    uint64_t *bar_s = reinterpret_cast<uint64_t *>(base + AttnSmem::kBar);
-    uint64_t *bar_o = bar_s + 1;
-    uint64_t *bar_d = bar_s + 2;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_s + 3);
-    volatile int *sh_ok = reinterpret_cast<volatile int *>(tslot + 1);
-    volatile int *abort = sh_ok + 1;
+__global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *vc, int max_ctx, int n_pos, int n_fill,
+                                                       __half *k16, __half *v16t, int kv_rows) {
+    __shared__ __align__(16) __half vt[kHeadDim][kShadowPos + 8];  // padded rows (144 B, 16-B aligned)
+    const int p0 = blockIdx.x * kShadowPos, kvh = blockIdx.y;
+    const KT *ks = kc + (size_t)kvh * max_ctx * kHeadDim;
+    const KT *vs = vc + (size_t)kvh * max_ctx * kHeadDim;
+    __half *kd = k16 + (size_t)kvh * kv_rows * kHeadDim;
+    // thread -> (position, 8 dims): K straight through, V into shared memory transposed
+    for (int c = threadIdx.x; c < kShadowPos * 16; c += 256) {
+        const int j = c >> 4, d0 = (c & 15) * 8, p = p0 + j;
+        float fk[8], fv[8];
+        if (p < n_pos) {
+            load8(ks + (size_t)p * kHeadDim + d0, fk);
+            load8(vs + (size_t)p * kHeadDim + d0, fv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) fk[i] = fv[i] = 0.f;
+        }
+        if (p < n_fill) *reinterpret_cast<uint4 *>(kd + (size_t)p * kHeadDim + d0) = pack_half8(fk);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vt[d0 + i][j] = __float2half_rn(fv[i]);
+    }
+    __syncthreads();
+    // thread -> (dim, 8 positions): rows of V^T
+    __half *vd = v16t + (size_t)kvh * kHeadDim * kv_rows;
+    for (int c = threadIdx.x; c < kHeadDim * (kShadowPos / 8); c += 256) {
+        const int d = c >> 3, j0 = (c & 7) * 8;
+        if (p0 + j0 < n_fill)
+            *reinterpret_cast<uint4 *>(vd + (size_t)d * kv_rows + p0 + j0) =
+                *reinterpret_cast<const uint4 *>(&vt[d][j0]);
+    }
+}
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int QT = kAttnThreads / p.G;  // positions per tile
+// ------------------------------------------------------------------ causal attention
+//
+// CTA = (query tile, KV head).  The 128 MMA rows are the G query heads of the KV head
+// stacked over 128/G positions: row r -> head kvh*G + r/(128/G), position
+// t0 + r%(128/G), so both heads of a group share every K/V tile.  Per 128-key block j:
+//   S_j = Q K_j^T into one of two TMEM buffers (the tensor core computes S_{j+1} while
+//   the softmax warps work on S_j);
+//   the thread owning row r applies the causal mask and the online softmax in the log2
+//   domain and writes P_j (fp16) to one of two shared-memory buffers;
+//   O += P_j V_j accumulates in TMEM.
+// O is rescaled only when a row's running max grows by more than 8 (factor 256): O and
+// the row sum l always refer to the same reference max, so O / l is unaffected, and
+// p <= 2^8 stays well inside fp16.
+// Warp 0 issues TMA loads (Q once; K and V^T per block into two 2-stage rings, so K of
+// block j+2 streams in as soon as S_j is done while V waits for P V), warp 1 owns TMEM
+// and issues the MMAs, warps 2-5 run the softmax and the output epilogue.
+
+constexpr int kFaThreads = 192;
+constexpr int kFaKeys = 128;
+constexpr int kFaStages = 2;
+
+struct FaSmem {
+    static constexpr int kQ = 0;                         // 2 regions x [128 rows][128 B]
+    static constexpr int kKV = 2 * 16384;                // stages x (K 2 x 16 KB | V^T 2 x 16 KB)
+    static constexpr int kStage = 4 * 16384;
+    static constexpr int kP = kKV + kFaStages * kStage;  // 2 buffers x 2 regions x [128 rows][128 B]
+    static constexpr int kBar = kP + 2 * 2 * 16384;
+    static constexpr int kBytes = kBar + 256;
+    static constexpr size_t kDyn = 1024 + kBytes;
+};
+static_assert(FaSmem::kDyn <= 227 * 1024, "shared memory budget");
+
+struct FaParams {
+    int n, pos0, G, Hq;
+    int q_rows, kv_rows;  // rows per head of the q16 and k16 buffers (V^T: columns)
+    float scale_log2;     // log2(e) / sqrt(128)
+    __half *o16;          // [n][Hq * 128]
+    StepFlags *flags;
+};
+
+// Lane 0 waits (bounded) and the verdict is shared with the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *b, unsigned parity, volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(b, parity, abort, true, kWaitLimitNs);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kFaThreads, 1)
+    fa_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const FaParams p) {
+    uint8_t *base = smem_base1024();
+    uint8_t *sQ = base + FaSmem::kQ, *sKV = base + FaSmem::kKV, *sP = base + FaSmem::kP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + FaSmem::kBar);
+    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7,
+             *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *pv_done = bars + 15, *drain = bars + 17;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 18);
+    volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G, QT = 128 / G;
     const int ntq = (p.n + QT - 1) / QT;
     const int qt = ntq - 1 - (int)blockIdx.x;  // longest (latest) tiles first
     const int g = blockIdx.y;
     const int t0 = qt * QT;
-    const int head = g * p.G + tid / QT;
-    const int t = t0 + tid % QT;
-    const int pr = p.pos0 + t;
-    const bool valid = t < p.n;
-    const int kv_len = p.pos0 + p.n;
-    const int last = p.pos0 + min(t0 + QT, p.n) - 1;
-    const int nkb = last / kAttnKeys + 1;
-    const KT *kc = reinterpret_cast<const KT *>(p.kc) + (size_t)g * p.max_ctx * kHeadDim;
-    const KT *vc = reinterpret_cast<const KT *>(p.vc) + (size_t)g * p.max_ctx * kHeadDim;
+    const int nkb = (p.pos0 + min(t0 + QT, p.n) - 1) / kFaKeys + 1;
+    const int first_masked = (p.pos0 + t0) / kFaKeys;  // blocks from here on cross the diagonal
 
-    if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_d, 1);
-        *sh_ok = 1;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+        }
+        mbar_init(drain, 1);
         *abort = 0;
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
-    // this thread's query row -> swizzled Q tile (zeros past the prompt)
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q16 + ((size_t)head * p.q_rows + t) * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(sQ + (c >> 3) * (128 * 128) + swz128(tid, c & 7)) = v;
-        }
-    }
+    if (warp == 1) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    constexpr uint32_t idesc_s = idesc_f16_f32(128, kAttnKeys);
-    constexpr uint32_t idesc_o = idesc_f16_f32(128, kHeadDim);
+    const uint32_t tO = tmem + 256;  // S buffers at columns 0 and 128
 
-    float m_used = -INFINITY, l = 0.f;
-    unsigned phs = 0, pho = 0;
-    bool ok = true;
-    for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int k0 = kb * kAttnKeys;
-        // K block: thread -> key tid/2, dims 64*(tid&1) .. +63 (one swizzle region row)
-        {
-            const int j = tid >> 1, reg = tid & 1, key = k0 + j;
-            uint8_t *dst = sK + reg * (64 * 128);
-            const KT *src = kc + (size_t)key * kHeadDim + reg * 64;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float f[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = key < kv_len ? kv_load(src + 8 * c + i) : 0.f;
-                *reinterpret_cast<uint4 *>(dst + swz128(j, c)) = pack_half8(f);
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            int k_par[kFaStages] = {-1, -1}, v_par[kFaStages] = {-1, -1};
+            bool ok = true;
+            mbar_expect_tx(q_full, 4 * 8192);
+            for (int half = 0; half < 2; ++half) {
+                const int head = g * G + (G == 2 ? half : 0);
+                const int row = head * p.q_rows + t0 + (G == 2 ? 0 : 64 * half);
+                for (int reg = 0; reg < 2; ++reg)
+                    tma_load_2d(sQ + reg * 16384 + half * 8192, &tq, reg * 64, row, q_full);
+            }
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j % kFaStages;
+                const unsigned ph = (unsigned)(j / kFaStages) & 1u;
+                uint8_t *sk = sKV + st * FaSmem::kStage, *sv = sk + 2 * 16384;
+                if (!mbar_wait(&k_empty[st], ph ^ 1u, abort, true, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&k_full[st], 2 * 16384);
+                for (int reg = 0; reg < 2; ++reg)
+                    tma_load_2d(sk + reg * 16384, &tk, reg * 64, g * p.kv_rows + j * kFaKeys, &k_full[st]);
+                k_par[st] = (int)ph;
+                if (!mbar_wait(&v_empty[st], ph ^ 1u, abort, true, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&v_full[st], 2 * 16384);
+                for (int reg = 0; reg < 2; ++reg)
+                    tma_load_2d(sv + reg * 16384, &tv, j * kFaKeys + reg * 64, g * kHeadDim, &v_full[st]);
+                v_par[st] = (int)ph;
+            }
+            if (!ok) {
+                *abort = 1;
+                raise(p.flags, kErrInvariant);
+                // no copy may land in shared memory after this CTA has exited
+                mbar_wait(q_full, 0, abort, false, kWaitLimitNs);
+                for (int i = 0; i < kFaStages; ++i) {
+                    if (k_par[i] >= 0) mbar_wait(&k_full[i], (unsigned)k_par[i], abort, false, kWaitLimitNs);
+                    if (v_par[i] >= 0) mbar_wait(&v_full[i], (unsigned)v_par[i], abort, false, kWaitLimitNs);
+                }
             }
         }
-        // V block transposed: thread -> dim tid, 8 keys per 16-byte chunk
-        {
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer: S_j, then P_{j-1} V_{j-1}
+            constexpr uint32_t idesc = idesc_f16_f32(128, 128);
+            bool ok = mbar_wait(q_full, 0, abort, true, kWaitLimitNs);
+            for (int j = 0; ok && j <= nkb; ++j) {
+                if (j < nkb) {
+                    const int st = j % kFaStages;
+                    if (!mbar_wait(&k_full[st], (unsigned)(j / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
+                        (j >= 2 && !mbar_wait(&s_free[j & 1], (unsigned)((j - 2) >> 1) & 1u, abort, true,
+                                              kWaitLimitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *sk = sKV + st * FaSmem::kStage;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float f[8];
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint64_t ad = desc_sw128(su32(sQ + (k >> 2) * 16384)) + 2u * (k & 3);
+                        const uint64_t bd = desc_sw128(su32(sk + (k >> 2) * 16384)) + 2u * (k & 3);
+                        mma_f16(tmem + 128u * (j & 1), ad, bd, idesc, k != 0);
+                    }
+                    mma_commit(&s_full[j & 1]);
+                    mma_commit(&k_empty[st]);
+                }
+                if (j >= 1) {
+                    const int i = j - 1, st = i % kFaStages;
+                    if (!mbar_wait(&v_full[st], (unsigned)(i / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
+                        !mbar_wait(&p_full[i & 1], (unsigned)(i >> 1) & 1u, abort, true, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *pb = sP + (i & 1) * 32768, *sv = sKV + st * FaSmem::kStage + 2 * 16384;
+#pragma unroll
+                    for (int k = 0; k < kFaKeys / 16; ++k) {
+                        const uint64_t ad = desc_sw128(su32(pb + (k >> 2) * 16384)) + 2u * (k & 3);
+                        const uint64_t bd = desc_sw128(su32(sv + (k >> 2) * 16384)) + 2u * (k & 3);
+                        mma_f16(tO, ad, bd, idesc, i > 0 || k > 0);
+                    }
+                    mma_commit(&pv_done[i & 1]);
+                    mma_commit(&v_empty[st]);
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                raise(p.flags, kErrInvariant);
+            }
+            // every MMA this thread issued completes before TMEM is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, abort, false, kWaitLimitNs);
+        }
+    } else {
+        // ---- softmax warps 2..5: TMEM lane quarter q = warp % 4, row r = 32 q + lane
+        const int q = warp & 3, r = 32 * q + lane;
+        const int t = G == 2 ? t0 + (r & 63) : t0 + r;
+        const int head = g * G + (G == 2 ? (r >> 6) : 0);
+        const int pr = p.pos0 + t;
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkb; ++j) {
+            const int b = j & 1;
+            if (!warp_wait(&s_full[b], (unsigned)(j >> 1) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + 128u * b + 32u * c, s[c]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
+            const int k0 = j * kFaKeys;
+            const bool masked = j >= first_masked;
+            float mb = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kFaKeys; ++i) {
+                float &v = s[i >> 5][i & 31];
+                v = (!masked || k0 + i <= pr) ? v * p.scale_log2 : -INFINITY;
+                mb = fmaxf(mb, v);
+            }
+            const bool resc = mb > m_used + 8.f;
+            const float m_new = resc ? mb : m_used;
+            const float factor = resc ? exp2f(m_used - m_new) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // O must be complete up to P_{j-1} V_{j-1} before it is rescaled
+                if (!warp_wait(&pv_done[(j - 1) & 1], (unsigned)((j - 1) >> 1) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim; c += 32) {
+                    float o[32];
+                    tmem_ld32(tO + lb + c, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= factor;
+                    tmem_st32(tO + lb + c, o);
+                }
+            }
+            l *= factor;
+            m_used = m_new;
+            // P buffer b is free once P_{j-2} V_{j-2} has completed
+            if (j >= 2 && !warp_wait(&pv_done[b], (unsigned)((j - 2) >> 1) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            uint8_t *pb = sP + b * 32768;
+#pragma unroll
+            for (int c = 0; c < kFaKeys / 8; ++c) {
+                float e[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int key = k0 + 8 * c + i;
-                    f[i] = key < kv_len ? kv_load(vc + (size_t)key * kHeadDim + tid) : 0.f;
+                    const __half h = __float2half_rn(exp2f(s[c >> 2][8 * (c & 3) + i] - m_used));
+                    e[i] = __half2float(h);
+                    l += e[i];
                 }
-                *reinterpret_cast<uint4 *>(sV + swz128(tid, c)) = pack_half8(f);
+                *reinterpret_cast<uint4 *>(pb + (c >> 3) * 16384 + swz128(r, c & 7)) = pack_half8(e);
             }
+            fence_async_shared();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
-        fence_async_shared();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-#pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) {
-                const uint64_t ad = desc_sw128(su32(sQ + (k >> 2) * (128 * 128))) + 2u * (k & 3);
-                const uint64_t bd = desc_sw128(su32(sK + (k >> 2) * (64 * 128))) + 2u * (k & 3);
-                mma_f16(tS, ad, bd, idesc_s, k != 0);
-            }
-            mma_commit(bar_s);
-            if (!mbar_wait(bar_s, phs, abort, false, kWaitLimitNs)) *sh_ok = 0;
-        }
-        phs ^= 1u;
-        __syncthreads();
-        tc_fence_after();
-        if (!*sh_ok) {
-            ok = false;
-            break;
-        }
-        float s[2][32];
-        tmem_ld32(tS + lane_base, s[0]);
-        tmem_ld32(tS + lane_base + 32, s[1]);
-        float mb = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kAttnKeys; ++j) {
-            float &sj = s[j >> 5][j & 31];
-            sj = (k0 + j <= pr) ? sj * p.scale_log2 : -INFINITY;
-            mb = fmaxf(mb, sj);
-        }
-        const bool resc = mb > m_used + 8.f;
-        const float m_new = resc ? mb : m_used;
-        const float factor = resc ? exp2f(m_used - m_new) : 1.f;
-        if (kb > 0 && __any_sync(0xffffffffu, resc)) {
+        if (ok && !warp_wait(&pv_done[(nkb - 1) & 1], (unsigned)((nkb - 1) >> 1) & 1u, abort)) ok = false;
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim;
 #pragma unroll 1
             for (int c = 0; c < kHeadDim; c += 32) {
                 float o[32];
-                tmem_ld32(tO + lane_base + c, o);
+                tmem_ld32(tO + lb + c, o);
+                if (t < p.n) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= factor;
-                tmem_st32(tO + lane_base + c, o);
+                    for (int i = 0; i < 32; ++i) o[i] *= inv;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + c)[i] = pack_half8(o + 8 * i);
+                }
             }
+        } else if (lane == 0) {
+            *abort = 1;
+            raise(p.flags, kErrInvariant);
         }
-        l *= factor;
-        m_used = m_new;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            float e[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const __half h = __float2half_rn(exp2f(s[c >> 2][8 * (c & 3) + i] - m_used));
-                e[i] = __half2float(h);
-                l += e[i];
-            }
-            *reinterpret_cast<uint4 *>(sP + swz128(tid, c)) = pack_half8(e);
-        }
-        fence_async_shared();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-#pragma unroll
-            for (int k = 0; k < kAttnKeys / 16; ++k) {
-                const uint64_t ad = desc_sw128(su32(sP)) + 2u * k;
-                const uint64_t bd = desc_sw128(su32(sV)) + 2u * k;
-                mma_f16(tO, ad, bd, idesc_o, kb > 0 || k > 0);
-            }
-            mma_commit(bar_o);
-            if (!mbar_wait(bar_o, pho, abort, false, kWaitLimitNs)) *sh_ok = 0;
-        }
-        pho ^= 1u;
-        __syncthreads();
-        tc_fence_after();
-        if (!*sh_ok) ok = false;
-    }
-    if (ok) {
-        const float inv = 1.0f / l;
-        __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim;
-#pragma unroll 1
-        for (int c = 0; c < kHeadDim; c += 32) {
-            float o[32];
-            tmem_ld32(tO + lane_base + c, o);
-            if (valid) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= inv;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + c)[i] = pack_half8(o + 8 * i);
-            }
-        }
-    } else if (tid == 0) {
-        raise(p.flags, kErrInvariant);
-        mma_commit(bar_d);  // every MMA issued completes before TMEM is released
-        mbar_wait(bar_d, 0, abort, false, kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -785,8 +900,9 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 size_t align_up(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PrefillLayout {
-    size_t w16, x, h, qkv, q16, o16, act, tok, misc, total;
+    size_t w16, x, h, qkv, q16, o16, act, k16, v16t, tok, misc, total;
     size_t w_layer;  // fp16 weight elements per layer
+    int kv_rows;     // positions per head in the fp16 K / V^T shadows (max_ctx rounded up to 128)
 };
 
 PrefillLayout prefill_layout(const qw_config &c, int rows) {
@@ -807,6 +923,9 @@ PrefillLayout prefill_layout(const qw_config &c, int rows) {
     L.q16 = take((size_t)rows * QD * 2);
     L.o16 = take((size_t)rows * QD * 2);
     L.act = take((size_t)rows * I * 2);
+    L.kv_rows = (c.max_ctx + kFaKeys - 1) / kFaKeys * kFaKeys;
+    L.k16 = take((size_t)c.n_kv_heads * L.kv_rows * c.head_dim * 2);
+    L.v16t = take((size_t)c.n_kv_heads * L.kv_rows * c.head_dim * 2);
     L.tok = take((size_t)rows * 4);
     L.misc = take(64);
     L.total = off;
@@ -820,6 +939,7 @@ struct PrefillImpl {
     qw_config cfg;
     std::vector<DevLayer> host_layers;  // the model's layer table (device pointers)
     std::vector<CUtensorMap> wmaps;     // per layer: qkv, o, gate/up, down
+    CUtensorMap tq, tk, tv;             // attention operands: q16, k16, v16t
 };
 
 size_t prefill_workspace_bytes(const qw_config &c, int rows_max) { return prefill_layout(c, rows_max).total; }
@@ -831,11 +951,7 @@ cudaError_t prefill_prepare() {
     if ((e = set_gemm_attr<256, EPI_SWIGLU>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_ADD>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_STORE>()) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)AttnSmem::kDyn)) != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(attn_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)AttnSmem::kDyn);
+    return cudaFuncSetAttribute(fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FaSmem::kDyn);
 }
 
 int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, uint8_t *buf, size_t bytes,
@@ -860,6 +976,14 @@ int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_laye
     const int H = c.hidden, QD = c.n_heads * c.head_dim, KD = c.n_kv_heads * c.head_dim, I = c.intermediate;
     unsigned *overflow = reinterpret_cast<unsigned *>(buf + L.misc + 16);
     if (cudaMemsetAsync(buf + L.misc, 0, 64, stream) != cudaSuccess) return 1;
+    // attention operand rows past the prompt are read (and masked); they must hold finite values
+    if (cudaMemsetAsync(buf + L.q16, 0, L.o16 - L.q16, stream) != cudaSuccess ||
+        cudaMemsetAsync(buf + L.k16, 0, L.tok - L.k16, stream) != cudaSuccess)
+        return 1;
+    if (!make_map(&im->tq, buf + L.q16, c.n_heads * rows_max, kHeadDim, 64) ||
+        !make_map(&im->tk, buf + L.k16, c.n_kv_heads * L.kv_rows, kHeadDim, kFaKeys) ||
+        !make_map(&im->tv, buf + L.v16t, c.n_kv_heads * kHeadDim, L.kv_rows, kFaKeys))
+        return 1;
     const int int8 = c.weight_format == QW_W_INT8_G32 ? 1 : 0;
     im->wmaps.resize((size_t)c.n_layers * 4);
     for (int l = 0; l < c.n_layers; ++l) {
@@ -958,25 +1082,32 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
                 qk_rope_kernel<__nv_bfloat16><<<qg, 256, 0, stream>>>(
                     qkv, m, Hq, Hkv, hl[l].q_norm, hl[l].k_norm, a.rope, p0, a.eps, q16, st->rows_max,
                     reinterpret_cast<__nv_bfloat16 *>(kc), reinterpret_cast<__nv_bfloat16 *>(vc), a.max_ctx);
-            // causal attention over the cache rows [0, p0 + m)
-            AttnParams ap{};
-            ap.q16 = q16;
-            ap.q_rows = st->rows_max;
-            ap.kc = kc;
-            ap.vc = vc;
-            ap.max_ctx = a.max_ctx;
-            ap.o16 = o16;
-            ap.n = m;
-            ap.pos0 = p0;
-            ap.Hq = Hq;
-            ap.G = G;
-            ap.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
-            ap.flags = a.flags;
-            const dim3 ag((m + kAttnThreads / G - 1) / (kAttnThreads / G), Hkv);
+            // causal attention over the cache rows [0, p0 + m): fp16 shadows of this layer's K
+            // and V^T, then the tensor-core attention
+            const int kv_len = p0 + m;
+            const int n_fill = (kv_len + kFaKeys - 1) / kFaKeys * kFaKeys;
+            const dim3 sg(n_fill / kShadowPos, Hkv);
+            __half *k16 = reinterpret_cast<__half *>(buf + L.k16), *v16t = reinterpret_cast<__half *>(buf + L.v16t);
             if (a.kv_f32)
-                attn_kernel<float><<<ag, kAttnThreads, AttnSmem::kDyn, stream>>>(ap);
+                kv_shadow_kernel<float><<<sg, 256, 0, stream>>>(reinterpret_cast<const float *>(kc),
+                                                                 reinterpret_cast<const float *>(vc), a.max_ctx,
+                                                                 kv_len, n_fill, k16, v16t, L.kv_rows);
             else
-                attn_kernel<__nv_bfloat16><<<ag, kAttnThreads, AttnSmem::kDyn, stream>>>(ap);
+                kv_shadow_kernel<__nv_bfloat16><<<sg, 256, 0, stream>>>(
+                    reinterpret_cast<const __nv_bfloat16 *>(kc), reinterpret_cast<const __nv_bfloat16 *>(vc),
+                    a.max_ctx, kv_len, n_fill, k16, v16t, L.kv_rows);
+            FaParams fp{};
+            fp.n = m;
+            fp.pos0 = p0;
+            fp.G = G;
+            fp.Hq = Hq;
+            fp.q_rows = st->rows_max;
+            fp.kv_rows = L.kv_rows;
+            fp.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+            fp.o16 = o16;
+            fp.flags = a.flags;
+            const dim3 ag((m + 128 / G - 1) / (128 / G), Hkv);
+            fa_kernel<<<ag, kFaThreads, FaSmem::kDyn, stream>>>(im->tq, im->tk, im->tv, fp);
             // x += o Wo^T
             gp.N = H;
             gp.K = QD;
