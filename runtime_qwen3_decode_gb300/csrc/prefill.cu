@@ -48,7 +48,21 @@ constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle span of f
 constexpr int kGemmThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+enum { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+
+// Where the q|k|v epilogue puts a row's heads (QK-Norm + RoPE of q and k first).
+struct QkvOut {
+    const __nv_bfloat16 *q_norm, *k_norm;  // [128] each
+    const float2 *rope;                    // [max_ctx][64] (cos, sin)
+    int pos0, Hq, Hkv;
+    float eps;
+    __half *q16;                           // [Hq][q_rows][128]
+    int q_rows;
+    void *kc, *vc;                         // this layer's cache planes [Hkv][max_ctx][128]
+    int kv_f32, max_ctx;
+    __half *k16, *v16t;                    // fp16 shadows [Hkv][kv_rows][128] and [Hkv][128][kv_rows]
+    int kv_rows;
+};
 
 struct GemmParams {
     int M, N, K;       // rows, output columns, reduction length
@@ -56,6 +70,7 @@ struct GemmParams {
     int ldo;
     __half *act;       // EPI_SWIGLU: act[M][ldh], column block nt * BN/2
     int ldh;
+    QkvOut qkv;        // EPI_QKV
     StepFlags *flags;
 };
 
@@ -97,10 +112,93 @@ __device__ __forceinline__ uint4 pack_half8(const float *v) {
 
 // ------------------------------------------------------------------ GEMM epilogues
 
+// One 128-wide head of the q|k|v tile for prompt row t: QK-Norm and RoPE of q and k
+// heads (the decode kernel's arithmetic: r = rsqrt(mean(v^2) + eps), v = w * (v * r),
+// then dims (i, i + 64) rotated by the position's angle), then q -> q16, k and v -> the
+// cache plus their fp16 shadows.
+template <typename KT>
+__device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32], int slot, int t) {
+    const int P = o.pos0 + t;
+    if (slot < o.Hq + o.Hkv) {
+        const __nv_bfloat16 *w = slot < o.Hq ? o.q_norm : o.k_norm;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kHeadDim; ++i) ss += v[i >> 5][i & 31] * v[i >> 5][i & 31];
+        const float r = rsqrtf(ss * (1.0f / kHeadDim) + o.eps);
+#pragma unroll
+        for (int i = 0; i < kHeadDim; ++i) v[i >> 5][i & 31] = __bfloat162float(w[i]) * (v[i >> 5][i & 31] * r);
+        const float2 *cs = o.rope + (size_t)P * (kHeadDim / 2);
+#pragma unroll
+        for (int i = 0; i < kHeadDim / 2; ++i) {
+            const float2 c = cs[i];
+            const float a = v[i >> 5][i & 31], b = v[(i + 64) >> 5][i & 31];
+            v[i >> 5][i & 31] = a * c.x - b * c.y;
+            v[(i + 64) >> 5][i & 31] = b * c.x + a * c.y;
+        }
+    }
+    if (slot < o.Hq) {
+        uint4 *dst = reinterpret_cast<uint4 *>(o.q16 + ((size_t)slot * o.q_rows + t) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = pack_half8(&v[c >> 2][8 * (c & 3)]);
+        return;
+    }
+    const bool is_k = slot < o.Hq + o.Hkv;
+    const int kvh = is_k ? slot - o.Hq : slot - o.Hq - o.Hkv;
+    KT *row = reinterpret_cast<KT *>(is_k ? o.kc : o.vc) + ((size_t)kvh * o.max_ctx + P) * kHeadDim;
+    if constexpr (sizeof(KT) == 4) {
+        float4 *d4 = reinterpret_cast<float4 *>(row);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            d4[c] = make_float4(v[c >> 3][4 * (c & 7)], v[c >> 3][4 * (c & 7) + 1], v[c >> 3][4 * (c & 7) + 2],
+                                v[c >> 3][4 * (c & 7) + 3]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            uint4 u;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3)], v[c >> 2][8 * (c & 3) + 1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 2], v[c >> 2][8 * (c & 3) + 3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 4], v[c >> 2][8 * (c & 3) + 5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 6], v[c >> 2][8 * (c & 3) + 7]);
+            u.x = *reinterpret_cast<uint32_t *>(&b0);
+            u.y = *reinterpret_cast<uint32_t *>(&b1);
+            u.z = *reinterpret_cast<uint32_t *>(&b2);
+            u.w = *reinterpret_cast<uint32_t *>(&b3);
+            reinterpret_cast<uint4 *>(row)[c] = u;
+        }
+    }
+    // the attention's fp16 operands hold the cached value (bf16-rounded for a bf16 cache)
+    if constexpr (sizeof(KT) == 2) {
+#pragma unroll
+        for (int i = 0; i < kHeadDim; ++i) v[i >> 5][i & 31] = __bfloat162float(__float2bfloat16_rn(v[i >> 5][i & 31]));
+    }
+    if (is_k) {
+        uint4 *dst = reinterpret_cast<uint4 *>(o.k16 + ((size_t)kvh * o.kv_rows + P) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = pack_half8(&v[c >> 2][8 * (c & 3)]);
+    } else {
+        __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P;
+#pragma unroll
+        for (int i = 0; i < kHeadDim; ++i) dst[(size_t)i * o.kv_rows] = __float2half_rn(v[i >> 5][i & 31]);
+    }
+}
+
 template <int BN, int EPI>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int row, int nt) {
     const bool live = row < p.M;
-    if constexpr (EPI == EPI_SWIGLU) {
+    if constexpr (EPI == EPI_QKV) {
+#pragma unroll 1
+        for (int hl = 0; hl < BN / kHeadDim; ++hl) {
+            float v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tacc + hl * kHeadDim + 32 * c, v[c]);
+            if (!live) continue;
+            const int slot = nt * (BN / kHeadDim) + hl;
+            if (p.qkv.kv_f32)
+                qkv_head_out<float>(p.qkv, v, slot, row);
+            else
+                qkv_head_out<__nv_bfloat16>(p.qkv, v, slot, row);
+        }
+    } else if constexpr (EPI == EPI_SWIGLU) {
         constexpr int HB = BN / 2;  // gate columns [0, HB), matching up columns [HB, BN)
 #pragma unroll 1
         for (int c = 0; c < HB; c += 32) {
@@ -348,57 +446,6 @@ __global__ void __launch_bounds__(kRowThreads) norm_rows_kernel(float *x, const 
     }
 }
 
-// One warp per (row, head slot): slots [0, Hq) query heads, [Hq, Hq+Hkv) key heads,
-// [Hq+Hkv, Hq+2Hkv) value heads.  A lane holds dims (lane, lane+32, lane+64, lane+96);
-// RoPE pairs dim i with i + 64.
-template <typename KT>
-__global__ void qk_rope_kernel(const float *qkv, int n, int Hq, int Hkv, const __nv_bfloat16 *q_norm,
-                               const __nv_bfloat16 *k_norm, const float2 *rope, int pos0, float eps,
-                               __half *q16, int q_rows, KT *kc, KT *vc, int max_ctx) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slot = blockIdx.y * (blockDim.x >> 5) + warp;
-    const int t = blockIdx.x;
-    const int nslot = Hq + 2 * Hkv;
-    if (slot >= nslot || t >= n) return;
-    const float *src = qkv + (size_t)t * nslot * kHeadDim + (size_t)slot * kHeadDim;
-    float v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
-    const int P = pos0 + t;
-    if (slot < Hq + Hkv) {
-        const __nv_bfloat16 *nw = slot < Hq ? q_norm : k_norm;
-        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __bfloat162float(nw[lane + 32 * i]) * (v[i] * r);
-        const float2 c0 = rope[(size_t)P * (kHeadDim / 2) + lane];
-        const float2 c1 = rope[(size_t)P * (kHeadDim / 2) + lane + 32];
-        const float a0 = v[0], a1 = v[1], b0 = v[2], b1 = v[3];
-        v[0] = a0 * c0.x - b0 * c0.y;
-        v[2] = b0 * c0.x + a0 * c0.y;
-        v[1] = a1 * c1.x - b1 * c1.y;
-        v[3] = b1 * c1.x + a1 * c1.y;
-    }
-    if (slot < Hq) {
-        __half *dst = q16 + ((size_t)slot * q_rows + t) * kHeadDim;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = __float2half_rn(v[i]);
-    } else {
-        const bool is_k = slot < Hq + Hkv;
-        const int kvh = is_k ? slot - Hq : slot - Hq - Hkv;
-        KT *dst = (is_k ? kc : vc) + ((size_t)kvh * max_ctx + P) * kHeadDim;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if constexpr (sizeof(KT) == 4)
-                dst[lane + 32 * i] = v[i];
-            else
-                dst[lane + 32 * i] = __float2bfloat16_rn(v[i]);
-        }
-    }
-}
-
 // ------------------------------------------------------------------ K/V fp16 shadows
 //
 // The attention reads K as fp16 [Hkv][kv_rows][128] and V transposed, V^T fp16
@@ -466,17 +513,19 @@ __global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *
 // t0 + r%(128/G), so both heads of a group share every K/V tile.  Per 128-key block j:
 //   S_j = Q K_j^T into one of two TMEM buffers (the tensor core computes S_{j+1} while
 //   the softmax warps work on S_j);
-//   the thread owning row r applies the causal mask and the online softmax in the log2
-//   domain and writes P_j (fp16) to one of two shared-memory buffers;
+//   two warps per row apply the causal mask and the online softmax in the log2 domain,
+//   each over 64 of the block's keys, exchanging their block maxima through shared
+//   memory, and write P_j (fp16) to shared memory;
 //   O += P_j V_j accumulates in TMEM.
 // O is rescaled only when a row's running max grows by more than 8 (factor 256): O and
 // the row sum l always refer to the same reference max, so O / l is unaffected, and
 // p <= 2^8 stays well inside fp16.
 // Warp 0 issues TMA loads (Q once; K and V^T per block into two 2-stage rings, so K of
 // block j+2 streams in as soon as S_j is done while V waits for P V), warp 1 owns TMEM
-// and issues the MMAs, warps 2-5 run the softmax and the output epilogue.
+// and issues the MMAs, warps 2-9 run the softmax and the output epilogue.
 
-constexpr int kFaThreads = 192;
+constexpr int kFaSoftmaxWarps = 8;
+constexpr int kFaThreads = 64 + 32 * kFaSoftmaxWarps;
 constexpr int kFaKeys = 128;
 constexpr int kFaStages = 2;
 
@@ -484,8 +533,9 @@ struct FaSmem {
     static constexpr int kQ = 0;                         // 2 regions x [128 rows][128 B]
     static constexpr int kKV = 2 * 16384;                // stages x (K 2 x 16 KB | V^T 2 x 16 KB)
     static constexpr int kStage = 4 * 16384;
-    static constexpr int kP = kKV + kFaStages * kStage;  // 2 buffers x 2 regions x [128 rows][128 B]
-    static constexpr int kBar = kP + 2 * 2 * 16384;
+    static constexpr int kP = kKV + kFaStages * kStage;  // 2 regions x [128 rows][128 B]
+    static constexpr int kX = kP + 2 * 16384;            // block maxima [2 parity][2 halves][128 rows]
+    static constexpr int kBar = kX + 2 * 2 * 128 * 4;
     static constexpr int kBytes = kBar + 256;
     static constexpr size_t kDyn = 1024 + kBytes;
 };
@@ -506,15 +556,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t *b, unsigned parity, volatile
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// 2^x on the special-function unit (ex2.approx: about 2 ulp; 2^-inf = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __launch_bounds__(kFaThreads, 1)
     fa_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const FaParams p) {
     uint8_t *base = smem_base1024();
     uint8_t *sQ = base + FaSmem::kQ, *sKV = base + FaSmem::kKV, *sP = base + FaSmem::kP;
+    float *mx = reinterpret_cast<float *>(base + FaSmem::kX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + FaSmem::kBar);
     uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7,
-             *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *pv_done = bars + 15, *drain = bars + 17;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 18);
+             *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *pv_done = bars + 14, *xbar = bars + 15,
+             *drain = bars + 19;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 20);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -534,10 +593,11 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&pv_done[i], 1);
+            mbar_init(&s_free[i], kFaSoftmaxWarps);
         }
+        mbar_init(p_full, kFaSoftmaxWarps);
+        mbar_init(pv_done, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);  // the two warps of a lane quarter
         mbar_init(drain, 1);
         *abort = 0;
         mbar_fence_init();
@@ -621,19 +681,19 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                 if (j >= 1) {
                     const int i = j - 1, st = i % kFaStages;
                     if (!mbar_wait(&v_full[st], (unsigned)(i / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
-                        !mbar_wait(&p_full[i & 1], (unsigned)(i >> 1) & 1u, abort, true, kWaitLimitNs)) {
+                        !mbar_wait(p_full, (unsigned)i & 1u, abort, true, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *pb = sP + (i & 1) * 32768, *sv = sKV + st * FaSmem::kStage + 2 * 16384;
+                    const uint8_t *sv = sKV + st * FaSmem::kStage + 2 * 16384;
 #pragma unroll
                     for (int k = 0; k < kFaKeys / 16; ++k) {
-                        const uint64_t ad = desc_sw128(su32(pb + (k >> 2) * 16384)) + 2u * (k & 3);
+                        const uint64_t ad = desc_sw128(su32(sP + (k >> 2) * 16384)) + 2u * (k & 3);
                         const uint64_t bd = desc_sw128(su32(sv + (k >> 2) * 16384)) + 2u * (k & 3);
                         mma_f16(tO, ad, bd, idesc, i > 0 || k > 0);
                     }
-                    mma_commit(&pv_done[i & 1]);
+                    mma_commit(pv_done);
                     mma_commit(&v_empty[st]);
                 }
             }
@@ -646,12 +706,14 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             mbar_wait(drain, 0, abort, false, kWaitLimitNs);
         }
     } else {
-        // ---- softmax warps 2..5: TMEM lane quarter q = warp % 4, row r = 32 q + lane
-        const int q = warp & 3, r = 32 * q + lane;
+        // ---- softmax warps 2..9: lane quarter q = warp % 4, row r = 32 q + lane; warp half
+        // hf takes keys [64 hf, 64 hf + 64) of every block, P region hf and O dims [64 hf, +64)
+        const int q = warp & 3, hf = (warp - 2) >> 2, r = 32 * q + lane;
         const int t = G == 2 ? t0 + (r & 63) : t0 + r;
         const int head = g * G + (G == 2 ? (r >> 6) : 0);
         const int pr = p.pos0 + t;
-        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        const uint32_t lb = ((uint32_t)(32 * q) << 16) + 64u * hf;
+        const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
@@ -661,78 +723,93 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                 break;
             }
             tc_fence_after();
-            float s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + 128u * b + 32u * c, s[c]);
+            float s[2][32];
+            tmem_ld32(tmem + lb + 128u * b, s[0]);
+            tmem_ld32(tmem + lb + 128u * b + 32u, s[1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[b]);
-            const int k0 = j * kFaKeys;
-            const bool masked = j >= first_masked;
+            const int k0 = j * kFaKeys + 64 * hf;
             float mb = -INFINITY;
+            if (j >= first_masked) {
 #pragma unroll
-            for (int i = 0; i < kFaKeys; ++i) {
-                float &v = s[i >> 5][i & 31];
-                v = (!masked || k0 + i <= pr) ? v * p.scale_log2 : -INFINITY;
-                mb = fmaxf(mb, v);
+                for (int i = 0; i < 64; ++i) {
+                    float &v = s[i >> 5][i & 31];
+                    v = k0 + i <= pr ? v : -INFINITY;
+                    mb = fmaxf(mb, v);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) mb = fmaxf(mb, s[i >> 5][i & 31]);
             }
+            // the row's maximum over the whole block, from both halves
+            mx[(b * 2 + hf) * 128 + r] = mb;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[q]);
+            if (!warp_wait(&xbar[q], (unsigned)j & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            mb = fmaxf(mb, mx[(b * 2 + (hf ^ 1)) * 128 + r]) * sc;
             const bool resc = mb > m_used + 8.f;
             const float m_new = resc ? mb : m_used;
-            const float factor = resc ? exp2f(m_used - m_new) : 1.f;
+            const float factor = resc ? fast_exp2(m_used - m_new) : 1.f;
+            // O (for the rescale) and the P buffer are free once P_{j-1} V_{j-1} has completed
+            if (j >= 1 && !warp_wait(pv_done, (unsigned)(j - 1) & 1u, abort)) {
+                ok = false;
+                break;
+            }
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                // O must be complete up to P_{j-1} V_{j-1} before it is rescaled
-                if (!warp_wait(&pv_done[(j - 1) & 1], (unsigned)((j - 1) >> 1) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < kHeadDim; c += 32) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
                     float o[32];
-                    tmem_ld32(tO + lb + c, o);
+                    tmem_ld32(tO + lb + 32u * c, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= factor;
-                    tmem_st32(tO + lb + c, o);
+                    tmem_st32(tO + lb + 32u * c, o);
                 }
             }
             l *= factor;
             m_used = m_new;
-            // P buffer b is free once P_{j-2} V_{j-2} has completed
-            if (j >= 2 && !warp_wait(&pv_done[b], (unsigned)((j - 2) >> 1) & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            uint8_t *pb = sP + b * 32768;
+            uint8_t *pb = sP + hf * 16384;
 #pragma unroll
-            for (int c = 0; c < kFaKeys / 8; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 float e[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const __half h = __float2half_rn(exp2f(s[c >> 2][8 * (c & 3) + i] - m_used));
-                    e[i] = __half2float(h);
+                    e[i] = fast_exp2(fmaf(s[c >> 2][8 * (c & 3) + i], sc, -m_used));
                     l += e[i];
                 }
-                *reinterpret_cast<uint4 *>(pb + (c >> 3) * 16384 + swz128(r, c & 7)) = pack_half8(e);
+                *reinterpret_cast<uint4 *>(pb + swz128(r, c)) = pack_half8(e);
             }
             fence_async_shared();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
+            if (lane == 0) mbar_arrive(p_full);
         }
-        if (ok && !warp_wait(&pv_done[(nkb - 1) & 1], (unsigned)((nkb - 1) >> 1) & 1u, abort)) ok = false;
+        // row sum over both halves (the exchange buffer of the parity after the last block)
+        if (ok) {
+            mx[((nkb & 1) * 2 + hf) * 128 + r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[q]);
+            ok = warp_wait(&xbar[q], (unsigned)nkb & 1u, abort);
+        }
+        if (ok) l += mx[((nkb & 1) * 2 + (hf ^ 1)) * 128 + r];
+        if (ok && !warp_wait(pv_done, (unsigned)(nkb - 1) & 1u, abort)) ok = false;
         if (ok) {
             tc_fence_after();
             const float inv = 1.0f / l;
-            __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim;
-#pragma unroll 1
-            for (int c = 0; c < kHeadDim; c += 32) {
+            __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim + 64 * hf;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 float o[32];
-                tmem_ld32(tO + lb + c, o);
+                tmem_ld32(tO + lb + 32u * c, o);
                 if (t < p.n) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= inv;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + c)[i] = pack_half8(o + 8 * i);
+                    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + 32 * c)[i] = pack_half8(o + 8 * i);
                 }
             }
         } else if (lane == 0) {
@@ -900,7 +977,7 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 size_t align_up(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PrefillLayout {
-    size_t w16, x, h, qkv, q16, o16, act, k16, v16t, tok, misc, total;
+    size_t w16, x, h, q16, o16, act, k16, v16t, tok, misc, total;
     size_t w_layer;  // fp16 weight elements per layer
     int kv_rows;     // positions per head in the fp16 K / V^T shadows (max_ctx rounded up to 128)
 };
@@ -919,7 +996,6 @@ PrefillLayout prefill_layout(const qw_config &c, int rows) {
     L.w16 = take((size_t)c.n_layers * L.w_layer * 2);
     L.x = take((size_t)rows * H * 4);
     L.h = take((size_t)rows * (H > I ? H : I) * 2);
-    L.qkv = take((size_t)rows * (QD + 2 * KD) * 4);
     L.q16 = take((size_t)rows * QD * 2);
     L.o16 = take((size_t)rows * QD * 2);
     L.act = take((size_t)rows * I * 2);
@@ -948,6 +1024,7 @@ cudaError_t prefill_prepare() {
     cudaError_t e = load_encoder();
     if (e != cudaSuccess) return e;
     if ((e = set_gemm_attr<256, EPI_STORE>()) != cudaSuccess) return e;
+    if ((e = set_gemm_attr<256, EPI_QKV>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<256, EPI_SWIGLU>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_ADD>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_STORE>()) != cudaSuccess) return e;
@@ -1033,10 +1110,8 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
     uint8_t *buf = st->buf;
     const int H = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, QD = Hq * kHeadDim, KD = Hkv * kHeadDim,
               I = c.intermediate, G = Hq / Hkv;
-    const int nslot = Hq + 2 * Hkv;
     float *x = reinterpret_cast<float *>(buf + L.x);
     __half *h = reinterpret_cast<__half *>(buf + L.h);
-    float *qkv = reinterpret_cast<float *>(buf + L.qkv);
     __half *q16 = reinterpret_cast<__half *>(buf + L.q16);
     __half *o16 = reinterpret_cast<__half *>(buf + L.o16);
     __half *act = reinterpret_cast<__half *>(buf + L.act);
@@ -1064,38 +1139,43 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             GemmParams gp{};
             gp.flags = a.flags;
             gp.M = m;
-            // q | k | v
-            gp.N = QD + 2 * KD;
-            gp.K = H;
-            gp.out = qkv;
-            gp.ldo = QD + 2 * KD;
-            if (launch_gemm<256, EPI_STORE>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
             uint8_t *kc = reinterpret_cast<uint8_t *>(a.kc) + (size_t)l * kv_plane;
             uint8_t *vc = reinterpret_cast<uint8_t *>(a.vc) + (size_t)l * kv_plane;
-            const dim3 qg(m, (nslot + 7) / 8);
-            if (a.kv_f32)
-                qk_rope_kernel<float><<<qg, 256, 0, stream>>>(qkv, m, Hq, Hkv, hl[l].q_norm, hl[l].k_norm, a.rope,
-                                                              p0, a.eps, q16, st->rows_max,
-                                                              reinterpret_cast<float *>(kc),
-                                                              reinterpret_cast<float *>(vc), a.max_ctx);
-            else
-                qk_rope_kernel<__nv_bfloat16><<<qg, 256, 0, stream>>>(
-                    qkv, m, Hq, Hkv, hl[l].q_norm, hl[l].k_norm, a.rope, p0, a.eps, q16, st->rows_max,
-                    reinterpret_cast<__nv_bfloat16 *>(kc), reinterpret_cast<__nv_bfloat16 *>(vc), a.max_ctx);
-            // causal attention over the cache rows [0, p0 + m): fp16 shadows of this layer's K
-            // and V^T, then the tensor-core attention
-            const int kv_len = p0 + m;
-            const int n_fill = (kv_len + kFaKeys - 1) / kFaKeys * kFaKeys;
-            const dim3 sg(n_fill / kShadowPos, Hkv);
             __half *k16 = reinterpret_cast<__half *>(buf + L.k16), *v16t = reinterpret_cast<__half *>(buf + L.v16t);
-            if (a.kv_f32)
-                kv_shadow_kernel<float><<<sg, 256, 0, stream>>>(reinterpret_cast<const float *>(kc),
-                                                                 reinterpret_cast<const float *>(vc), a.max_ctx,
-                                                                 kv_len, n_fill, k16, v16t, L.kv_rows);
-            else
-                kv_shadow_kernel<__nv_bfloat16><<<sg, 256, 0, stream>>>(
-                    reinterpret_cast<const __nv_bfloat16 *>(kc), reinterpret_cast<const __nv_bfloat16 *>(vc),
-                    a.max_ctx, kv_len, n_fill, k16, v16t, L.kv_rows);
+            // fp16 shadows of cache rows written before this chunk (earlier chunks, decode
+            // steps or an import); the chunk's own rows come from the q|k|v epilogue below
+            if (p0 > 0) {
+                const dim3 sg((p0 + kShadowPos - 1) / kShadowPos, Hkv);
+                if (a.kv_f32)
+                    kv_shadow_kernel<float><<<sg, 256, 0, stream>>>(reinterpret_cast<const float *>(kc),
+                                                                     reinterpret_cast<const float *>(vc), a.max_ctx,
+                                                                     p0, p0, k16, v16t, L.kv_rows);
+                else
+                    kv_shadow_kernel<__nv_bfloat16><<<sg, 256, 0, stream>>>(
+                        reinterpret_cast<const __nv_bfloat16 *>(kc), reinterpret_cast<const __nv_bfloat16 *>(vc),
+                        a.max_ctx, p0, p0, k16, v16t, L.kv_rows);
+            }
+            // q | k | v with QK-Norm, RoPE, the K/V append and the shadows in the epilogue
+            gp.N = QD + 2 * KD;
+            gp.K = H;
+            QkvOut &qo = gp.qkv;
+            qo.q_norm = hl[l].q_norm;
+            qo.k_norm = hl[l].k_norm;
+            qo.rope = a.rope;
+            qo.pos0 = p0;
+            qo.Hq = Hq;
+            qo.Hkv = Hkv;
+            qo.eps = a.eps;
+            qo.q16 = q16;
+            qo.q_rows = st->rows_max;
+            qo.kc = kc;
+            qo.vc = vc;
+            qo.kv_f32 = a.kv_f32;
+            qo.max_ctx = a.max_ctx;
+            qo.k16 = k16;
+            qo.v16t = v16t;
+            qo.kv_rows = L.kv_rows;
+            if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
             FaParams fp{};
             fp.n = m;
             fp.pos0 = p0;
