@@ -474,70 +474,6 @@ __device__ __forceinline__ bool poll_vec(const unsigned long long *src, unsigned
     return true;
 }
 
-// sm.vec[h*128 + d] = attention output of query head h: the exact merge of the S
-// split partials (acc, running max m, running sum l; log2 domain) written by the
-// attention phase, o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s,
-// accumulated with online rescaling.  Thread t merges 16 dims of one head; two
-// splits are polled per round.
-constexpr int kMergeDims = 16;
-constexpr int kMergeWords = 2 + kMergeDims;
-
-__device__ __forceinline__ void merge_split(const unsigned long long (&w)[kMergeWords], float &mx, float &ls,
-                                            float (&acc)[kMergeDims]) {
-    const float ms = tag_val(w[0]);
-    if (ms == -INFINITY) return;
-    const float mn = fmaxf(mx, ms);
-    const float sa = (mx == -INFINITY) ? 0.f : exp2f(mx - mn), sb = exp2f(ms - mn);
-    ls = ls * sa + tag_val(w[1]) * sb;
-#pragma unroll
-    for (int e = 0; e < kMergeDims; ++e) acc[e] = acc[e] * sa + tag_val(w[2 + e]) * sb;
-    mx = mn;
-}
-
-__device__ __forceinline__ bool load_split(const unsigned long long *pp, int d0, unsigned tag,
-                                           unsigned long long (&w)[kMergeWords]) {
-    ld_tag2(pp + kHeadDim, w[0], w[1]);
-#pragma unroll
-    for (int e = 0; e < kMergeDims; e += 2) ld_tag2(pp + d0 + e, w[2 + e], w[3 + e]);
-    bool ok = true;
-#pragma unroll
-    for (int e = 0; e < kMergeWords; ++e) ok &= tag_is(w[e], tag);
-    return ok;
-}
-
-template <int G>
-__device__ __forceinline__ bool stage_attn_merge(unsigned tag) {
-    Smem &sm = smem();
-    const DecodeArgs &a = sm.args;
-    const int S = a.n_split;
-    const int base = ctid() * kMergeDims;
-    if (base >= a.Hq * kHeadDim) return true;
-    const int h = base / kHeadDim, d0 = base % kHeadDim;
-    const unsigned long long *p0 = a.partt + ((size_t)(h / G) * S * G + (h % G)) * kPartStride;
-    const size_t sstride = (size_t)G * kPartStride;
-    float mx = -INFINITY, ls = 0.f, acc[kMergeDims];
-#pragma unroll
-    for (int e = 0; e < kMergeDims; ++e) acc[e] = 0.f;
-    for (int s = 0; s < S; s += 2) {
-        const bool two = s + 1 < S;
-        unsigned long long w0[kMergeWords], w1[kMergeWords];
-        unsigned long long t0 = 0;
-        for (unsigned i = 0;; ++i) {
-            bool ok = load_split(p0 + s * sstride, d0, tag, w0);
-            if (two) ok &= load_split(p0 + (s + 1) * sstride, d0, tag, w1);
-            if (ok) break;
-            if (!poll_more(i, t0, a.flags)) return false;
-        }
-        merge_split(w0, mx, ls, acc);
-        if (two) merge_split(w1, mx, ls, acc);
-    }
-    float4 *d = reinterpret_cast<float4 *>(sm.vec + base);
-#pragma unroll
-    for (int e = 0; e < kMergeDims; e += 4)
-        d[e / 4] = make_float4(acc[e] / ls, acc[e + 1] / ls, acc[e + 2] / ls, acc[e + 3] / ls);
-    return true;
-}
-
 // Raw weight piece m (8 columns 8*(lane + 32 m) ..) of stored row j of a slot holding ns
 // rows: 16 bytes of bf16, or 8 bytes of int8 codes plus their group's fp16 scale.
 template <int KM, bool I8>
@@ -643,9 +579,7 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (!phase_wait(ph)) return kFailed;
     bool ok = true;
     float4 *vec4 = reinterpret_cast<float4 *>(sm.vec);
-    if constexpr (PT == T_OPROJ) {
-        ok = stage_attn_merge<G>(in_tag);
-    } else {
+    {
         if (embed) {
             const uint2 *row = reinterpret_cast<const uint2 *>(a.embed + (size_t)sm.tok * a.H);
 #pragma unroll
@@ -659,7 +593,7 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
                 }
             }
         } else {
-            const unsigned long long *src = PT == T_GATEUP ? a.xb : PT == T_DOWN ? a.actt : a.xa;
+            const unsigned long long *src = PT == T_GATEUP ? a.xb : PT == T_DOWN ? a.actt : PT == T_OPROJ ? a.ot : a.xa;
             ok = poll_vec<KM>(src, in_tag, v, a.flags);
         }
     }
@@ -684,7 +618,7 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
                 vec4[idx] = make_float4(nw[i].x * (v[i].x * r), nw[i].y * (v[i].y * r), nw[i].z * (v[i].z * r),
                                         nw[i].w * (v[i].w * r));
         }
-    } else if constexpr (PT != T_OPROJ) {
+    } else {
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
             const int idx = tid + kConsumerThreads * i;
@@ -1041,6 +975,59 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
             st_tag(pp + kHeadDim, mx, out_tag);
             st_tag(pp + kHeadDim + 1, ls, out_tag);
         }
+    }
+    // The CTA that finishes the last split of this KV head merges all S partials into the
+    // group's attention output (once, instead of in every o_proj CTA):
+    // o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s.
+    bar_consumers();
+    if (tid == 0) {
+        __threadfence();  // this CTA's partial before its count
+        unsigned *ctr = a.merge + (size_t)l * kMaxKvHeads + kvh;
+        sm.flag = atomicAdd(ctr, 1u) + 1u == (unsigned)S;
+        if (sm.flag) *ctr = 0u;  // every split has counted; the next use is the next step
+    }
+    bar_consumers();
+    if (sm.flag) {
+        __threadfence();  // the other splits' partials, published before their counts
+        bool ok = true;
+        for (int t = tid; t < G * kHeadDim && ok; t += kConsumerThreads) {
+            const int h = t / kHeadDim, dim = t % kHeadDim;
+            const unsigned long long *p0 = a.partt + ((size_t)kvh * S * G + h) * kPartStride;
+            float mx = -INFINITY, ls = 0.f, av = 0.f;
+            for (int s0 = 0; s0 < S && ok; s0 += 4) {
+                unsigned long long w[4][3];
+                unsigned long long t0 = 0;
+                for (unsigned i = 0;; ++i) {
+                    bool got = true;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (s0 + k >= S) break;
+                        const unsigned long long *pp = p0 + (size_t)(s0 + k) * G * kPartStride;
+                        ld_tag2(pp + kHeadDim, w[k][0], w[k][1]);
+                        w[k][2] = ld_tag(pp + dim);
+                        got &= tag_is(w[k][0], out_tag) && tag_is(w[k][1], out_tag) && tag_is(w[k][2], out_tag);
+                    }
+                    if (got) break;
+                    if (!poll_more(i, t0, a.flags)) {
+                        ok = false;
+                        break;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (!ok || s0 + k >= S) break;
+                    const float ms = tag_val(w[k][0]);
+                    if (ms == -INFINITY) continue;
+                    const float mn = fmaxf(mx, ms);
+                    const float sa = (mx == -INFINITY) ? 0.f : exp2f(mx - mn), sb = exp2f(ms - mn);
+                    ls = ls * sa + tag_val(w[k][1]) * sb;
+                    av = av * sa + tag_val(w[k][2]) * sb;
+                    mx = mn;
+                }
+            }
+            if (ok) st_tag(a.ot + (size_t)(kvh * G + h) * kHeadDim + dim, av / ls, out_tag);
+        }
+        if (!all_ok(ok)) return kFailed;
     }
     return (int)(it | (dead ? kDeadBit : 0u));
 }

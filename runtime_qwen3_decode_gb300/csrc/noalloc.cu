@@ -34,7 +34,7 @@ constexpr size_t kOffFlags = 0;         // StepFlags
 constexpr size_t kOffStep = 256;        // argmax keys [2] + arrival counters [5 L + 1]
 constexpr size_t kOffLayers = 2048;     // DevLayer [n_layers]
 constexpr size_t kOffRope = 12288;      // float2 [head_dim / 2], this call's position
-constexpr size_t kOffTagged = 16384;    // tagged words: xa, xb, qkvt, actt, partt
+constexpr size_t kOffTagged = 16384;    // tagged words: xa, xb, qkvt, actt, partt, ot; then merge counters
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -45,7 +45,7 @@ uint32_t g_seq[kMaxDevices];     // tag sequence of the last call on each device
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct TaggedLayout {
-    size_t xa, xb, qkvt, actt, partt, end;
+    size_t xa, xb, qkvt, actt, partt, ot, merge, end;
 };
 
 TaggedLayout tagged_layout(const qw_config &c, int ncta) {
@@ -62,6 +62,10 @@ TaggedLayout tagged_layout(const qw_config &c, int ncta) {
     off += align256((size_t)c.intermediate * 8);
     t.partt = off;
     off += align256((size_t)ncta * g * qw::kPartStride * 8);
+    t.ot = off;
+    off += align256((size_t)c.n_heads * c.head_dim * 8);
+    t.merge = off;
+    off += align256(qw::merge_block_bytes(c.n_layers));
     t.end = off;
     return t;
 }
@@ -189,6 +193,9 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
         rc = cuda_rc(cudaMemcpyAsync(base + kOffRope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice,
                                      stream), "cudaMemcpyAsync");
     if (!rc) rc = cuda_rc(cudaMemsetAsync(base + kOffFlags, 0, kOffLayers, stream), "cudaMemsetAsync");
+    if (!rc)
+        rc = cuda_rc(cudaMemsetAsync(base + t.merge, 0, qw::merge_block_bytes(cfg->n_layers), stream),
+                     "cudaMemsetAsync");
     if (rc) return rc;
     // the two host sources are locals of this call: wait until the copies have run
     rc = cuda_rc(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
@@ -218,6 +225,8 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     a.qkvt = (unsigned long long *)(base + t.qkvt);
     a.actt = (unsigned long long *)(base + t.actt);
     a.partt = (unsigned long long *)(base + t.partt);
+    a.ot = (unsigned long long *)(base + t.ot);
+    a.merge = (unsigned *)(base + t.merge);
     a.logits = logits_dev;
     a.hidden = nullptr;
     a.key = (unsigned long long *)(base + kOffStep);

@@ -24,7 +24,7 @@ constexpr size_t kAlign = 256;
 constexpr int kPrefillRowsMax = 2048;
 
 struct Layout {
-    size_t kc, vc, rope, layers, xa, xb, qkvt, actt, partt, logits, hidden, step, flags, trace;
+    size_t kc, vc, rope, layers, xa, xb, qkvt, actt, partt, ot, logits, hidden, step, merge, flags, trace;
     size_t tagged_begin, tagged_end;
     size_t prefill, prefill_bytes;
     size_t total;
@@ -80,10 +80,12 @@ int make_layout(const qw_config *c, Layout *L) {
     L->qkvt = take((size_t)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim * 8);
     L->actt = take((size_t)c->intermediate * 8);
     L->partt = take((size_t)kMaxCtas * g * qw::kPartStride * 8);
+    L->ot = take((size_t)c->n_heads * c->head_dim * 8);
     L->tagged_end = off;
     L->logits = take((size_t)c->vocab * 4);
     L->hidden = take((size_t)(c->n_layers + 1) * c->hidden * 4);
     L->step = take(qw::step_block_bytes(c->n_layers));
+    L->merge = take(qw::merge_block_bytes(c->n_layers));
     L->flags = take(sizeof(qw::StepFlags));
     L->trace = take(((size_t)qw::kPhasesPerLayer * c->n_layers + 1) * kMaxCtas * qw::kTraceStamps * 8);
     const int rows = c->max_ctx < kPrefillRowsMax ? c->max_ctx : kPrefillRowsMax;
@@ -308,7 +310,9 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
         rc = cuda_status(cudaMemcpyAsync(ws + L.layers, host_layers.data(), host_layers.size() * sizeof(qw::DevLayer),
                                          cudaMemcpyHostToDevice, m->stream));
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.flags, 0, sizeof(qw::StepFlags), m->stream));
-    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, qw::step_block_bytes(cfg->n_layers), m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, L.merge + qw::merge_block_bytes(cfg->n_layers) - L.step,
+                                         m->stream));
     // tagged exchange words start with tag 0, which no step ever uses
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.tagged_begin, 0, L.tagged_end - L.tagged_begin, m->stream));
     if (!rc) rc = cuda_status(cudaStreamSynchronize(m->stream));  // host staging buffers go out of scope
@@ -340,6 +344,8 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     a.qkvt = (unsigned long long *)(ws + L.qkvt);
     a.actt = (unsigned long long *)(ws + L.actt);
     a.partt = (unsigned long long *)(ws + L.partt);
+    a.ot = (unsigned long long *)(ws + L.ot);
+    a.merge = (unsigned *)(ws + L.merge);
     a.logits = (float *)(ws + L.logits);
     a.hidden = (float *)(ws + L.hidden);
     a.key = (unsigned long long *)(ws + L.step);
@@ -347,7 +353,7 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     a.flags = (qw::StepFlags *)(ws + L.flags);
     m->flags = a.flags;
     m->step_block = ws + L.step;
-    m->step_bytes = qw::step_block_bytes(cfg->n_layers);
+    m->step_bytes = L.merge + qw::merge_block_bytes(cfg->n_layers) - L.step;  // counters and merge counters
     m->logits = a.logits;
     m->hidden = a.hidden;
     if (qw::prefill_init(&m->pf, *cfg, host_layers.data(), ws + L.prefill, L.prefill_bytes,

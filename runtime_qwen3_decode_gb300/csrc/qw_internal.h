@@ -27,6 +27,7 @@ constexpr int kSlots = 6;
 __host__ __device__ constexpr int kv_chunk_rows(int elem_bytes) { return 4 * kConsumerWarps * (4 / elem_bytes); }
 constexpr int kPartStride = kHeadDim + 4;    // split-attention partial: acc[128], max, sum, 2 pad (16-B rows)
 constexpr int kMaxOwnRows = 64;             // residual rows per CTA kept in shared memory
+constexpr int kMaxKvHeads = 32;             // split-merge counters per layer
 
 // Debug timeline stamps per (phase, CTA): consumer before wait, after wait, after
 // compute, after arrive; producer first issue, last issue of the phase.
@@ -72,6 +73,9 @@ struct DecodeArgs {
     unsigned long long *qkvt;        // [(Hq + 2 Hkv) * 128]
     unsigned long long *actt;        // SwiGLU output [I]
     unsigned long long *partt;       // split-attention partials [Hkv][S][G][kPartStride]
+    unsigned long long *ot;          // attention output, the merged partials [Hq * 128]
+    unsigned *merge;                 // finished splits per (layer, KV head) [L][kMaxKvHeads]; the
+                                     // merging CTA sets its counter back to 0
     float *logits;                   // [V]
     float *hidden;                   // [(L + 1) H] debug dump
     unsigned *sync;                  // arrivals per phase [5L+1]; each step adds the CTA count
@@ -89,6 +93,7 @@ struct DecodeArgs {
 // Step bookkeeping: two argmax keys then the per-phase arrival counters (zeroed at
 // creation, by qw_kv_reset and when the counters would overflow).
 inline size_t step_block_bytes(int L) { return 16 + 4 * ((size_t)kPhasesPerLayer * L + 1); }
+inline size_t merge_block_bytes(int L) { return 4 * (size_t)kMaxKvHeads * L; }
 
 size_t decode_smem_bytes();
 cudaError_t decode_prepare(int group, int *blocks_per_sm);
