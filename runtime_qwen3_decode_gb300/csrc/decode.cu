@@ -135,6 +135,10 @@ __device__ __forceinline__ unsigned long long policy_evict_normal() {
     return p;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
@@ -390,6 +394,7 @@ __device__ __noinline__ void producer() {
 
 constexpr int kFailed = -1;                 // uniform: the step is aborting
 constexpr unsigned kDeadBit = 0x80000000u;  // this warp gave up inside a chunk loop
+constexpr int kFusedChunks = kSlots - 2;     // phases with at most this many chunks take them all at once
 
 __device__ __forceinline__ int ctid() { return threadIdx.x; }
 __device__ __forceinline__ int cwarp() { return threadIdx.x >> 5; }
@@ -474,15 +479,16 @@ __device__ __forceinline__ bool poll_vec(const unsigned long long *src, unsigned
     return true;
 }
 
-// Raw weight piece m (8 columns 8*(lane + 32 m) ..) of stored row j of a slot holding ns
-// rows: 16 bytes of bf16, or 8 bytes of int8 codes plus their group's fp16 scale.
+// Raw weight piece m (8 columns 8*(lane + 32 m) ..) of one stored row: 16 bytes of
+// bf16, or 8 bytes of int8 codes plus their group's fp16 scale.  row points at the
+// row's weights in a slot; srow at its scales (int8 only).
 template <int KM, bool I8>
 struct WPiece;
 template <int KM>
 struct WPiece<KM, false> {
     uint4 v;
-    __device__ __forceinline__ void load(const uint8_t *sp, int, int j, int lane, int m) {
-        v = reinterpret_cast<const uint4 *>(sp + (size_t)j * (2048 * KM))[lane + 32 * m];
+    __device__ __forceinline__ void load(const uint8_t *row, const uint8_t *, int lane, int m) {
+        v = reinterpret_cast<const uint4 *>(row)[lane + 32 * m];
     }
     __device__ __forceinline__ void unpack(float (&w)[8]) const {
         w[0] = bf_lo(v.x); w[1] = bf_hi(v.x); w[2] = bf_lo(v.y); w[3] = bf_hi(v.y);
@@ -493,9 +499,9 @@ template <int KM>
 struct WPiece<KM, true> {
     uint2 v;
     __half s;
-    __device__ __forceinline__ void load(const uint8_t *sp, int ns, int j, int lane, int m) {
-        v = reinterpret_cast<const uint2 *>(sp + (size_t)j * (1024 * KM))[lane + 32 * m];
-        s = reinterpret_cast<const __half *>(sp + (size_t)ns * (1024 * KM) + (size_t)j * (64 * KM))[(lane + 32 * m) >> 2];
+    __device__ __forceinline__ void load(const uint8_t *row, const uint8_t *srow, int lane, int m) {
+        v = reinterpret_cast<const uint2 *>(row)[lane + 32 * m];
+        s = reinterpret_cast<const __half *>(srow)[(lane + 32 * m) >> 2];
     }
     // int8 group-32 codes dequantised in registers: w = f32(q) * f32(s), an exact product
     __device__ __forceinline__ void unpack(float (&w)[8]) const {
@@ -507,18 +513,28 @@ struct WPiece<KM, true> {
     }
 };
 
+// Stored row j of a slot holding ns rows: weights, and (int8) scales.
+template <int KM, bool I8>
+__device__ __forceinline__ const uint8_t *slot_row(const uint8_t *sp, int j) {
+    return sp + (size_t)j * (I8 ? 1024 * KM : 2048 * KM);
+}
+template <int KM, bool I8>
+__device__ __forceinline__ const uint8_t *slot_scales(const uint8_t *sp, int ns, int j) {
+    return I8 ? sp + (size_t)ns * (1024 * KM) + (size_t)j * (64 * KM) : nullptr;
+}
+
 // Dot products of NR stored rows with the activation held in registers
 // (act[8 m + e] = activation column 8*(lane + 32 m) + e).  All weight loads of the
 // row group are issued before any arithmetic, and the accumulation chains of the
-// rows are interleaved; rows must be valid slot rows (callers clamp unused ones).
+// rows are interleaved; rows must be valid (callers repeat a valid row for unused ones).
 template <int KM, bool I8, int NR>
-__device__ __forceinline__ void dot_rows(const uint8_t *sp, int ns, const int (&rows)[NR], int lane,
+__device__ __forceinline__ void dot_rows(const uint8_t *const (&rp)[NR], const uint8_t *const (&sc)[NR], int lane,
                                          const float *act, float (&out)[NR]) {
     WPiece<KM, I8> wp[NR][4 * KM];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int m = 0; m < 4 * KM; ++m) wp[r][m].load(sp, ns, rows[r], lane, m);
+        for (int m = 0; m < 4 * KM; ++m) wp[r][m].load(rp[r], sc[r], lane, m);
     float acc[NR][2];
 #pragma unroll
     for (int r = 0; r < NR; ++r) acc[r][0] = acc[r][1] = 0.f;
@@ -635,61 +651,118 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     }
     unsigned long long best = 0;
     bool bad = false, dead = false;
-    for (int ch = 0; ch < p.nchunks; ++ch) {
-        const unsigned slot = it % kSlots, par = (it / kSlots) & 1u;
-        ++it;
-        if (!take_slot(slot, par)) {
-            dead = true;
-            break;
-        }
-        const uint8_t *sp = sm.slot[slot];
-        const int a0 = p.r0 + ch * p.rpc;
-        const int n = min(p.rpc, p.r1 - a0);
-        const int ns = pair ? 2 * n : n;
-        for (int j = warp; j < n; j += 2 * kConsumerWarps) {
-            const int j2 = j + kConsumerWarps;
-            const int cnt = j2 < n ? 2 : 1;
-            const int j2c = cnt == 2 ? j2 : j;  // an unused second row repeats the first
-            if constexpr (pair) {
-                // gate row j, up row j (stored at n + j), and the same for j2
-                const int rows[4] = {j, n + j, j2c, n + j2c};
-                float o[4];
-                dot_rows<KM, I8, 4>(sp, ns, rows, lane, areg, o);
-                if (lane == 0) {
-                    st_tag(a.actt + a0 + j, (o[0] / (1.0f + __expf(-o[0]))) * o[1], out_tag);
-                    if (cnt == 2) st_tag(a.actt + a0 + j2, (o[2] / (1.0f + __expf(-o[2]))) * o[3], out_tag);
-                }
+    // the value of output row (CTA-local index g) -> its destination (lane 0 only)
+    auto emit = [&](int g, float v, float up) {
+        const int row = p.r0 + g;
+        if constexpr (PT == T_GATEUP) {
+            st_tag(a.actt + row, (v / (1.0f + __expf(-v))) * up, out_tag);
+        } else if constexpr (PT == T_QKV) {
+            st_tag(a.qkvt + row, v, out_tag);
+        } else if constexpr (PT == T_OPROJ || PT == T_DOWN) {
+            // the residual rows of this CTA live in shared memory for the whole step
+            const float nx = sm.xown[row - own0] + v;
+            sm.xown[row - own0] = nx;
+            st_tag((PT == T_OPROJ ? a.xb : a.xa) + row, nx, out_tag);
+            if (PT == T_DOWN && (a.debug & 1)) a.hidden[(size_t)(p.l + 1) * a.H + row] = nx;
+        } else {
+            a.logits[row] = v;
+            if (isfinite(v)) {
+                const unsigned long long k = argmax_key(v, row);
+                best = k > best ? k : best;
             } else {
-                const int rows[2] = {j, j2c};
-                float o[2];
-                dot_rows<KM, I8, 2>(sp, ns, rows, lane, areg, o);
+                bad = true;
+            }
+        }
+    };
+    if (PT != T_LMHEAD && p.nchunks <= kFusedChunks) {
+        // Every chunk of the phase fits in the ring at once: take them all, then each warp
+        // computes its rows g = warp, warp + 7, ... in as few passes as possible (the rows
+        // of one pass may sit in different slots), then release every chunk.
+        const unsigned it0 = it;
+        for (int ch = 0; ch < p.nchunks && !dead; ++ch)
+            dead = !take_slot((it0 + ch) % kSlots, ((it0 + ch) / kSlots) & 1u);
+        it += p.nchunks;
+        if (!dead) {
+            constexpr int NRW = pair ? 3 : (KM == 1 ? 4 : 1);  // rows (gate/up pairs) per pass
+            constexpr int NR = pair ? 2 * NRW : NRW;
+            const int R = p.r1 - p.r0;
+            for (int g0 = warp; g0 < R; g0 += NRW * kConsumerWarps) {
+                const uint8_t *rp[NR], *sc[NR];
+                int cnt = 0;
+#pragma unroll
+                for (int i = 0; i < NRW; ++i) {
+                    int g = g0 + i * kConsumerWarps;
+                    if (g < R) cnt = i + 1;
+                    else g = g0;  // an unused row repeats a valid one
+                    const int c = g / p.rpc, j = g - c * p.rpc;
+                    const int n = min(p.rpc, R - c * p.rpc), ns = pair ? 2 * n : n;
+                    const uint8_t *sp = sm.slot[(it0 + c) % kSlots];
+                    if constexpr (pair) {
+                        rp[2 * i] = slot_row<KM, I8>(sp, j);
+                        sc[2 * i] = slot_scales<KM, I8>(sp, ns, j);
+                        rp[2 * i + 1] = slot_row<KM, I8>(sp, n + j);
+                        sc[2 * i + 1] = slot_scales<KM, I8>(sp, ns, n + j);
+                    } else {
+                        rp[i] = slot_row<KM, I8>(sp, j);
+                        sc[i] = slot_scales<KM, I8>(sp, ns, j);
+                    }
+                }
+                float o[NR];
+                dot_rows<KM, I8, NR>(rp, sc, lane, areg, o);
                 if (lane == 0) {
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if (r >= cnt) break;
-                        const int row = a0 + (r ? j2 : j);
-                        if constexpr (PT == T_QKV) {
-                            st_tag(a.qkvt + row, o[r], out_tag);
-                        } else if constexpr (PT == T_OPROJ || PT == T_DOWN) {
-                            // the residual rows of this CTA live in shared memory for the whole step
-                            const float nx = sm.xown[row - own0] + o[r];
-                            sm.xown[row - own0] = nx;
-                            st_tag((PT == T_OPROJ ? a.xb : a.xa) + row, nx, out_tag);
-                            if (PT == T_DOWN && (a.debug & 1)) a.hidden[(size_t)(p.l + 1) * a.H + row] = nx;
-                        } else {
-                            a.logits[row] = o[r];
-                            if (isfinite(o[r])) {
-                                const unsigned long long k = argmax_key(o[r], row);
-                                best = k > best ? k : best;
-                            } else {
-                                bad = true;
-                            }
+                    for (int i = 0; i < NRW; ++i)
+                        if (i < cnt) {
+                            if constexpr (pair)
+                                emit(g0 + i * kConsumerWarps, o[2 * i], o[2 * i + 1]);
+                            else
+                                emit(g0 + i * kConsumerWarps, o[i], 0.f);
                         }
+                }
+            }
+            for (int ch = 0; ch < p.nchunks; ++ch) release_slot((it0 + ch) % kSlots);
+        }
+    } else {
+        for (int ch = 0; ch < p.nchunks; ++ch) {
+            const unsigned slot = it % kSlots, par = (it / kSlots) & 1u;
+            ++it;
+            if (!take_slot(slot, par)) {
+                dead = true;
+                break;
+            }
+            const uint8_t *sp = sm.slot[slot];
+            const int c0 = ch * p.rpc;
+            const int n = min(p.rpc, p.r1 - p.r0 - c0);
+            const int ns = pair ? 2 * n : n;
+            for (int j = warp; j < n; j += 2 * kConsumerWarps) {
+                const int j2 = j + kConsumerWarps;
+                const int cnt = j2 < n ? 2 : 1;
+                const int j2c = cnt == 2 ? j2 : j;  // an unused second row repeats the first
+                if constexpr (pair) {
+                    // gate row j, up row j (stored at n + j), and the same for j2
+                    const uint8_t *rp[4] = {slot_row<KM, I8>(sp, j), slot_row<KM, I8>(sp, n + j),
+                                            slot_row<KM, I8>(sp, j2c), slot_row<KM, I8>(sp, n + j2c)};
+                    const uint8_t *sc[4] = {slot_scales<KM, I8>(sp, ns, j), slot_scales<KM, I8>(sp, ns, n + j),
+                                            slot_scales<KM, I8>(sp, ns, j2c), slot_scales<KM, I8>(sp, ns, n + j2c)};
+                    float o[4];
+                    dot_rows<KM, I8, 4>(rp, sc, lane, areg, o);
+                    if (lane == 0) {
+                        emit(c0 + j, o[0], o[1]);
+                        if (cnt == 2) emit(c0 + j2, o[2], o[3]);
+                    }
+                } else {
+                    const uint8_t *rp[2] = {slot_row<KM, I8>(sp, j), slot_row<KM, I8>(sp, j2c)};
+                    const uint8_t *sc[2] = {slot_scales<KM, I8>(sp, ns, j), slot_scales<KM, I8>(sp, ns, j2c)};
+                    float o[2];
+                    dot_rows<KM, I8, 2>(rp, sc, lane, areg, o);
+                    if (lane == 0) {
+                        emit(c0 + j, o[0], 0.f);
+                        if (cnt == 2) emit(c0 + j2, o[1], 0.f);
                     }
                 }
             }
+            release_slot(slot);
         }
-        release_slot(slot);
     }
     if constexpr (PT == T_LMHEAD) {
         if (lane == 0) {
@@ -907,7 +980,7 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
                 acc[h][r][e] = 0.f;
             }
     }
-    bool dead = false;
+    bool dead = false, folded = false;
     for (int ch = 0; ch < p.nchunks; ++ch) {
         const unsigned slot = it % kSlots, par = (it / kSlots) & 1u;
         ++it;
@@ -915,12 +988,27 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
             dead = true;
             break;
         }
-        const uint8_t *sp = sm.slot[slot];
-        const int n = min(CH, p.p1 - (p.p0 + ch * CH));
+        uint8_t *sp = sm.slot[slot];
+        int n = min(CH, p.p1 - (p.p0 + ch * CH));
+        if (owner && ch == p.nchunks - 1 && n < CH) {
+            // the owner appends this position's K and V rows to its last chunk (a slot half
+            // holds more rows than a chunk), so the new position costs no separate pass
+            constexpr int W16 = kHeadDim * (int)sizeof(KT) / 16;
+            if (tid < 2 * W16) {
+                const bool isv = tid >= W16;
+                const uint4 *src = reinterpret_cast<const uint4 *>(isv ? (const void *)snew_v : (const void *)snew_k);
+                reinterpret_cast<uint4 *>(sp + (isv ? kSlotBytes / 2 : 0) + (size_t)n * (W16 * 16))[tid % W16] =
+                    src[tid % W16];
+                fence_async_smem();  // ordered before the producer's next bulk copy into this slot
+            }
+            bar_consumers();
+            ++n;
+            folded = true;
+        }
         attn_block<G, KT>(sp, sp + kSlotBytes / 2, n, warp, lane, qr, acc, M, Ls);
         release_slot(slot);
     }
-    if (owner && !dead)
+    if (owner && !dead && !folded)
         attn_block<G, KT>(reinterpret_cast<const uint8_t *>(snew_k), reinterpret_cast<const uint8_t *>(snew_v), 1,
                           warp, lane, qr, acc, M, Ls);
     // combine the four positions of each warp (lanes with equal o8 share a dim order)
@@ -979,55 +1067,94 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
     // The CTA that finishes the last split of this KV head merges all S partials into the
     // group's attention output (once, instead of in every o_proj CTA):
     // o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s.
+    // The count needs no fence: the merging CTA checks every word's tag and re-polls any
+    // partial that is not visible yet.
     bar_consumers();
     if (tid == 0) {
-        __threadfence();  // this CTA's partial before its count
         unsigned *ctr = a.merge + (size_t)l * kMaxKvHeads + kvh;
         sm.flag = atomicAdd(ctr, 1u) + 1u == (unsigned)S;
         if (sm.flag) *ctr = 0u;  // every split has counted; the next use is the next step
     }
     bar_consumers();
     if (sm.flag) {
-        __threadfence();  // the other splits' partials, published before their counts
+        // warp w folds splits w, w + 7, w + 14 (one polling round), lane holds dims lane + 32 k
+        constexpr int KS = kMaxSplits / kConsumerWarps;  // splits per warp
+        static_assert(KS * kConsumerWarps >= kMaxSplits, "every split has a merging warp");
+        float mw[G], lw[G], aw[G][4];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mw[h] = -INFINITY;
+            lw[h] = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) aw[h][k] = 0.f;
+        }
+        unsigned long long w[KS][G][6];
+        unsigned long long t0 = 0;
         bool ok = true;
-        for (int t = tid; t < G * kHeadDim && ok; t += kConsumerThreads) {
-            const int h = t / kHeadDim, dim = t % kHeadDim;
-            const unsigned long long *p0 = a.partt + ((size_t)kvh * S * G + h) * kPartStride;
-            float mx = -INFINITY, ls = 0.f, av = 0.f;
-            for (int s0 = 0; s0 < S && ok; s0 += 4) {
-                unsigned long long w[4][3];
-                unsigned long long t0 = 0;
-                for (unsigned i = 0;; ++i) {
-                    bool got = true;
+        for (unsigned i = 0;; ++i) {
+            bool got = true;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (s0 + k >= S) break;
-                        const unsigned long long *pp = p0 + (size_t)(s0 + k) * G * kPartStride;
-                        ld_tag2(pp + kHeadDim, w[k][0], w[k][1]);
-                        w[k][2] = ld_tag(pp + dim);
-                        got &= tag_is(w[k][0], out_tag) && tag_is(w[k][1], out_tag) && tag_is(w[k][2], out_tag);
-                    }
-                    if (got) break;
-                    if (!poll_more(i, t0, a.flags)) {
-                        ok = false;
-                        break;
-                    }
-                }
+            for (int q = 0; q < KS; ++q) {
+                const int sidx = warp + kConsumerWarps * q;
+                if (sidx >= S) break;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (!ok || s0 + k >= S) break;
-                    const float ms = tag_val(w[k][0]);
-                    if (ms == -INFINITY) continue;
-                    const float mn = fmaxf(mx, ms);
-                    const float sa = (mx == -INFINITY) ? 0.f : exp2f(mx - mn), sb = exp2f(ms - mn);
-                    ls = ls * sa + tag_val(w[k][1]) * sb;
-                    av = av * sa + tag_val(w[k][2]) * sb;
-                    mx = mn;
+                for (int h = 0; h < G; ++h) {
+                    const unsigned long long *pp = a.partt + ((size_t)(kvh * S + sidx) * G + h) * kPartStride;
+                    ld_tag2(pp + kHeadDim, w[q][h][0], w[q][h][1]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w[q][h][2 + k] = ld_tag(pp + lane + 32 * k);
+#pragma unroll
+                    for (int e = 0; e < 6; ++e) got &= tag_is(w[q][h][e], out_tag);
                 }
             }
-            if (ok) st_tag(a.ot + (size_t)(kvh * G + h) * kHeadDim + dim, av / ls, out_tag);
+            if (__all_sync(0xffffffffu, got)) break;
+            if (!poll_more(i, t0, a.flags)) {
+                ok = false;
+                break;
+            }
         }
-        if (!all_ok(ok)) return kFailed;
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < KS; ++q) {
+                if (warp + kConsumerWarps * q >= S) break;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float ms = tag_val(w[q][h][0]);
+                    if (ms == -INFINITY) continue;
+                    const float mn = fmaxf(mw[h], ms);
+                    const float sa = (mw[h] == -INFINITY) ? 0.f : exp2f(mw[h] - mn), sb = exp2f(ms - mn);
+                    lw[h] = lw[h] * sa + tag_val(w[q][h][1]) * sb;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) aw[h][k] = aw[h][k] * sa + tag_val(w[q][h][2 + k]) * sb;
+                    mw[h] = mn;
+                }
+            }
+        }
+        if (!all_ok(ok)) return kFailed;  // its barrier also ends every read of wacc / wml
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sm.wacc[warp][h][lane + 32 * k] = aw[h][k];
+            if (lane == 0) {
+                sm.wml[warp][h][0] = mw[h];
+                sm.wml[warp][h][1] = lw[h];
+            }
+        }
+        bar_consumers();
+        for (int t = tid; t < G * kHeadDim; t += kConsumerThreads) {
+            const int h = t / kHeadDim, dim = t % kHeadDim;
+            float mx = -INFINITY;
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) mx = fmaxf(mx, sm.wml[w2][h][0]);
+            float av = 0.f, ls = 0.f;
+            for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+                const float m2 = sm.wml[w2][h][0];
+                if (m2 == -INFINITY) continue;
+                const float sc = exp2f(m2 - mx);
+                av = fmaf(sm.wacc[w2][h][dim], sc, av);
+                ls = fmaf(sm.wml[w2][h][1], sc, ls);
+            }
+            st_tag(a.ot + (size_t)(kvh * G + h) * kHeadDim + dim, av / ls, out_tag);
+        }
     }
     return (int)(it | (dead ? kDeadBit : 0u));
 }
@@ -1052,7 +1179,9 @@ __device__ __forceinline__ int gemv_dispatch(const DecodeArgs &a, int type, int 
     }
 }
 
-template <int G>
+// One kernel per (group size, weight format, cache element type), so each carries only
+// the phase code it runs.
+template <int G, bool I8, typename KT>
 __device__ void consumer() {
     Smem &sm = smem();
     const DecodeArgs &a = sm.args;
@@ -1079,11 +1208,9 @@ __device__ void consumer() {
         const int type = phase_type(a, ph);
         int r;
         if (type == T_ATTN)
-            r = a.kv_f32 ? attn_phase<G, float>(ph, it) : attn_phase<G, __nv_bfloat16>(ph, it);
-        else if (a.fmt == 1)
-            r = gemv_dispatch<true, G>(a, type, ph, it);
+            r = attn_phase<G, KT>(ph, it);
         else
-            r = gemv_dispatch<false, G>(a, type, ph, it);
+            r = gemv_dispatch<I8, G>(a, type, ph, it);
         unsigned long long *tr = trace_of(a, ph);
         if (tr && tid == 0) tr[2] = gtime();
         if (r == kFailed) return;  // uniform: decided at a barrier
@@ -1116,7 +1243,7 @@ __device__ void consumer() {
     }
 }
 
-template <int G>
+template <int G, bool I8, typename KT>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
     Smem &sm = smem();
     if (threadIdx.x == 0) {
@@ -1132,7 +1259,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         if (threadIdx.x == kConsumerThreads) producer();
         return;
     }
-    consumer<G>();
+    consumer<G, I8, KT>();
+}
+
+// The kernel instantiation for (group, weight format, cache element type).
+const void *decode_fn(int group, int fmt, int kv_f32) {
+    if (group == 1) {
+        if (fmt == 1) return kv_f32 ? (const void *)decode_kernel<1, true, float> : (const void *)decode_kernel<1, true, __nv_bfloat16>;
+        return kv_f32 ? (const void *)decode_kernel<1, false, float> : (const void *)decode_kernel<1, false, __nv_bfloat16>;
+    }
+    if (fmt == 1) return kv_f32 ? (const void *)decode_kernel<2, true, float> : (const void *)decode_kernel<2, true, __nv_bfloat16>;
+    return kv_f32 ? (const void *)decode_kernel<2, false, float> : (const void *)decode_kernel<2, false, __nv_bfloat16>;
 }
 
 __global__ void kv_widen_kernel(const __nv_bfloat16 *__restrict__ src, float *__restrict__ dst, long long heads,
@@ -1166,10 +1303,18 @@ size_t decode_smem_bytes() { return sizeof(Smem); }
 
 cudaError_t decode_prepare(int group, int *blocks_per_sm) {
     const int bytes = (int)decode_smem_bytes();
-    const void *fn = group == 1 ? (const void *)decode_kernel<1> : (const void *)decode_kernel<2>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kDecodeThreads, bytes);
+    *blocks_per_sm = 1 << 30;
+    for (int fmt = 0; fmt < 2; ++fmt)
+        for (int kv = 0; kv < 2; ++kv) {
+            const void *fn = decode_fn(group, fmt, kv);
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e != cudaSuccess) return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kDecodeThreads, bytes);
+            if (e != cudaSuccess) return e;
+            if (n < *blocks_per_sm) *blocks_per_sm = n;
+        }
+    return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, int group, int ncta, cudaStream_t stream) {
@@ -1183,10 +1328,8 @@ cudaError_t launch_decode(const DecodeArgs &a, int group, int ncta, cudaStream_t
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    switch (group) {
-        case 1: return cudaLaunchKernelEx(&cfg, decode_kernel<1>, a);
-        default: return cudaLaunchKernelEx(&cfg, decode_kernel<2>, a);
-    }
+    void *args[] = {const_cast<DecodeArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, decode_fn(group, a.fmt, a.kv_f32), args);
 }
 
 }  // namespace qw

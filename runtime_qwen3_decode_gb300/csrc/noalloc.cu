@@ -236,11 +236,7 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     a.trace = nullptr;
     a.pos = pos;
     a.token = token;
-    int s = (pos + 95) / 96;
-    if (s > ncta / cfg->n_kv_heads) s = ncta / cfg->n_kv_heads;
-    if (s > pos) s = pos;
-    if (s < 1) s = 1;
-    a.n_split = s;
+    a.n_split = qw::attn_splits(pos, cfg->kv_format == QW_KV_F32 ? 4 : 2, ncta, cfg->n_kv_heads);
     a.debug = 0;
     a.step = 1;          // counters and keys were zeroed for this call
     a.target = (unsigned)ncta;

@@ -136,14 +136,8 @@ int cuda_status(cudaError_t e) {
 
 bool aligned(const void *p, size_t a) { return p && ((uintptr_t)p % a) == 0; }
 
-// Attention splits per KV head: about 96 cached positions each, at most the CTAs per head.
 int split_for(const qw_model *m, int pos) {
-    int s = (pos + 95) / 96;
-    const int cap = m->ncta / m->cfg.n_kv_heads;
-    if (s > cap) s = cap;
-    if (s > pos) s = pos;
-    if (s < 1) s = 1;
-    return s;
+    return qw::attn_splits(pos, m->cfg.kv_format == QW_KV_F32 ? 4 : 2, m->ncta, m->cfg.n_kv_heads);
 }
 
 // One decode step at position len; token >= 0 or -1 (device-resident previous pick).

@@ -28,6 +28,18 @@ __host__ __device__ constexpr int kv_chunk_rows(int elem_bytes) { return 4 * kCo
 constexpr int kPartStride = kHeadDim + 4;    // split-attention partial: acc[128], max, sum, 2 pad (16-B rows)
 constexpr int kMaxOwnRows = 64;             // residual rows per CTA kept in shared memory
 constexpr int kMaxKvHeads = 32;             // split-merge counters per layer
+constexpr int kMaxSplits = 21;              // attention splits per KV head (3 per consumer warp in the merge)
+// Attention splits for a step at position pos: one chunk of cached rows per split, at
+// most one split per CTA and KV head, at most kMaxSplits.
+inline int attn_splits(int pos, int kv_elem_bytes, int ncta, int n_kv_heads) {
+    const int ch = kv_chunk_rows(kv_elem_bytes);
+    int s = (pos + ch - 1) / ch;
+    const int cap = ncta / n_kv_heads < kMaxSplits ? ncta / n_kv_heads : kMaxSplits;
+    if (s > cap) s = cap;
+    if (s > pos) s = pos;
+    if (s < 1) s = 1;
+    return s;
+}
 
 // Debug timeline stamps per (phase, CTA): consumer before wait, after wait, after
 // compute, after arrive; producer first issue, last issue of the phase.
