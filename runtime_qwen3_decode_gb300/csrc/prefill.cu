@@ -82,7 +82,8 @@ struct GemmCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
     static constexpr int kBarBytes = 256;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+    static constexpr int kStgBytes = 4 * 32 * 36 * 4;  // epilogue staging, 4 warps x 32 rows x 36 floats
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStgBytes + kBarBytes;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -111,13 +112,60 @@ __device__ __forceinline__ uint4 pack_half8(const float *v) {
 }
 
 // ------------------------------------------------------------------ GEMM epilogues
+//
+// An epilogue warp holds 32 output rows, one per lane (TMEM lane = tile row).  Stores
+// straight from that layout would make every instruction touch 32 cache lines, so each
+// 32-column block goes through a per-warp shared-memory staging area (32 rows x 36
+// floats: 16-byte accesses of a quarter warp fall in distinct banks both ways) and
+// leaves transposed: one store instruction covers 4 rows x 32 columns.
 
-// One 128-wide head of the q|k|v tile for prompt row t: QK-Norm and RoPE of q and k
-// heads (the decode kernel's arithmetic: r = rsqrt(mean(v^2) + eps), v = w * (v * r),
-// then dims (i, i + 64) rotated by the position's angle), then q -> q16, k and v -> the
-// cache plus their fp16 shadows.
+constexpr int kStgStride = 36;                       // floats per staged row
+constexpr int kStgWarpFloats = 32 * kStgStride;     // per epilogue warp
+
+// Lane l's 32 values -> staging row l.
+__device__ __forceinline__ void stage_rows(float *stg, const float *v) {
+    const int lane = threadIdx.x & 31;
+    float4 *d = reinterpret_cast<float4 *>(stg + lane * kStgStride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    __syncwarp();
+}
+
+// Visit the staged block transposed: f(r, c4, x) for row r (0..31) and columns 4 c4..4 c4+3,
+// 8 passes of 4 rows per warp.  Ends with a __syncwarp so the area can be restaged.
+template <typename F>
+__device__ __forceinline__ void unstage(const float *stg, F &&f) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = 4 * it + (lane >> 3), c4 = lane & 7;
+        f(r, c4, *reinterpret_cast<const float4 *>(stg + r * kStgStride + 4 * c4));
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ uint2 pack_half4(float4 x) {
+    __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+    return make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+}
+
+__device__ __forceinline__ uint2 pack_bf164(float4 x) {
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y), h1 = __floats2bfloat162_rn(x.z, x.w);
+    return make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+}
+
+__device__ __forceinline__ float4 round_bf16(float4 x) {
+    return make_float4(__bfloat162float(__float2bfloat16_rn(x.x)), __bfloat162float(__float2bfloat16_rn(x.y)),
+                       __bfloat162float(__float2bfloat16_rn(x.z)), __bfloat162float(__float2bfloat16_rn(x.w)));
+}
+
+// One 128-wide head of the q|k|v tile for the warp's 32 prompt rows (lane = row, t = the
+// lane's row): QK-Norm and RoPE of q and k heads (the decode kernel's arithmetic:
+// r = rsqrt(mean(v^2) + eps), v = w * (v * r), then dims (i, i + 64) rotated by the
+// position's angle), then q -> q16, k and v -> the cache plus their fp16 shadows.
 template <typename KT>
-__device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32], int slot, int t) {
+__device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32], int slot, int t, int r0, int M,
+                                             float *stg) {
     const int P = o.pos0 + t;
     if (slot < o.Hq + o.Hkv) {
         const __nv_bfloat16 *w = slot < o.Hq ? o.q_norm : o.k_norm;
@@ -127,7 +175,7 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32],
         const float r = rsqrtf(ss * (1.0f / kHeadDim) + o.eps);
 #pragma unroll
         for (int i = 0; i < kHeadDim; ++i) v[i >> 5][i & 31] = __bfloat162float(w[i]) * (v[i >> 5][i & 31] * r);
-        const float2 *cs = o.rope + (size_t)P * (kHeadDim / 2);
+        const float2 *cs = o.rope + (size_t)min(P, o.max_ctx - 1) * (kHeadDim / 2);
 #pragma unroll
         for (int i = 0; i < kHeadDim / 2; ++i) {
             const float2 c = cs[i];
@@ -136,67 +184,59 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32],
             v[(i + 64) >> 5][i & 31] = b * c.x + a * c.y;
         }
     }
-    if (slot < o.Hq) {
-        uint4 *dst = reinterpret_cast<uint4 *>(o.q16 + ((size_t)slot * o.q_rows + t) * kHeadDim);
+    const bool is_q = slot < o.Hq, is_k = !is_q && slot < o.Hq + o.Hkv;
+    const int kvh = is_q ? 0 : is_k ? slot - o.Hq : slot - o.Hq - o.Hkv;
+    KT *cache = reinterpret_cast<KT *>(is_k ? o.kc : o.vc) + (size_t)kvh * o.max_ctx * kHeadDim;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = pack_half8(&v[c >> 2][8 * (c & 3)]);
-        return;
+    for (int k = 0; k < 4; ++k) {
+        stage_rows(stg, v[k]);
+        unstage(stg, [&](int r, int c4, float4 x) {
+            const int tr = r0 + r;  // prompt row
+            if (tr >= M) return;
+            const int d = 32 * k + 4 * c4;
+            if (is_q) {
+                *reinterpret_cast<uint2 *>(o.q16 + ((size_t)slot * o.q_rows + tr) * kHeadDim + d) = pack_half4(x);
+                return;
+            }
+            const size_t prow = (size_t)(o.pos0 + tr) * kHeadDim + d;
+            if constexpr (sizeof(KT) == 4) {
+                *reinterpret_cast<float4 *>(cache + prow) = x;
+            } else {
+                *reinterpret_cast<uint2 *>(cache + prow) = pack_bf164(x);
+                x = round_bf16(x);  // the shadows hold the cached value
+            }
+            if (is_k)
+                *reinterpret_cast<uint2 *>(o.k16 + ((size_t)kvh * o.kv_rows + o.pos0 + tr) * kHeadDim + d) =
+                    pack_half4(x);
+        });
     }
-    const bool is_k = slot < o.Hq + o.Hkv;
-    const int kvh = is_k ? slot - o.Hq : slot - o.Hq - o.Hkv;
-    KT *row = reinterpret_cast<KT *>(is_k ? o.kc : o.vc) + ((size_t)kvh * o.max_ctx + P) * kHeadDim;
-    if constexpr (sizeof(KT) == 4) {
-        float4 *d4 = reinterpret_cast<float4 *>(row);
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            d4[c] = make_float4(v[c >> 3][4 * (c & 7)], v[c >> 3][4 * (c & 7) + 1], v[c >> 3][4 * (c & 7) + 2],
-                                v[c >> 3][4 * (c & 7) + 3]);
-    } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            uint4 u;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3)], v[c >> 2][8 * (c & 3) + 1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 2], v[c >> 2][8 * (c & 3) + 3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 4], v[c >> 2][8 * (c & 3) + 5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(v[c >> 2][8 * (c & 3) + 6], v[c >> 2][8 * (c & 3) + 7]);
-            u.x = *reinterpret_cast<uint32_t *>(&b0);
-            u.y = *reinterpret_cast<uint32_t *>(&b1);
-            u.z = *reinterpret_cast<uint32_t *>(&b2);
-            u.w = *reinterpret_cast<uint32_t *>(&b3);
-            reinterpret_cast<uint4 *>(row)[c] = u;
-        }
-    }
-    // the attention's fp16 operands hold the cached value (bf16-rounded for a bf16 cache)
-    if constexpr (sizeof(KT) == 2) {
-#pragma unroll
-        for (int i = 0; i < kHeadDim; ++i) v[i >> 5][i & 31] = __bfloat162float(__float2bfloat16_rn(v[i >> 5][i & 31]));
-    }
-    if (is_k) {
-        uint4 *dst = reinterpret_cast<uint4 *>(o.k16 + ((size_t)kvh * o.kv_rows + P) * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = pack_half8(&v[c >> 2][8 * (c & 3)]);
-    } else {
+    // V^T shadow: for each dim the warp's 32 rows are 32 consecutive positions (64 B)
+    if (!is_q && !is_k && t < M) {
         __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P;
 #pragma unroll
-        for (int i = 0; i < kHeadDim; ++i) dst[(size_t)i * o.kv_rows] = __float2half_rn(v[i >> 5][i & 31]);
+        for (int i = 0; i < kHeadDim; ++i) {
+            float x = v[i >> 5][i & 31];
+            if constexpr (sizeof(KT) == 2) x = __bfloat162float(__float2bfloat16_rn(x));
+            dst[(size_t)i * o.kv_rows] = __float2half_rn(x);
+        }
     }
 }
 
+// r0: the warp's first row (tile rows r0 .. r0 + 31); stg: its staging area.
 template <int BN, int EPI>
-__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int row, int nt) {
-    const bool live = row < p.M;
+__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int r0, int nt, float *stg) {
+    const int lane = threadIdx.x & 31;
     if constexpr (EPI == EPI_QKV) {
 #pragma unroll 1
         for (int hl = 0; hl < BN / kHeadDim; ++hl) {
             float v[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tacc + hl * kHeadDim + 32 * c, v[c]);
-            if (!live) continue;
             const int slot = nt * (BN / kHeadDim) + hl;
             if (p.qkv.kv_f32)
-                qkv_head_out<float>(p.qkv, v, slot, row);
+                qkv_head_out<float>(p.qkv, v, slot, r0 + lane, r0, p.M, stg);
             else
-                qkv_head_out<__nv_bfloat16>(p.qkv, v, slot, row);
+                qkv_head_out<__nv_bfloat16>(p.qkv, v, slot, r0 + lane, r0, p.M, stg);
         }
     } else if constexpr (EPI == EPI_SWIGLU) {
         constexpr int HB = BN / 2;  // gate columns [0, HB), matching up columns [HB, BN)
@@ -205,35 +245,46 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
             float g[32], u[32];
             tmem_ld32(tacc + c, g);
             tmem_ld32(tacc + HB + c, u);
-            if (live) {
-                float a[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = (g[i] * (1.0f / (1.0f + expf(-g[i])))) * u[i];
-                uint4 *dst = reinterpret_cast<uint4 *>(p.act + (size_t)row * p.ldh + (size_t)nt * HB + c);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = pack_half8(a + 8 * i);
-            }
+            for (int i = 0; i < 32; ++i) g[i] = (g[i] * (1.0f / (1.0f + expf(-g[i])))) * u[i];
+            stage_rows(stg, g);
+            unstage(stg, [&](int r, int c4, float4 x) {
+                if (r0 + r < p.M)
+                    *reinterpret_cast<uint2 *>(p.act + (size_t)(r0 + r) * p.ldh + (size_t)nt * HB + c + 4 * c4) =
+                        pack_half4(x);
+            });
         }
     } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
             float v[32];
-            tmem_ld32(tacc + c, v);
-            if (live) {
-                float4 *dst = reinterpret_cast<float4 *>(p.out + (size_t)row * p.ldo + (size_t)nt * BN + c);
+            float4 y[8];
+            if constexpr (EPI == EPI_ADD) {
+                // the residual block this lane updates, loaded before the accumulator is read
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    if constexpr (EPI == EPI_ADD) {
-                        const float4 x = dst[i];
-                        o.x += x.x;
-                        o.y += x.y;
-                        o.z += x.z;
-                        o.w += x.w;
-                    }
-                    dst[i] = o;
+                for (int it = 0; it < 8; ++it) {
+                    const int r = 4 * it + (lane >> 3);
+                    y[it] = r0 + r < p.M ? reinterpret_cast<const float4 *>(p.out + (size_t)(r0 + r) * p.ldo +
+                                                                             (size_t)nt * BN + c)[lane & 7]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            tmem_ld32(tacc + c, v);
+            stage_rows(stg, v);
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = 4 * it + (lane >> 3), c4 = lane & 7;
+                float4 x = *reinterpret_cast<const float4 *>(stg + r * kStgStride + 4 * c4);
+                if (r0 + r >= p.M) continue;
+                if constexpr (EPI == EPI_ADD) {
+                    x.x += y[it].x;
+                    x.y += y[it].y;
+                    x.z += y[it].z;
+                    x.w += y[it].w;
+                }
+                reinterpret_cast<float4 *>(p.out + (size_t)(r0 + r) * p.ldo + (size_t)nt * BN + c)[c4] = x;
+            }
+            __syncwarp();
         }
     }
 }
@@ -251,7 +302,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t *base = smem_base1024();
     uint8_t *sa = base;
     uint8_t *sb = base + C::kStages * C::kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sb + C::kStages * C::kBBytes);
+    float *stg_all = reinterpret_cast<float *>(sb + C::kStages * C::kBBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sb + C::kStages * C::kBBytes + C::kStgBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
@@ -381,7 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             const int mt = tile % tiles_m, nt = tile / tiles_m;
             const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32 + lane, nt);
+            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32, nt, stg_all + (warp - 2) * kStgWarpFloats);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
