@@ -86,6 +86,12 @@ def lib():
             L.ora_rope_apply.argtypes = [f32p, ctypes.c_int, f32p, f32p]
             L.ora_attention_head.argtypes = [f32p, f32p, f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, f32p, f32p]
             L.ora_argmax.argtypes = [f32p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32)]
+            u64p = ctypes.POINTER(ctypes.c_uint64)
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            L.ora_pcg32_seed.argtypes = [ctypes.c_uint64, ctypes.c_uint64, u64p]
+            L.ora_pcg32_seed.restype = None
+            L.ora_sample.argtypes = [f32p, ctypes.c_int32, i32p, ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                     ctypes.c_float, ctypes.c_float, u64p, i32p, i32p, f32p, i32p, f32p]
             L.ora_create.argtypes = [ctypes.POINTER(_Config), vp, vp, ctypes.POINTER(_Layer), ctypes.POINTER(vp)]
             L.ora_destroy.argtypes = [vp]
             L.ora_destroy.restype = None
@@ -185,6 +191,35 @@ def argmax(logits) -> int:
 
 
 # -------------------------------------------------------------------- model
+
+def pcg32_seed(seed: int, stream: int) -> np.ndarray:
+    """PCG32 state (state, increment) after the pages' seeding procedure."""
+    out = np.zeros(2, np.uint64)
+    lib().ora_pcg32_seed(ctypes.c_uint64(seed), ctypes.c_uint64(stream), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+    return out
+
+
+def sample(logits, rng: np.ndarray, temperature: float, top_k: int = 0, top_p: float = 1.0, penalty: float = 1.0,
+           history=()):
+    """One sampling step over f32 logits; rng ([state, increment], uint64) advances in place.
+
+    Returns (token, retained candidate ids in draw order, their cumulative probabilities, u)."""
+    x = _f32(logits)
+    V = x.size
+    h = np.ascontiguousarray(history, dtype=np.int32)
+    ids = np.empty(V, np.int32)
+    cum = np.empty(V, np.float32)
+    n = ctypes.c_int32(0)
+    tok = ctypes.c_int32(-1)
+    u = ctypes.c_float(0.0)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    rc = lib().ora_sample(_fp(x), V, h.ctypes.data_as(i32p), h.size, float(temperature), int(top_k), float(top_p),
+                          float(penalty), rng.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), ctypes.byref(tok),
+                          ids.ctypes.data_as(i32p), _fp(cum), ctypes.byref(n), ctypes.byref(u))
+    if rc:
+        raise OracleError(rc, "sample")
+    return int(tok.value), ids[:n.value].copy(), cum[:n.value].copy(), float(u.value)
+
 
 class OracleModel:
     """The decoder over borrowed numpy weights (from ``qw_inputs.make_weights``)."""

@@ -46,6 +46,7 @@ enum {
     ORA_UNSUPPORTED_QUANTIZATION = 12,
     ORA_UNSUPPORTED_SHAPE = 13,
     ORA_CONTEXT_EXCEEDED = 14,
+    ORA_OUT_OF_MEMORY = 9,
     ORA_NUMERICAL_FAILURE = 18,
 };
 
@@ -620,5 +621,173 @@ int ora_full(const ora_model *md, const int32_t *tokens, int32_t T, float *logit
     for (int t = 0; t < T && !rc; ++t) rc = head_logits(md, X + (size_t)t * H, logits + (size_t)t * c->vocab, h);
 done:
     free(X); free(h); free(Q); free(K); free(V); free(Kh); free(Vh); free(O); free(G); free(U); free(tmp); free(scr);
+    return rc;
+}
+
+/* ------------------------------------------------------------- sampling
+ *
+ * The sampler of "Portable WebAssembly Runtime Architecture for TinyRustLM",
+ * sections "Deterministic sampling contract" (PCG32: transition, seeding and the
+ * f32 uniform) and "Sampling order", with the repetition penalty of "Scalar-Native
+ * Qwen3 Reference Runtime ...", section 7 (a repeated positive logit is divided by
+ * the penalty, a repeated negative one multiplied).  Readings where the two pages
+ * differ or stay open: the nucleus keeps the minimal prefix whose cumulative
+ * probability is at least top_p (the former page; the latter says "exceeds");
+ * probabilities of the top-k survivors are renormalised before the nucleus and the
+ * nucleus is renormalised before the draw; a draw u picks the first candidate whose
+ * cumulative probability exceeds u (the last one if rounding leaves none); every
+ * sampled (temperature > 0) step consumes exactly one PCG32 word, a greedy step
+ * none; top_k <= 0 keeps every token.  All arithmetic is binary32 in candidate
+ * order. */
+
+typedef struct {
+    uint64_t state, inc;
+} ora_pcg32;
+
+static uint32_t ora_pcg32_next(ora_pcg32 *r) {
+    const uint64_t old = r->state;
+    r->state = old * 6364136223846793005ULL + r->inc;
+    const uint32_t xorshifted = (uint32_t)(((old >> 18) ^ old) >> 27);
+    const uint32_t rot = (uint32_t)(old >> 59);
+    return (xorshifted >> rot) | (xorshifted << ((32u - rot) & 31u));
+}
+
+/* Seeded state: state 0, increment (stream << 1) | 1, advance, add the seed, advance. */
+void ora_pcg32_seed(uint64_t seed, uint64_t stream, uint64_t out[2]) {
+    ora_pcg32 r = {0, (stream << 1) | 1u};
+    (void)ora_pcg32_next(&r);
+    r.state += seed;
+    (void)ora_pcg32_next(&r);
+    out[0] = r.state;
+    out[1] = r.inc;
+}
+
+static int cand_before(float xa, int32_t ia, float xb, int32_t ib) {
+    return xa > xb || (xa == xb && ia < ib);  /* descending value, ascending id */
+}
+
+/*
+ * logits [V] (unchanged), history [n_hist] token ids (each present token penalised
+ * once), rng [2] = (state, increment) updated in place.  Outputs: the token; and,
+ * when the arrays are given, the retained candidates in draw order (ids), their
+ * cumulative probabilities, their count, and the draw u (-1 for a greedy step).
+ * Errors: INVALID_ARGUMENT for V <= 0, a token id out of range, a non-positive or
+ * non-finite penalty or a negative / non-finite temperature, top_p outside (0, 1];
+ * NUMERICAL_FAILURE when every logit is -inf (nothing can be drawn).
+ */
+int ora_sample(const float *logits, int32_t V, const int32_t *history, int32_t n_hist, float temperature,
+               int32_t top_k, float top_p, float penalty, uint64_t rng[2], int32_t *token, int32_t *ids_out,
+               float *cum_out, int32_t *n_out, float *u_out) {
+    if (V <= 0 || n_hist < 0 || !token || !rng) return ORA_INVALID_ARGUMENT;
+    if (!(penalty > 0.0f) || !isfinite(penalty)) return ORA_INVALID_ARGUMENT;
+    if (!(temperature >= 0.0f) || !isfinite(temperature)) return ORA_INVALID_ARGUMENT;
+    if (!(top_p > 0.0f) || top_p > 1.0f) return ORA_INVALID_ARGUMENT;
+    float *x = (float *)malloc(sizeof(float) * (size_t)V);
+    int32_t *ord = (int32_t *)malloc(sizeof(int32_t) * (size_t)V);
+    unsigned char *seen = (unsigned char *)calloc((size_t)V, 1);
+    float *p = (float *)malloc(sizeof(float) * (size_t)V);
+    int rc = ORA_OK;
+    if (!x || !ord || !seen || !p) {
+        rc = ORA_OUT_OF_MEMORY;
+        goto out;
+    }
+    /* 1. logits in token-id order */
+    memcpy(x, logits, sizeof(float) * (size_t)V);
+    /* 3. repetition penalty, once per distinct token of the history */
+    for (int32_t i = 0; i < n_hist; ++i) {
+        const int32_t t = history[i];
+        if (t < 0 || t >= V) {
+            rc = ORA_INVALID_ARGUMENT;
+            goto out;
+        }
+        if (seen[t]) continue;
+        seen[t] = 1;
+        if (x[t] > 0.0f)
+            x[t] = x[t] / penalty;
+        else if (x[t] < 0.0f)
+            x[t] = x[t] * penalty;
+    }
+    /* NaN -> -inf, -0 -> +0 */
+    int any = 0;
+    for (int32_t i = 0; i < V; ++i) {
+        if (isnan(x[i])) x[i] = -INFINITY;
+        if (x[i] == 0.0f) x[i] = 0.0f;
+        if (x[i] != -INFINITY) any = 1;
+    }
+    if (!any) {
+        rc = ORA_NUMERICAL_FAILURE;
+        goto out;
+    }
+    /* temperature 0: the greatest logit, lowest id on ties, no draw */
+    if (temperature == 0.0f) {
+        int32_t best = 0;
+        for (int32_t i = 1; i < V; ++i)
+            if (cand_before(x[i], i, x[best], best)) best = i;
+        *token = best;
+        if (ids_out) ids_out[0] = best;
+        if (cum_out) cum_out[0] = 1.0f;
+        if (n_out) *n_out = 1;
+        if (u_out) *u_out = -1.0f;
+        goto out;
+    }
+    for (int32_t i = 0; i < V; ++i) x[i] = x[i] / temperature;
+    /* top-k: descending logit, ascending id (insertion into a sorted prefix of k) */
+    const int32_t k = (top_k <= 0 || top_k > V) ? V : top_k;
+    int32_t nk = 0;
+    for (int32_t i = 0; i < V; ++i) {
+        if (nk == k && !cand_before(x[i], i, x[ord[k - 1]], ord[k - 1])) continue;
+        int32_t j = nk < k ? nk++ : k - 1;
+        while (j > 0 && cand_before(x[i], i, x[ord[j - 1]], ord[j - 1])) {
+            ord[j] = ord[j - 1];
+            --j;
+        }
+        ord[j] = i;
+    }
+    /* stable probabilities over the survivors (max-shifted exp, sum in order) */
+    const float m = x[ord[0]];
+    float s = 0.0f;
+    for (int32_t j = 0; j < nk; ++j) {
+        p[j] = expf(x[ord[j]] - m);
+        s = s + p[j];
+    }
+    for (int32_t j = 0; j < nk; ++j) p[j] = p[j] / s;
+    /* top-p: the minimal prefix whose cumulative probability is at least top_p */
+    int32_t n = nk;
+    if (top_p < 1.0f) {
+        float c = 0.0f;
+        for (int32_t j = 0; j < nk; ++j) {
+            c = c + p[j];
+            if (c >= top_p) {
+                n = j + 1;
+                break;
+            }
+        }
+    }
+    /* renormalise the nucleus; cumulative scan in the same order */
+    float z = 0.0f;
+    for (int32_t j = 0; j < n; ++j) z = z + p[j];
+    /* one PCG32 word -> u = (w >> 8) * 2^-24 in [0, 1) */
+    ora_pcg32 g = {rng[0], rng[1]};
+    const uint32_t w = ora_pcg32_next(&g);
+    rng[0] = g.state;
+    const float u = (float)(w >> 8) * (1.0f / 16777216.0f);
+    /* the first candidate whose cumulative probability exceeds u */
+    int32_t pick = -1;
+    float c = 0.0f;
+    for (int32_t j = 0; j < n; ++j) {
+        c = c + p[j] / z;
+        if (cum_out) cum_out[j] = c;
+        if (ids_out) ids_out[j] = ord[j];
+        if (pick < 0 && c > u) pick = j;
+    }
+    if (pick < 0) pick = n - 1;
+    *token = ord[pick];
+    if (n_out) *n_out = n;
+    if (u_out) *u_out = u;
+out:
+    free(x);
+    free(ord);
+    free(seen);
+    free(p);
     return rc;
 }
