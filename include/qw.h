@@ -270,6 +270,59 @@ int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *weights, void
                            void *cuda_stream, int32_t wait);
 
 /*
+ * On-device sampling ("Portable WebAssembly Runtime Architecture for TinyRustLM",
+ * sections "Sampling order" and "Deterministic sampling contract"; repetition
+ * penalty of "Scalar-Native Qwen3 Reference Runtime ...", section 7).  Order:
+ * repetition penalty (each distinct history token once: positive logit / penalty,
+ * negative * penalty), NaN -> -inf, -0 -> +0; temperature 0 takes the greatest logit
+ * (lowest id on ties) and draws nothing; otherwise logits / temperature, top-k by
+ * descending value then ascending id, max-shifted probabilities over the survivors,
+ * the minimal prefix whose cumulative probability reaches top_p, renormalised, and
+ * one PCG32 word u = (w >> 8) * 2^-24 picks the first candidate whose cumulative
+ * probability exceeds u.
+ */
+enum { QW_SAMPLE_MAX_TOP_K = 64 };
+typedef struct {
+    float temperature;        /* >= 0, finite; 0 = greedy */
+    int32_t top_k;            /* 1 .. QW_SAMPLE_MAX_TOP_K (and <= vocab) when temperature > 0 */
+    float top_p;              /* (0, 1]; 1 keeps every top-k survivor */
+    float repetition_penalty; /* > 0, finite; 1 = off */
+} qw_sampling;
+
+/* Device scratch bytes qw_sample_logits needs for a vocabulary of this size. */
+size_t qw_sample_scratch_bytes(int32_t vocab);
+
+/*
+ * Sample one token from device f32 logits [vocab] (not modified).  history_dev:
+ * device int32 token ids [n_history] for the repetition penalty (may be NULL when
+ * n_history == 0).  rng_dev: device uint64 [2] = PCG32 (state, increment), advanced
+ * by one word when temperature > 0.  token_dev: device int32 result, -1 when nothing
+ * can be drawn (every logit masked) or a history id is out of range.  scratch_dev:
+ * qw_sample_scratch_bytes(vocab) device bytes, 256-byte aligned.  Stream-ordered on
+ * cuda_stream; returns after enqueueing (QW_INVALID_ARGUMENT for bad parameters).
+ */
+int qw_sample_logits(const float *logits_dev, int32_t vocab, const int32_t *history_dev, int32_t n_history,
+                     const qw_sampling *params, uint64_t *rng_dev, int32_t *token_dev, void *scratch_dev,
+                     size_t scratch_bytes, void *cuda_stream);
+
+/* Seed the model's sampler: PCG32 state 0, increment (stream << 1) | 1, advance, add
+ * seed, advance (the pages' seeding).  Stream-ordered. */
+int qw_sampler_seed(qw_model *m, uint64_t seed, uint64_t stream);
+
+/* The model's PCG32 (state, increment) after every enqueued call (waits for the stream). */
+int qw_sampler_state(qw_model *m, uint64_t *state_host);
+
+/*
+ * Sample the next token from the logits of the last processed position with the
+ * model's sampler.  The pick becomes the device-resident token that
+ * qw_decode_step(-1) consumes; with next_token_host != NULL the call waits and
+ * writes it there.  A device-side failure (nothing drawable, a history id out of
+ * range) is reported by the next call that waits.
+ */
+int qw_sample(qw_model *m, const qw_sampling *params, const int32_t *history_dev, int32_t n_history,
+              int32_t *next_token_host);
+
+/*
  * Test entry of the tensor-core GEMM the prefill uses: C = A B^T with A fp16
  * [M, K], B fp16 [N, K] (row-major, K contiguous) and C f32 [M, N], all device
  * pointers, 16-byte aligned.  K must be a multiple of 64, N of the tile width bn

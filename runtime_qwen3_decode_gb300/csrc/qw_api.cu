@@ -16,6 +16,7 @@
 #include "qw.h"
 #include "qw_internal.h"
 #include "qw_prefill.h"
+#include "qw_sample.h"
 
 namespace {
 
@@ -27,6 +28,7 @@ struct Layout {
     size_t kc, vc, rope, layers, xa, xb, qkvt, actt, partt, ot, logits, hidden, step, merge, flags, trace;
     size_t tagged_begin, tagged_end;
     size_t prefill, prefill_bytes;
+    size_t sampler, sampler_bytes;  // PCG32 state (16 B) + sampling scratch
     size_t total;
 };
 
@@ -91,6 +93,8 @@ int make_layout(const qw_config *c, Layout *L) {
     const int rows = c->max_ctx < kPrefillRowsMax ? c->max_ctx : kPrefillRowsMax;
     L->prefill_bytes = qw::prefill_workspace_bytes(*c, rows);
     L->prefill = take(L->prefill_bytes);
+    L->sampler_bytes = 256 + qw::sample_scratch_bytes(c->vocab);
+    L->sampler = take(L->sampler_bytes);
     L->total = off;
     return QW_OK;
 }
@@ -304,6 +308,7 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
         rc = cuda_status(cudaMemcpyAsync(ws + L.layers, host_layers.data(), host_layers.size() * sizeof(qw::DevLayer),
                                          cudaMemcpyHostToDevice, m->stream));
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.flags, 0, sizeof(qw::StepFlags), m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.sampler, 0, 256, m->stream));
     if (!rc)
         rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, L.merge + qw::merge_block_bytes(cfg->n_layers) - L.step,
                                          m->stream));
@@ -536,6 +541,70 @@ int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n) {
     if (!dst_dev || n != len) return QW_INVALID_ARGUMENT;
     return cuda_status(cudaMemcpyAsync(dst_dev, m->ws + m->lay.trace, (size_t)n * 8, cudaMemcpyDeviceToDevice,
                                        m->stream));
+}
+
+static int check_sampling(const qw_sampling *sp, int32_t vocab, int32_t n_history, const int32_t *history) {
+    if (!sp || n_history < 0 || (n_history > 0 && !history)) return QW_INVALID_ARGUMENT;
+    if (!(sp->temperature >= 0.0f) || !std::isfinite(sp->temperature)) return QW_INVALID_ARGUMENT;
+    if (!(sp->repetition_penalty > 0.0f) || !std::isfinite(sp->repetition_penalty)) return QW_INVALID_ARGUMENT;
+    if (!(sp->top_p > 0.0f) || !(sp->top_p <= 1.0f)) return QW_INVALID_ARGUMENT;
+    if (sp->temperature > 0.0f && (sp->top_k < 1 || sp->top_k > QW_SAMPLE_MAX_TOP_K || sp->top_k > vocab))
+        return QW_INVALID_ARGUMENT;
+    return QW_OK;
+}
+
+size_t qw_sample_scratch_bytes(int32_t vocab) { return vocab > 0 ? qw::sample_scratch_bytes(vocab) : 0; }
+
+int qw_sample_logits(const float *logits_dev, int32_t vocab, const int32_t *history_dev, int32_t n_history,
+                     const qw_sampling *params, uint64_t *rng_dev, int32_t *token_dev, void *scratch_dev,
+                     size_t scratch_bytes, void *cuda_stream) {
+    if (vocab < 1 || vocab > (1 << 24) || !logits_dev || !rng_dev || !token_dev || !scratch_dev)
+        return QW_INVALID_ARGUMENT;
+    int rc = check_sampling(params, vocab, n_history, history_dev);
+    if (rc) return rc;
+    if (!aligned(scratch_dev, 256) || !aligned(rng_dev, 16)) return QW_ALIGNMENT;
+    if (scratch_bytes < qw::sample_scratch_bytes(vocab)) return QW_OUT_OF_MEMORY;
+    return cuda_status(qw::launch_sample(logits_dev, vocab, history_dev, n_history, params->temperature,
+                                         params->top_k, params->top_p, params->repetition_penalty, rng_dev,
+                                         token_dev, nullptr, nullptr, scratch_dev, (cudaStream_t)cuda_stream));
+}
+
+int qw_sampler_seed(qw_model *m, uint64_t seed, uint64_t stream) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    // PCG32 seeding of the pages: state 0, increment (stream << 1) | 1, advance, add seed, advance
+    uint64_t st = 0, inc = (stream << 1) | 1u;
+    st = st * 6364136223846793005ull + inc;
+    st += seed;
+    st = st * 6364136223846793005ull + inc;
+    const uint64_t host[2] = {st, inc};
+    int rc = cuda_status(cudaMemcpyAsync(m->ws + m->lay.sampler, host, 16, cudaMemcpyHostToDevice, m->stream));
+    if (rc) return rc;
+    return cuda_status(cudaStreamSynchronize(m->stream));  // the host source is a local
+}
+
+int qw_sampler_state(qw_model *m, uint64_t *state_host) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (!state_host) return QW_INVALID_ARGUMENT;
+    int rc = cuda_status(cudaMemcpyAsync(state_host, m->ws + m->lay.sampler, 16, cudaMemcpyDeviceToHost, m->stream));
+    if (rc) return rc;
+    return cuda_status(cudaStreamSynchronize(m->stream));
+}
+
+int qw_sample(qw_model *m, const qw_sampling *params, const int32_t *history_dev, int32_t n_history,
+              int32_t *next_token_host) {
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (m->failed) return m->failed;
+    if (!m->has_last) return QW_INVALID_ARGUMENT;  // no logits yet
+    int rc = check_sampling(params, m->cfg.vocab, n_history, history_dev);
+    if (rc) return rc;
+    uint8_t *base = m->ws + m->lay.sampler;
+    rc = cuda_status(qw::launch_sample(m->logits, m->cfg.vocab, history_dev, n_history, params->temperature,
+                                       params->top_k, params->top_p, params->repetition_penalty,
+                                       reinterpret_cast<uint64_t *>(base), nullptr, &m->flags->next_tok,
+                                       &m->flags->err, base + 256, m->stream));
+    if (rc) return rc;
+    if (next_token_host) return read_flags(m, next_token_host);
+    return QW_OK;
 }
 
 int qw_debug_gemm_f16(const void *a_dev, const void *b_dev, float *c_dev, int32_t M, int32_t N, int32_t K,

@@ -45,7 +45,8 @@ MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_step", "qw_generate", "qw_logits",
            "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
            "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query",
-           "qw_decode_step_noalloc", "qw_debug_gemm_f16")
+           "qw_decode_step_noalloc", "qw_debug_gemm_f16", "qw_sample_scratch_bytes", "qw_sample_logits",
+           "qw_sampler_seed", "qw_sampler_state", "qw_sample")
 
 
 class QwError(RuntimeError):
@@ -65,6 +66,14 @@ class Config(ctypes.Structure):
 class LayerWeights(ctypes.Structure):
     _fields_ = [("input_norm", ctypes.c_void_p), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
                 ("post_norm", ctypes.c_void_p), ("w", ctypes.c_void_p * 7), ("s", ctypes.c_void_p * 7)]
+
+
+class Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("repetition_penalty", ctypes.c_float)]
+
+
+SAMPLE_MAX_TOP_K = 64
 
 
 class Weights(ctypes.Structure):
@@ -107,6 +116,12 @@ def _lib():
             L.qw_decode_step_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, i32, i32, vp,
                                                  vp, vp, i32]
             L.qw_debug_gemm_f16.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
+            L.qw_sample_scratch_bytes.argtypes = [i32]
+            L.qw_sample_scratch_bytes.restype = ctypes.c_size_t
+            L.qw_sample_logits.argtypes = [vp, i32, vp, i32, ctypes.POINTER(Sampling), vp, vp, vp, ctypes.c_size_t, vp]
+            L.qw_sampler_seed.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64]
+            L.qw_sampler_state.argtypes = [vp, vp]
+            L.qw_sample.argtypes = [vp, ctypes.POINTER(Sampling), vp, i32, vp]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -202,6 +217,21 @@ def debug_gemm_f16(a, b, c, bn: int = 256, stream=None):
     N = b.shape[0]
     _check(_lib().qw_debug_gemm_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), int(M), int(N), int(K), int(bn),
                                     st.cuda_stream), "qw_debug_gemm_f16")
+
+
+def sample_logits(logits, params: Sampling, rng, token_out, history=None, scratch=None, stream=None):
+    """qw_sample_logits on device tensors: logits f32 [V], rng uint64 [2] (int64 tensor),
+    token_out int32 [1], history int32 [n] or None."""
+    import torch
+    V = logits.numel()
+    need = _lib().qw_sample_scratch_bytes(V)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    n = 0 if history is None else history.numel()
+    _check(_lib().qw_sample_logits(logits.data_ptr(), V, history.data_ptr() if n else None, n, ctypes.byref(params),
+                                   rng.data_ptr(), token_out.data_ptr(), scratch.data_ptr(), scratch.numel(),
+                                   st.cuda_stream), "qw_sample_logits")
 
 
 class Model:
@@ -305,6 +335,22 @@ class Model:
         v = torch.empty(shape, dtype=dt, device="cuda")
         _check(_lib().qw_kv_export(self._h, k.data_ptr(), v.data_ptr(), int(n_pos)), "qw_kv_export")
         return k, v
+
+    def sampler_seed(self, seed: int, stream: int):
+        _check(_lib().qw_sampler_seed(self._h, ctypes.c_uint64(seed), ctypes.c_uint64(stream)), "qw_sampler_seed")
+
+    def sampler_state(self):
+        out = (ctypes.c_uint64 * 2)()
+        _check(_lib().qw_sampler_state(self._h, out), "qw_sampler_state")
+        return int(out[0]), int(out[1])
+
+    def sample(self, params: Sampling, history=None, want_token: bool = True):
+        """qw_sample: next token from the last position's logits; history: device int32 tensor or None."""
+        out = ctypes.c_int32(-1)
+        n = 0 if history is None else history.numel()
+        _check(_lib().qw_sample(self._h, ctypes.byref(params), history.data_ptr() if n else None, n,
+                                ctypes.byref(out) if want_token else None), "qw_sample")
+        return int(out.value) if want_token else None
 
     def set_debug(self, flags: int):
         _check(_lib().qw_set_debug(self._h, int(flags)), "qw_set_debug")
