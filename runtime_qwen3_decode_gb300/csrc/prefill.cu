@@ -470,32 +470,75 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 }
 
 // h[t] = fp16(w * (x[t] * rsqrt(mean(x[t]^2) + eps))); with tokens, x[t] = f32(E[tok[t]]) first.
+// One warp per row of H = 1024 KM; lane l holds the 8-element chunks l + 32 c.
+template <int KM>
 __global__ void __launch_bounds__(kRowThreads) norm_rows_kernel(float *x, const int32_t *tokens,
                                                                 const __nv_bfloat16 *embed,
-                                                                const __nv_bfloat16 *w, __half *h, int H,
+                                                                const __nv_bfloat16 *w, __half *h, int rows,
                                                                 float eps) {
-    __shared__ float red[kRowThreads / 32];
-    const int t = blockIdx.x;
-    float *xr = x + (size_t)t * H;
-    float v[12];  // H <= 3072
-    const int per = H / kRowThreads;
-    float ss = 0.f;
+    constexpr int H = 1024 * KM, NC = 4 * KM;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (kRowThreads / 32) + warp;
+    if (t >= rows) return;
+    float4 *xr = reinterpret_cast<float4 *>(x + (size_t)t * H);
+    float v[NC][8];
     if (tokens) {
-        const __nv_bfloat16 *er = embed + (size_t)tokens[t] * H;
-        for (int i = 0; i < per; ++i) {
-            v[i] = __bfloat162float(er[threadIdx.x + kRowThreads * i]);
-            xr[threadIdx.x + kRowThreads * i] = v[i];
+        const uint4 *er = reinterpret_cast<const uint4 *>(embed + (size_t)tokens[t] * H);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 u = er[lane + 32 * c];
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(b2[i]);
+                v[c][2 * i] = f.x;
+                v[c][2 * i + 1] = f.y;
+            }
+            xr[2 * (lane + 32 * c)] = make_float4(v[c][0], v[c][1], v[c][2], v[c][3]);
+            xr[2 * (lane + 32 * c) + 1] = make_float4(v[c][4], v[c][5], v[c][6], v[c][7]);
         }
     } else {
-        for (int i = 0; i < per; ++i) v[i] = xr[threadIdx.x + kRowThreads * i];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const float4 a0 = xr[2 * (lane + 32 * c)], a1 = xr[2 * (lane + 32 * c) + 1];
+            v[c][0] = a0.x, v[c][1] = a0.y, v[c][2] = a0.z, v[c][3] = a0.w;
+            v[c][4] = a1.x, v[c][5] = a1.y, v[c][6] = a1.z, v[c][7] = a1.w;
+        }
     }
-    for (int i = 0; i < per; ++i) ss += v[i] * v[i];
-    const float r = rsqrtf(block_sum(ss, red) / (float)H + eps);
-    __half *hr = h + (size_t)t * H;
-    for (int i = 0; i < per; ++i) {
-        const int c = threadIdx.x + kRowThreads * i;
-        hr[c] = __float2half_rn(__bfloat162float(w[c]) * (v[i] * r));
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss += v[c][i] * v[c][i];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / (float)H + eps);
+    const uint4 *wr = reinterpret_cast<const uint4 *>(w);
+    uint4 *hr = reinterpret_cast<uint4 *>(h + (size_t)t * H);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const uint4 u = wr[lane + 32 * c];
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(b2[i]);
+            o[2 * i] = f.x * (v[c][2 * i] * r);
+            o[2 * i + 1] = f.y * (v[c][2 * i + 1] * r);
+        }
+        hr[lane + 32 * c] = pack_half8(o);
     }
+}
+
+cudaError_t launch_norm_rows(float *x, const int32_t *tokens, const __nv_bfloat16 *embed, const __nv_bfloat16 *w,
+                             __half *h, int rows, int H, float eps, cudaStream_t st) {
+    const int grid = (rows + kRowThreads / 32 - 1) / (kRowThreads / 32);
+    switch (H >> 10) {
+        case 1: norm_rows_kernel<1><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
+        case 2: norm_rows_kernel<2><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
+        default: norm_rows_kernel<3><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
+    }
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ K/V fp16 shadows
@@ -890,6 +933,7 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
 
 // logits[v] = E[v] . (final_norm * RMSNorm(x)), packed-key argmax (ties -> lowest id);
 // the last CTA to finish publishes the token and re-arms the key for the next call.
+template <int KM>
 __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float *x, const __nv_bfloat16 *final_norm,
                                                             const __nv_bfloat16 *E, int V, int H, float eps,
                                                             float *logits, unsigned long long *key,
@@ -907,34 +951,54 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float *x, cons
     __syncthreads();
     unsigned long long kbest = 0;
     bool bad = false;
-    const int nchunk = H / 256;  // 16-byte chunks of 8 bf16 per lane
+    constexpr int NC = 4 * KM;  // 16-byte chunks of 8 bf16 per lane and row
     const int gw = blockIdx.x * (kHeadThreads / 32) + warp, nw = gridDim.x * (kHeadThreads / 32);
-    for (int v = gw; v < V; v += nw) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(E + (size_t)v * H);
-        float acc = 0.f;
-        for (int i = 0; i < nchunk; ++i) {
+    // two rows per pass, every load of both rows issued before the arithmetic
+    for (int v0 = gw; v0 < V; v0 += 2 * nw) {
+        const int v1 = v0 + nw < V ? v0 + nw : v0;
+        const uint4 *r0 = reinterpret_cast<const uint4 *>(E + (size_t)v0 * H);
+        const uint4 *r1 = reinterpret_cast<const uint4 *>(E + (size_t)v1 * H);
+        uint4 u0[NC], u1[NC];
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+            u0[i] = __ldg(r0 + lane + 32 * i);
+            u1[i] = __ldg(r1 + lane + 32 * i);
+        }
+        float acc[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
             const int c = lane + 32 * i;
-            const uint4 u = __ldg(row + c);
-            const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
             const float4 h0 = *reinterpret_cast<const float4 *>(hf + 8 * c);
             const float4 h1 = *reinterpret_cast<const float4 *>(hf + 8 * c + 4);
-            float2 f;
-            f = __bfloat1622float2(b[0]);
-            acc += f.x * h0.x + f.y * h0.y;
-            f = __bfloat1622float2(b[1]);
-            acc += f.x * h0.z + f.y * h0.w;
-            f = __bfloat1622float2(b[2]);
-            acc += f.x * h1.x + f.y * h1.y;
-            f = __bfloat1622float2(b[3]);
-            acc += f.x * h1.z + f.y * h1.w;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(r ? &u1[i] : &u0[i]);
+                float2 f;
+                f = __bfloat1622float2(b[0]);
+                acc[r] += f.x * h0.x + f.y * h0.y;
+                f = __bfloat1622float2(b[1]);
+                acc[r] += f.x * h0.z + f.y * h0.w;
+                f = __bfloat1622float2(b[2]);
+                acc[r] += f.x * h1.x + f.y * h1.y;
+                f = __bfloat1622float2(b[3]);
+                acc[r] += f.x * h1.z + f.y * h1.w;
+            }
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        for (int o = 16; o; o >>= 1) {
+            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+            acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
+        }
         if (lane == 0) {
-            logits[v] = acc;
-            if (!isfinite(acc)) bad = true;
-            const unsigned long long k = argmax_key(acc, v);
-            kbest = k > kbest ? k : kbest;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (r == 1 && v1 == v0) break;
+                const int v = r ? v1 : v0;
+                logits[v] = acc[r];
+                if (!isfinite(acc[r])) bad = true;
+                const unsigned long long k = argmax_key(acc[r], v);
+                kbest = k > kbest ? k : kbest;
+            }
         }
     }
     if (lane == 0) {
@@ -1183,7 +1247,7 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
         CUtensorMap mh, mo, ma;
         if (!make_map(&mh, h, m, H, BM) || !make_map(&mo, o16, m, QD, BM) || !make_map(&ma, act, m, I, BM))
             return 1;
-        norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, tok, a.embed, hl[0].input_norm, h, H, a.eps);
+        launch_norm_rows(x, tok, a.embed, hl[0].input_norm, h, m, H, a.eps, stream);
         if (debug & 1)
             cudaMemcpyAsync(a.hidden, x + (size_t)(m - 1) * H, (size_t)H * 4, cudaMemcpyDeviceToDevice, stream);
         for (int l = 0; l < c.n_layers; ++l) {
@@ -1246,7 +1310,7 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             gp.out = x;
             gp.ldo = H;
             if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
-            norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, nullptr, nullptr, hl[l].post_norm, h, H, a.eps);
+            launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, m, H, a.eps, stream);
             // a = silu(h Wg^T) * (h Wu^T)
             gp.N = 2 * I;
             gp.K = H;
@@ -1263,13 +1327,21 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
                 cudaMemcpyAsync(a.hidden + (size_t)(l + 1) * H, x + (size_t)(m - 1) * H, (size_t)H * 4,
                                 cudaMemcpyDeviceToDevice, stream);
             if (l + 1 < c.n_layers)
-                norm_rows_kernel<<<m, kRowThreads, 0, stream>>>(x, nullptr, nullptr, hl[l + 1].input_norm, h, H,
-                                                                a.eps);
+                launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, m, H, a.eps, stream);
         }
         done += m;
         if (done == n) {
-            head_kernel<<<4 * st->nsm, kHeadThreads, 0, stream>>>(x + (size_t)(m - 1) * H, a.final_norm, a.lm_head,
-                                                                  a.V, H, a.eps, a.logits, key, count, a.flags);
+            const float *xl = x + (size_t)(m - 1) * H;
+            const dim3 hg(4 * st->nsm);
+            if (H == 1024)
+                head_kernel<1><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
+                                                                key, count, a.flags);
+            else if (H == 2048)
+                head_kernel<2><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
+                                                                key, count, a.flags);
+            else
+                head_kernel<3><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
+                                                                key, count, a.flags);
         }
         if (cudaGetLastError() != cudaSuccess) return 1;
     }
