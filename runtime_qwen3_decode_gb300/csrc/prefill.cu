@@ -609,32 +609,47 @@ __global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *
 //   S_j = Q K_j^T into one of two TMEM buffers (the tensor core computes S_{j+1} while
 //   the softmax warps work on S_j);
 //   two warps per row apply the causal mask and the online softmax in the log2 domain,
-//   each over 64 of the block's keys, exchanging their block maxima through shared
-//   memory, and write P_j (fp16) to shared memory;
+//   each over 64 of the block's keys, exchange their block maxima through shared
+//   memory, and write P_j (fp16) into tensor memory;
 //   O += P_j V_j accumulates in TMEM.
+// Both A operands live in tensor memory (Q copied there once by the softmax warps, P
+// written by them per block), so the tensor core reads only K and V^T from shared
+// memory.  Per block, shared memory then carries the two 32 KB TMA writes and the two
+// 32 KB operand reads; staging Q and P there as well doubled that traffic, and it was
+// shared-memory bandwidth, not the tensor core or the softmax, that set the block time.
 // O is rescaled only when a row's running max grows by more than 8 (factor 256): O and
 // the row sum l always refer to the same reference max, so O / l is unaffected, and
 // p <= 2^8 stays well inside fp16.
-// Warp 0 issues TMA loads (Q once; K and V^T per block into two 2-stage rings, so K of
-// block j+2 streams in as soon as S_j is done while V waits for P V), warp 1 owns TMEM
-// and issues the MMAs, warps 2-9 run the softmax and the output epilogue.
+// Warp 0 issues the TMA loads of Q once and K per block, warp 10 those of V^T per block,
+// into two independent 3-stage rings (K of block j+3 streams in as soon as S_j is done,
+// V of block j+3 once P_j V_j is; under load a 32 KB tile takes about 3000 cycles to
+// arrive, more than one block's softmax).  The third V stage is the Q tile's shared
+// memory, refilled only after Q has been copied into TMEM.  The two producers sit in different warps: two
+// spinning branches of one warp are not guaranteed to interleave, and a K load held
+// behind a V wait delays S_{j+2} past the end of softmax j+1.  Warp 1 owns TMEM and
+// issues the MMAs; warps 2-9 copy Q into TMEM, run the softmax and the output epilogue.
 
 constexpr int kFaSoftmaxWarps = 8;
-constexpr int kFaThreads = 64 + 32 * kFaSoftmaxWarps;
+constexpr int kFaVWarp = 2 + kFaSoftmaxWarps;
+constexpr int kFaThreads = 32 * (kFaVWarp + 1);
 constexpr int kFaKeys = 128;
-constexpr int kFaStages = 2;
+constexpr int kFaStages = 3;
 
+// Each tile (Q, a K block, a V^T block) is 2 regions x [128 rows][128 B] = 32 KB.
 struct FaSmem {
-    static constexpr int kQ = 0;                         // 2 regions x [128 rows][128 B]
-    static constexpr int kKV = 2 * 16384;                // stages x (K 2 x 16 KB | V^T 2 x 16 KB)
-    static constexpr int kStage = 4 * 16384;
-    static constexpr int kP = kKV + kFaStages * kStage;  // 2 regions x [128 rows][128 B]
-    static constexpr int kX = kP + 2 * 16384;            // block maxima [2 parity][2 halves][128 rows]
+    static constexpr int kTile = 2 * 16384;
+    static constexpr int kQ = 0;                              // Q, later V^T stage 2
+    static constexpr int kK = kTile;                          // K stages 0..2
+    static constexpr int kV = kK + kFaStages * kTile;         // V^T stages 0, 1
+    static constexpr int kX = kV + (kFaStages - 1) * kTile;   // f32 [2 parity][2 halves][128 rows]
     static constexpr int kBar = kX + 2 * 2 * 128 * 4;
     static constexpr int kBytes = kBar + 256;
     static constexpr size_t kDyn = 1024 + kBytes;
 };
+// TMEM columns: S buffers 0 and 128 and O 256 (f32); P 384 and Q 448 (fp16 pairs).
+constexpr uint32_t kFaColO = 256, kFaColP = 384, kFaColQ = 448;
 static_assert(FaSmem::kDyn <= 227 * 1024, "shared memory budget");
+static_assert(kFaStages == 3, "the last V^T stage is the Q tile");
 
 struct FaParams {
     int n, pos0, G, Hq;
@@ -662,13 +677,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     fa_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const FaParams p) {
     uint8_t *base = smem_base1024();
-    uint8_t *sQ = base + FaSmem::kQ, *sKV = base + FaSmem::kKV, *sP = base + FaSmem::kP;
-    float *mx = reinterpret_cast<float *>(base + FaSmem::kX);
+    uint8_t *sQ = base + FaSmem::kQ, *sK = base + FaSmem::kK, *sV = base + FaSmem::kV;
+    float *sX = reinterpret_cast<float *>(base + FaSmem::kX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + FaSmem::kBar);
-    uint64_t *q_full = bars, *k_full = bars + 1, *k_empty = bars + 3, *v_full = bars + 5, *v_empty = bars + 7,
-             *s_full = bars + 9, *s_free = bars + 11, *p_full = bars + 13, *pv_done = bars + 14, *xbar = bars + 15,
-             *drain = bars + 19;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 20);
+    uint64_t *q_full = bars, *q_tm = bars + 1, *k_full = bars + 2, *k_empty = bars + 5, *v_full = bars + 8,
+             *v_empty = bars + 11, *s_full = bars + 14, *s_free = bars + 16, *p_full = bars + 18, *pv_done = bars + 19,
+             *xbar = bars + 20, *drain = bars + 24;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 25);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -682,11 +697,14 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        mbar_init(q_tm, kFaSoftmaxWarps);
+        for (int i = 0; i < kFaStages; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], kFaSoftmaxWarps);
         }
@@ -702,12 +720,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tO = tmem + 256;  // S buffers at columns 0 and 128
+    const uint32_t tO = tmem + kFaColO;  // S buffers at columns 0 and 128
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer
-            int k_par[kFaStages] = {-1, -1}, v_par[kFaStages] = {-1, -1};
+            // ---- TMA producer of Q, then K per block
+            int par[kFaStages] = {-1, -1, -1};
             bool ok = true;
             mbar_expect_tx(q_full, 4 * 8192);
             for (int half = 0; half < 2; ++half) {
@@ -719,41 +737,61 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             for (int j = 0; j < nkb; ++j) {
                 const int st = j % kFaStages;
                 const unsigned ph = (unsigned)(j / kFaStages) & 1u;
-                uint8_t *sk = sKV + st * FaSmem::kStage, *sv = sk + 2 * 16384;
                 if (!mbar_wait(&k_empty[st], ph ^ 1u, abort, true, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 mbar_expect_tx(&k_full[st], 2 * 16384);
+                uint8_t *sk = sK + st * FaSmem::kTile;
                 for (int reg = 0; reg < 2; ++reg)
                     tma_load_2d(sk + reg * 16384, &tk, reg * 64, g * p.kv_rows + j * kFaKeys, &k_full[st]);
-                k_par[st] = (int)ph;
-                if (!mbar_wait(&v_empty[st], ph ^ 1u, abort, true, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                mbar_expect_tx(&v_full[st], 2 * 16384);
-                for (int reg = 0; reg < 2; ++reg)
-                    tma_load_2d(sv + reg * 16384, &tv, j * kFaKeys + reg * 64, g * kHeadDim, &v_full[st]);
-                v_par[st] = (int)ph;
+                par[st] = (int)ph;
             }
             if (!ok) {
                 *abort = 1;
                 raise(p.flags, kErrInvariant);
                 // no copy may land in shared memory after this CTA has exited
                 mbar_wait(q_full, 0, abort, false, kWaitLimitNs);
-                for (int i = 0; i < kFaStages; ++i) {
-                    if (k_par[i] >= 0) mbar_wait(&k_full[i], (unsigned)k_par[i], abort, false, kWaitLimitNs);
-                    if (v_par[i] >= 0) mbar_wait(&v_full[i], (unsigned)v_par[i], abort, false, kWaitLimitNs);
+                for (int i = 0; i < kFaStages; ++i)
+                    if (par[i] >= 0) mbar_wait(&k_full[i], (unsigned)par[i], abort, false, kWaitLimitNs);
+            }
+        }
+    } else if (warp == kFaVWarp) {
+        if (lane == 0) {
+            // ---- TMA producer of V^T per block
+            int par[kFaStages] = {-1, -1, -1};
+            bool ok = true;
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j % kFaStages;
+                const unsigned ph = (unsigned)(j / kFaStages) & 1u;
+                // stage 2 is Q's tile: its first fill waits until Q sits in TMEM
+                if (!mbar_wait(&v_empty[st], ph ^ 1u, abort, true, kWaitLimitNs) ||
+                    (j == 2 && !mbar_wait(q_tm, 0, abort, true, kWaitLimitNs))) {
+                    ok = false;
+                    break;
                 }
+                mbar_expect_tx(&v_full[st], 2 * 16384);
+                uint8_t *sv = st == 2 ? sQ : sV + st * FaSmem::kTile;
+                for (int reg = 0; reg < 2; ++reg)
+                    tma_load_2d(sv + reg * 16384, &tv, j * kFaKeys + reg * 64, g * kHeadDim, &v_full[st]);
+                par[st] = (int)ph;
+            }
+            if (!ok) {
+                *abort = 1;
+                raise(p.flags, kErrInvariant);
+                for (int i = 0; i < kFaStages; ++i)
+                    if (par[i] >= 0) mbar_wait(&v_full[i], (unsigned)par[i], abort, false, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer: S_j, then P_{j-1} V_{j-1}
+            // ---- MMA issuer: S_j, then P_{j-2} V_{j-2}; A operands (Q, P) in TMEM.  S_j
+            // only needs softmax j-2 to have read S_{j-2} (the start of that softmax), so it
+            // goes ahead of P_{j-2} V_{j-2}, which needs the end of it: the next S is always
+            // ready before the softmax warps reach it.
             constexpr uint32_t idesc = idesc_f16_f32(128, 128);
-            bool ok = mbar_wait(q_full, 0, abort, true, kWaitLimitNs);
-            for (int j = 0; ok && j <= nkb; ++j) {
+            bool ok = mbar_wait(q_tm, 0, abort, true, kWaitLimitNs);
+            for (int j = 0; ok && j < nkb + 2; ++j) {
                 if (j < nkb) {
                     const int st = j % kFaStages;
                     if (!mbar_wait(&k_full[st], (unsigned)(j / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
@@ -763,30 +801,28 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *sk = sKV + st * FaSmem::kStage;
+                    const uint32_t sk = su32(sK + st * FaSmem::kTile);
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint64_t ad = desc_sw128(su32(sQ + (k >> 2) * 16384)) + 2u * (k & 3);
-                        const uint64_t bd = desc_sw128(su32(sk + (k >> 2) * 16384)) + 2u * (k & 3);
-                        mma_f16(tmem + 128u * (j & 1), ad, bd, idesc, k != 0);
+                        const uint64_t bd = desc_sw128(sk + (k >> 2) * 16384) + 2u * (k & 3);
+                        mma_f16_ts(tmem + 128u * (j & 1), tmem + kFaColQ + 8u * k, bd, idesc, k != 0);
                     }
                     mma_commit(&s_full[j & 1]);
                     mma_commit(&k_empty[st]);
                 }
-                if (j >= 1) {
-                    const int i = j - 1, st = i % kFaStages;
+                if (j >= 2) {
+                    const int i = j - 2, st = i % kFaStages;
                     if (!mbar_wait(&v_full[st], (unsigned)(i / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
                         !mbar_wait(p_full, (unsigned)i & 1u, abort, true, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *sv = sKV + st * FaSmem::kStage + 2 * 16384;
+                    const uint32_t sv = su32(st == 2 ? sQ : sV + st * FaSmem::kTile);
 #pragma unroll
                     for (int k = 0; k < kFaKeys / 16; ++k) {
-                        const uint64_t ad = desc_sw128(su32(sP + (k >> 2) * 16384)) + 2u * (k & 3);
-                        const uint64_t bd = desc_sw128(su32(sv + (k >> 2) * 16384)) + 2u * (k & 3);
-                        mma_f16(tO, ad, bd, idesc, i > 0 || k > 0);
+                        const uint64_t bd = desc_sw128(sv + (k >> 2) * 16384) + 2u * (k & 3);
+                        mma_f16_ts(tO, tmem + kFaColP + 8u * k, bd, idesc, i > 0 || k > 0);
                     }
                     mma_commit(pv_done);
                     mma_commit(&v_empty[st]);
@@ -802,16 +838,35 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         }
     } else {
         // ---- softmax warps 2..9: lane quarter q = warp % 4, row r = 32 q + lane; warp half
-        // hf takes keys [64 hf, 64 hf + 64) of every block, P region hf and O dims [64 hf, +64)
+        // hf takes head dims [64 hf, +64) of Q, keys [64 hf, 64 hf + 64) of every block (P
+        // columns [32 hf, +32)) and O dims [64 hf, +64)
         const int q = warp & 3, hf = (warp - 2) >> 2, r = 32 * q + lane;
         const int t = G == 2 ? t0 + (r & 63) : t0 + r;
         const int head = g * G + (G == 2 ? (r >> 6) : 0);
         const int pr = p.pos0 + t;
-        const uint32_t lb = ((uint32_t)(32 * q) << 16) + 64u * hf;
+        const uint32_t lb0 = (uint32_t)(32 * q) << 16, lb = lb0 + 64u * hf;
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nkb; ++j) {
+        // Q row r, dims [64 hf, +64): eight 16-byte chunks of the swizzled tile, already
+        // fp16 pairs in K order, into 32 TMEM columns
+        bool ok = warp_wait(q_full, 0, abort);
+        if (ok) {
+            uint32_t qv[32];
+            const uint8_t *src = sQ + hf * 16384;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(src + swz128(r, c));
+                qv[4 * c] = u.x;
+                qv[4 * c + 1] = u.y;
+                qv[4 * c + 2] = u.z;
+                qv[4 * c + 3] = u.w;
+            }
+            tmem_st32u(tmem + lb0 + kFaColQ + 32u * hf, qv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_tm);
+        }
+        for (int j = 0; ok && j < nkb; ++j) {
             const int b = j & 1;
             if (!warp_wait(&s_full[b], (unsigned)(j >> 1) & 1u, abort)) {
                 ok = false;
@@ -837,24 +892,28 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 64; ++i) mb = fmaxf(mb, s[i >> 5][i & 31]);
             }
-            // the row's maximum over the whole block, from both halves
-            mx[(b * 2 + hf) * 128 + r] = mb;
+            // the row's maximum over the whole block, from both halves (the two warps of
+            // a lane quarter; exchange slots of parity b)
+            float *xb = sX + 256 * b;
+            xb[128 * hf + r] = mb;
+            __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar[q]);
             if (!warp_wait(&xbar[q], (unsigned)j & 1u, abort)) {
                 ok = false;
                 break;
             }
-            mb = fmaxf(mb, mx[(b * 2 + (hf ^ 1)) * 128 + r]) * sc;
+            __syncwarp();
+            mb = fmaxf(mb, xb[128 * (hf ^ 1) + r]) * sc;
             const bool resc = mb > m_used + 8.f;
             const float m_new = resc ? mb : m_used;
             const float factor = resc ? fast_exp2(m_used - m_new) : 1.f;
-            // O (for the rescale) and the P buffer are free once P_{j-1} V_{j-1} has completed
-            if (j >= 1 && !warp_wait(pv_done, (unsigned)(j - 1) & 1u, abort)) {
-                ok = false;
-                break;
-            }
+            // O must hold P_{j-1} V_{j-1} before it is rescaled
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                if (!warp_wait(pv_done, (unsigned)(j - 1) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -867,30 +926,41 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             }
             l *= factor;
             m_used = m_new;
-            uint8_t *pb = sP + hf * 16384;
+            // P for keys 2c, 2c + 1 of this half in column c
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float e[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    e[i] = fast_exp2(fmaf(s[c >> 2][8 * (c & 3) + i], sc, -m_used));
-                    l += e[i];
-                }
-                *reinterpret_cast<uint4 *>(pb + swz128(r, c)) = pack_half8(e);
+            for (int c = 0; c < 32; ++c) {
+                const float e0 = fast_exp2(fmaf(s[c >> 4][2 * (c & 15)], sc, -m_used));
+                const float e1 = fast_exp2(fmaf(s[c >> 4][2 * (c & 15) + 1], sc, -m_used));
+                l += e0;
+                l += e1;
+                __half2 h = __floats2half2_rn(e0, e1);
+                pk[c] = *reinterpret_cast<uint32_t *>(&h);
             }
-            fence_async_shared();
+            // the P columns are free once P_{j-1} V_{j-1} has completed
+            if (j > 0 && !warp_wait(pv_done, (unsigned)(j - 1) & 1u, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st32u(tmem + lb0 + kFaColP + 32u * hf, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
-        // row sum over both halves (the exchange buffer of the parity after the last block)
+        // row sum over both halves (exchange slots of the parity after the last block)
         if (ok) {
-            mx[((nkb & 1) * 2 + hf) * 128 + r] = l;
+            float *xb = sX + 256 * (nkb & 1);
+            xb[128 * hf + r] = l;
+            __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar[q]);
             ok = warp_wait(&xbar[q], (unsigned)nkb & 1u, abort);
+            if (ok) {
+                __syncwarp();
+                l += xb[128 * (hf ^ 1) + r];
+            }
         }
-        if (ok) l += mx[((nkb & 1) * 2 + (hf ^ 1)) * 128 + r];
         if (ok && !warp_wait(pv_done, (unsigned)(nkb - 1) & 1u, abort)) ok = false;
         if (ok) {
             tc_fence_after();
