@@ -900,7 +900,9 @@ __device__ __forceinline__ void attn_block(const uint8_t *kb, const uint8_t *vb,
 // One (KV head, split) item: QK-Norm + RoPE of the group's queries and of the new key,
 // append k, v at this position (the last split owns it), online softmax over the
 // split's cached positions (+ the new one), and the split's tagged partial (acc, max,
-// sum) for each query head of the group.  The o_proj phase merges the partials.
+// sum) for each query head of the group; the CTA that finishes a KV head's last split
+// merges the partials into the group's output.  A single split writes the output
+// directly.
 template <int G, typename KT>
 __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
     using T = KvTraits<KT>;
@@ -1057,6 +1059,10 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
                 ls = fmaf(sm.wml[w][h][1], sc, ls);
             }
         }
+        if (S == 1) {  // the only split: its result is the group's output
+            st_tag(a.ot + (size_t)(kvh * G + h) * kHeadDim + dim, av / ls, out_tag);
+            continue;
+        }
         unsigned long long *pp = a.partt + ((size_t)(kvh * S + p.s) * G + h) * kPartStride;
         st_tag(pp + dim, av, out_tag);
         if (dim == 0) {
@@ -1064,6 +1070,7 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
             st_tag(pp + kHeadDim + 1, ls, out_tag);
         }
     }
+    if (S == 1) return (int)(it | (dead ? kDeadBit : 0u));
     // The CTA that finishes the last split of this KV head merges all S partials into the
     // group's attention output (once, instead of in every o_proj CTA):
     // o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s.

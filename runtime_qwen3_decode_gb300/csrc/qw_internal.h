@@ -29,10 +29,15 @@ constexpr int kPartStride = kHeadDim + 4;    // split-attention partial: acc[128
 constexpr int kMaxOwnRows = 64;             // residual rows per CTA kept in shared memory
 constexpr int kMaxKvHeads = 32;             // split-merge counters per layer
 constexpr int kMaxSplits = 21;              // attention splits per KV head (3 per consumer warp in the merge)
-// Attention splits for a step at position pos: one chunk of cached rows per split, at
-// most one split per CTA and KV head, at most kMaxSplits.
+// Cached-row chunks per attention split.  A split streams its chunks through the
+// CTA's ring back to back; every extra split adds a tagged partial that the merge
+// must wait for, so splits are only worth it once a split's own stream takes longer
+// than that round trip.
+constexpr int kSplitChunks = 2;
+// Attention splits for a step at position pos: kSplitChunks chunks of cached rows per
+// split, at most one split per CTA and KV head, at most kMaxSplits.
 inline int attn_splits(int pos, int kv_elem_bytes, int ncta, int n_kv_heads) {
-    const int ch = kv_chunk_rows(kv_elem_bytes);
+    const int ch = kv_chunk_rows(kv_elem_bytes) * kSplitChunks;
     int s = (pos + ch - 1) / ch;
     const int cap = ncta / n_kv_heads < kMaxSplits ? ncta / n_kv_heads : kMaxSplits;
     if (s > cap) s = cap;
