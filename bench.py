@@ -155,11 +155,18 @@ def kernel_traffic():
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    src = os.path.join(ROOT, "runtime_qwen3_decode_gb300", "csrc", "decode.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if d.get("decode_cu_sha256_16") != sha:
+    if d.get("source_sha256_16") != decode_source_sha():
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def decode_source_sha():
+    """First 16 hex digits of the SHA-256 over the decode kernel's sources (its .cu and the
+    shared constants header), in this order."""
+    h = hashlib.sha256()
+    for f in ("decode.cu", "qw_internal.h"):
+        h.update(open(os.path.join(ROOT, "runtime_qwen3_decode_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def dist_info():

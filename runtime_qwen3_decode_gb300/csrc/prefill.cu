@@ -689,8 +689,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, QT = 128 / G;
     const int ntq = (p.n + QT - 1) / QT;
-    const int qt = ntq - 1 - (int)blockIdx.x;  // longest (latest) tiles first
-    const int g = blockIdx.y;
+    // block i: query tile ntq-1-i/Hkv of KV head i%Hkv.  Blocks start in index order, so
+    // the longest (latest) tiles of every head go first and the short ones fill the tail;
+    // a (tile, head) grid would start all tiles of the first heads before the longest
+    // tiles of the last ones.
+    const int Hkv = p.Hq / G;
+    const int qt = ntq - 1 - (int)blockIdx.x / Hkv;
+    const int g = (int)blockIdx.x % Hkv;
     const int t0 = qt * QT;
     const int nkb = (p.pos0 + min(t0 + QT, p.n) - 1) / kFaKeys + 1;
     const int first_masked = (p.pos0 + t0) / kFaKeys;  // blocks from here on cross the diagonal
@@ -1372,7 +1377,7 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             fp.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
             fp.o16 = o16;
             fp.flags = a.flags;
-            const dim3 ag((m + 128 / G - 1) / (128 / G), Hkv);
+            const dim3 ag((m + 128 / G - 1) / (128 / G) * Hkv);
             fa_kernel<<<ag, kFaThreads, FaSmem::kDyn, stream>>>(im->tq, im->tk, im->tv, fp);
             // x += o Wo^T
             gp.N = H;
