@@ -6,8 +6,8 @@
 // The Numerical Authority", section 2 steps 1-7 give the per-row arithmetic):
 //
 //   embed+norm   x = f32(E[tok]), h = fp16(RMSNorm(x) * w_in)            row kernel
-//   QKV GEMM     qkv = h Wqkv^T                    (f32 out)              tcgen05
-//   qk/rope      QK-Norm + RoPE of q (fp16 out) and k, K/V rows -> cache  row kernel
+//   QKV GEMM     qkv = h Wqkv^T, epilogue: QK-Norm + RoPE of q (fp16 out)
+//                and k, K/V rows -> cache, fp16 K / V^T shadows           tcgen05
 //   attention    causal GQA, S = Q K^T, online softmax, O += P V          tcgen05
 //   O GEMM       x += o Wo^T                       (residual epilogue)    tcgen05
 //   norm         h = fp16(RMSNorm(x) * w_post)                            row kernel
