@@ -422,7 +422,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_decode", choices=sorted(qi.WORKLOADS))
-    ap.add_argument("--cpu-steps", type=int, default=24)
+    ap.add_argument("--cpu-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-workload", default="qwen3_0p6b_prefill2048", choices=sorted(qi.WORKLOADS))
     ap.add_argument("--prefill-reps", type=int, default=5)
