@@ -83,12 +83,13 @@ enum qw_kv_format {
 };
 
 /*
- * Model dimensions.  Supported by the kernels: head_dim == 128;
- * n_heads % n_kv_heads == 0 with group size n_heads/n_kv_heads in {1, 2};
- * hidden, n_heads*head_dim and intermediate each a multiple of 1024 and at
- * most 3072; vocab >= 1; 1 <= n_layers <= 64; 1 <= max_ctx <= 131072.
- * Anything else returns QW_UNSUPPORTED_SHAPE.  rms_eps is the RMSNorm epsilon
- * (1e-6 for Qwen3), rope_theta the RoPE base (1e6 for Qwen3).
+ * Model dimensions.  The decode kernel is built for the Qwen3-0.6B decoder block
+ * ("M1 - Load the weights", the layer tensor table): hidden 1024, n_heads 16,
+ * n_kv_heads 8, head_dim 128, intermediate 3072.  Free: 1 <= n_layers <= 64,
+ * vocab >= 1, 1 <= max_ctx <= 131072, rms_eps (the RMSNorm epsilon, 1e-6 for
+ * Qwen3) and rope_theta (the RoPE base, 1e6 for Qwen3).  Any other block returns
+ * QW_UNSUPPORTED_SHAPE (QW_UNSUPPORTED_QUANTIZATION when a dimension is not a
+ * multiple of 32).
  */
 typedef struct {
     int32_t n_layers;
@@ -222,8 +223,12 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos);
  * stream after the embedding and after each layer, read by qw_debug_hidden.
  * QW_DEBUG_PREFILL_BY_TOKEN: qw_prefill runs the prompt through the decode
  * path one token at a time (the differential baseline of the batched prefill).
+ * QW_DEBUG_TRACE: decode steps record a timeline (qw_debug_trace).
+ * QW_DEBUG_ONE_GROUP: decode steps run with every SM in one group instead of one
+ * group per die (the layout used where no two-die structure is measured; o_proj
+ * and down then sum all columns in one dot product instead of two halves).
  */
-enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2, QW_DEBUG_TRACE = 4 };
+enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2, QW_DEBUG_TRACE = 4, QW_DEBUG_ONE_GROUP = 8 };
 int qw_set_debug(qw_model *m, int32_t flags);
 
 /*
@@ -235,14 +240,27 @@ int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
 /*
  * Timeline of the last decode step (needs QW_DEBUG_TRACE): uint64 %globaltimer
  * nanoseconds [phase][cta][8], phase = 5*layer + {0 QKV, 1 attention, 2 o_proj,
- * 3 gate/up, 4 down} and 5*n_layers for the head; stamps 0..3 = consumer before
- * its wait, after the wait, after its work, after its arrival; 4, 5 = producer's
- * first and last copy issue of the phase.  n must equal QW_QUERY_TRACE_LEN.
+ * 3 gate/up, 4 down} and 5*n_layers for the head; stamps 0..3 = consumer entering
+ * the phase, its inputs arrived, inputs staged (compute starts), phase done; 4, 5 =
+ * producer's first and last copy issue of the phase.  n must equal
+ * QW_QUERY_TRACE_LEN.
  */
 int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n);
 
-/* Integer facts about a created model. */
-enum { QW_QUERY_DECODE_CTAS = 1, QW_QUERY_TRACE_LEN = 2, QW_QUERY_WORKSPACE_BYTES = 3 };
+/* Integer facts about a created model: CTAs of a decode step, timeline length, workspace
+ * bytes, SM groups of the decode step (2 = one per die, 1 = none measured), CTAs in group 0,
+ * the measured same-die and cross-die ping-pong round trips in ns (0 when one group), and
+ * where the decode step's exchange pages sit in the workspace. */
+enum {
+    QW_QUERY_DECODE_CTAS = 1,
+    QW_QUERY_TRACE_LEN = 2,
+    QW_QUERY_WORKSPACE_BYTES = 3,
+    QW_QUERY_DECODE_GROUPS = 4,
+    QW_QUERY_GROUP0_CTAS = 5,
+    QW_QUERY_RT_NEAR_NS = 6,
+    QW_QUERY_RT_FAR_NS = 7,
+    QW_QUERY_XREGION_OFFSET = 8  /* byte offset of the exchange pages in the workspace (tests) */
+};
 int qw_query(const qw_model *m, int32_t what, int64_t *out);
 
 /*
@@ -251,19 +269,27 @@ int qw_query(const qw_model *m, int32_t what, int64_t *out);
  * memory when they decode, e.g. code running inside another framework's memory
  * pool or under a fixed memory budget, where a cudaMalloc would fail or stall the
  * device).  No handle and no workspace: the caller passes the config, the weight
- * table, the K/V cache planes (device, [n_layers][n_kv_heads][max_ctx][head_dim]
- * in cfg->kv_format; rows [0, pos) hold earlier positions, row pos is written),
- * the position pos, the input token id, and device outputs logits_dev (f32
- * [vocab]) and next_token_dev (int32, the greedy pick).  Every other buffer lives
- * in one fixed 1 MiB array in the library's device memory, which holds configs of
- * up to 64 layers on GPUs of up to 256 SMs; larger needs return QW_OUT_OF_MEMORY
- * with a message on stderr.  The library calls no allocating routine here.
- * The first call on a device sets the array up (looks up its device address and
- * zeroes it) and must come before any stream capture.  The array is shared by all
- * calls on a device and keeps the last call's contents (counters and flags are
- * zeroed by every call), so calls that overlap on the GPU race: serialise them.
- * The call waits for the stream after copying the layer table and the RoPE row;
- * with wait != 0 it also waits for the step and returns any device-side error.
+ * table, the K/V cache planes, the position pos, the input token id, and device
+ * outputs logits_dev and next_token_dev.  The caller's buffers must be:
+ *   k_cache, v_cache: device, n_layers * n_kv_heads * max_ctx * head_dim elements
+ *     each, of the element type cfg->kv_format names (f32 or bf16), laid out
+ *     [n_layers][n_kv_heads][max_ctx][head_dim]; rows [0, pos) hold earlier
+ *     positions, row pos is written;
+ *   logits_dev: device f32 [vocab]; next_token_dev: device int32 (the greedy pick).
+ * The library cannot see the sizes of these buffers; smaller ones are read and
+ * written out of bounds.  Every other buffer lives in one fixed 4 MiB array in the
+ * library's device memory, which holds configs of up to 64 layers; a larger
+ * need returns QW_OUT_OF_MEMORY with a message on stderr.  The library calls no
+ * allocating routine here.  The first call on a device sets the array up: it looks
+ * up the array's device address, zeroes it, and measures which SMs and which of the
+ * array's 4 KB pages sit on which die of the GPU (a few short kernels, about 20 ms,
+ * waited for); that first call must come before any stream capture.  The array is
+ * shared by all calls on a device and keeps the last call's contents (flags, keys
+ * and counters are zeroed by every call), so calls that overlap on the GPU race:
+ * serialise them.  The call waits for the stream after copying the layer table and
+ * the RoPE row; with wait != 0 it also waits for the step and returns any
+ * device-side error.  The step runs the same kernel with the same SM groups as a
+ * model created on the same device, so the two give identical results.
  */
 int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *weights, void *k_cache, void *v_cache,
                            int32_t pos, int32_t token, float *logits_dev, int32_t *next_token_dev,

@@ -6,10 +6,11 @@
 // synchronise the device or fail under a cap).  qw_decode_step_noalloc serves them: the
 // caller passes the weights, the K/V cache, the input token and the output
 // buffers, and every other buffer the decode kernel needs (the tagged exchange
-// words between phases, split-attention partials, arrival counters, argmax keys,
-// the layer pointer table and this position's RoPE row) lives in one file-scope
-// device array of fixed size, kScratchBytes.  The kernel itself is the unchanged
-// decode kernel of decode.cu.
+// pages between phases, argmax keys and the arrival counter, the layer pointer table,
+// this position's RoPE row, the SM-group tables and the probe scratch) lives in one
+// file-scope device array of fixed size, kScratchBytes.  The kernel itself is the
+// unchanged decode kernel of decode_kernel.cuh, with the same SM groups as a model
+// created on the same device, so both give the same bits.
 //
 // The array is shared by every call in the process on a given device and keeps the
 // last call's contents, so calls whose work overlaps on the GPU (different streams,
@@ -25,50 +26,28 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = 1u << 20;  // 1 MiB per device
+constexpr size_t kScratchBytes = (size_t)4 << 20;  // 4 MiB per device
 constexpr int kMaxDevices = 64;
-constexpr int kMaxNoallocCtas = 256;
 
-// Scratch regions (bytes, 256-aligned offsets inside the array)
-constexpr size_t kOffFlags = 0;         // StepFlags
-constexpr size_t kOffStep = 256;        // argmax keys [2] + arrival counters [5 L + 1]
-constexpr size_t kOffLayers = 2048;     // DevLayer [n_layers]
-constexpr size_t kOffRope = 12288;      // float2 [head_dim / 2], this call's position
-constexpr size_t kOffTagged = 16384;    // tagged words: xa, xb, qkvt, actt, partt, ot; then merge counters
+// Regions of the array (byte offsets; the array itself is 256-aligned)
+constexpr size_t kOffFlags = 0;                                   // StepFlags
+constexpr size_t kOffStep = 256;                                  // argmax keys [2] + head arrival counter
+constexpr size_t kOffRope = 512;                                  // float2 [head_dim / 2], this call's position
+constexpr size_t kOffLayers = 1024;                               // DevLayer [n_layers]
+constexpr size_t kOffRoles = kOffLayers + 64 * 160;               // uint16 [2][kMaxSmIds]
+constexpr size_t kOffPlans = kOffRoles + 2 * qw::kMaxSmIds * 2;   // XPlan [2]
+constexpr size_t kOffProbe = 65536;                               // probe scratch (4 KB aligned after rounding)
+constexpr size_t kOffXRegion = kOffProbe + qw::kProbeScratchBytes + 4096;  // exchange pages (4 KB aligned)
+static_assert(64 * 160 >= qw::kMaxLayers * sizeof(qw::DevLayer), "layer table space");
+static_assert(kOffPlans + 2 * sizeof(qw::XPlan) <= kOffProbe, "plan space");
+static_assert(kOffXRegion + qw::kXRegionBytes + 4096 <= kScratchBytes, "exchange pages fit the array");
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void *g_ptr[kMaxDevices];        // device address of g_scratch, per device (set-up done when non-null)
 uint32_t g_seq[kMaxDevices];     // tag sequence of the last call on each device
-
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-struct TaggedLayout {
-    size_t xa, xb, qkvt, actt, partt, ot, merge, end;
-};
-
-TaggedLayout tagged_layout(const qw_config &c, int ncta) {
-    TaggedLayout t;
-    const int g = c.n_heads / c.n_kv_heads;
-    size_t off = kOffTagged;
-    t.xa = off;
-    off += align256((size_t)c.hidden * 8);
-    t.xb = off;
-    off += align256((size_t)c.hidden * 8);
-    t.qkvt = off;
-    off += align256((size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim * 8);
-    t.actt = off;
-    off += align256((size_t)c.intermediate * 8);
-    t.partt = off;
-    off += align256((size_t)ncta * g * qw::kPartStride * 8);
-    t.ot = off;
-    off += align256((size_t)c.n_heads * c.head_dim * 8);
-    t.merge = off;
-    off += align256(qw::merge_block_bytes(c.n_layers));
-    t.end = off;
-    return t;
-}
+qw::GroupPlans g_plans[kMaxDevices];
 
 int cuda_rc(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return QW_OK;
@@ -77,6 +56,8 @@ int cuda_rc(cudaError_t e, const char *what) {
 }
 
 bool aligned16(const void *p) { return p && ((uintptr_t)p % 16) == 0; }
+
+unsigned char *align4k(unsigned char *p) { return (unsigned char *)(((uintptr_t)p + 4095) & ~(uintptr_t)4095); }
 
 }  // namespace
 
@@ -116,58 +97,74 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
         fprintf(stderr, "qw_decode_step_noalloc: device compute capability %d.%d; built for sm_103a only\n", major, minor);
         return QW_CUDA_ERROR;
     }
-    const int ncta = nsm;
-    const int group = cfg->n_heads / cfg->n_kv_heads;
-
-    // everything must fit the fixed array; say so plainly when it does not
-    const TaggedLayout t = tagged_layout(*cfg, ncta);
-    const size_t step_bytes = 16 + 4 * ((size_t)qw::kPhasesPerLayer * cfg->n_layers + 1);
-    if (ncta > kMaxNoallocCtas || t.end > kScratchBytes || kOffStep + step_bytes > kOffLayers ||
-        kOffLayers + (size_t)cfg->n_layers * sizeof(qw::DevLayer) > kOffRope ||
-        kOffRope + (size_t)cfg->head_dim / 2 * sizeof(float2) > kOffTagged ||
-        (cfg->hidden + ncta - 1) / ncta > qw::kMaxOwnRows) {
-        fprintf(stderr,
-                "qw_decode_step_noalloc: this config needs %zu bytes of fixed scratch (%d CTAs); the static array "
-                "holds %zu bytes for at most %d CTAs\n",
-                t.end, ncta, kScratchBytes, kMaxNoallocCtas);
+    if (cfg->n_layers * sizeof(qw::DevLayer) > kOffRoles - kOffLayers) {
+        fprintf(stderr, "qw_decode_step_noalloc: %d layers do not fit the fixed array\n", cfg->n_layers);
         return QW_OUT_OF_MEMORY;
     }
 
     cudaStream_t stream = (cudaStream_t)cuda_stream;
     int bps = 0;
-    rc = cuda_rc(qw::decode_prepare(group, &bps), "decode_prepare");  // shared-memory attribute of the kernel
+    rc = cuda_rc(qw::decode_prepare(&bps), "decode_prepare");  // shared-memory attribute of the kernel
     if (rc) return rc;
     if (bps < 1) return QW_CUDA_ERROR;
     unsigned char *base = nullptr;
     uint32_t seq = 0;
+    const qw::GroupPlans *gp = nullptr;
     {
         std::lock_guard<std::mutex> g(g_mu);
         if (!g_ptr[dev]) {
             // Once per device, with that device current: find the array's device
             // address (in host code g_scratch is only a stand-in symbol, not an address
-            // the GPU can use) and zero the array.  This first call on a device therefore
-            // enqueues a memset and must come before any stream capture.
+            // the GPU can use), zero the array, and measure which SMs and which of its
+            // exchange pages sit on which die.  This first call on a device therefore
+            // launches kernels and waits for them, and must come before any stream capture.
             void *p = nullptr;
             rc = cuda_rc(cudaGetSymbolAddress(&p, g_scratch), "cudaGetSymbolAddress");
             if (rc) return rc;
-            rc = cuda_rc(cudaMemsetAsync(p, 0, kScratchBytes, stream), "cudaMemsetAsync");
+            unsigned char *b = (unsigned char *)p;
+            rc = cuda_rc(cudaMemsetAsync(b, 0, kScratchBytes, stream), "cudaMemsetAsync");
+            if (rc) return rc;
+            qw::GroupPlans &pl = g_plans[dev];
+            if (qw::plan_groups(dev, align4k(b + kOffProbe), align4k(b + kOffXRegion), cfg->hidden, cfg->n_heads,
+                                cfg->n_kv_heads, cfg->intermediate, stream, &pl)) {
+                fprintf(stderr, "qw_decode_step_noalloc: measuring the SM groups failed\n");
+                return QW_CUDA_ERROR;
+            }
+            if (pl.ncta != nsm) return QW_CUDA_ERROR;
+            rc = cuda_rc(cudaMemcpyAsync(b + kOffRoles, pl.role1, sizeof(pl.role1), cudaMemcpyHostToDevice, stream),
+                         "cudaMemcpyAsync");
+            if (!rc)
+                rc = cuda_rc(cudaMemcpyAsync(b + kOffRoles + sizeof(pl.role1), pl.role2, sizeof(pl.role2),
+                                             cudaMemcpyHostToDevice, stream), "cudaMemcpyAsync");
+            if (!rc)
+                rc = cuda_rc(cudaMemcpyAsync(b + kOffPlans, &pl.plan1, sizeof(qw::XPlan), cudaMemcpyHostToDevice,
+                                             stream), "cudaMemcpyAsync");
+            if (!rc)
+                rc = cuda_rc(cudaMemcpyAsync(b + kOffPlans + sizeof(qw::XPlan), &pl.plan2, sizeof(qw::XPlan),
+                                             cudaMemcpyHostToDevice, stream), "cudaMemcpyAsync");
+            // the page probe wrote into the exchange pages: clear them (tag 0 is never live)
+            if (!rc)
+                rc = cuda_rc(cudaMemsetAsync(align4k(b + kOffXRegion), 0, qw::kXRegionBytes, stream), "cudaMemsetAsync");
+            if (!rc) rc = cuda_rc(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
             if (rc) return rc;
             g_ptr[dev] = p;
             g_seq[dev] = 0;
         }
         base = (unsigned char *)g_ptr[dev];
+        gp = &g_plans[dev];
         g_seq[dev] += 1;
         if (g_seq[dev] >= (1u << 23)) g_seq[dev] = 1;
         seq = g_seq[dev];
     }
+    unsigned char *xregion = align4k(base + kOffXRegion);
     if (seq == 1) {
-        // tags restart: clear the tagged words so no stale word carries a live tag
-        rc = cuda_rc(cudaMemsetAsync(base + kOffTagged, 0, kScratchBytes - kOffTagged, stream), "cudaMemsetAsync");
+        // tags restart: clear the exchange pages so no stale word carries a live tag
+        rc = cuda_rc(cudaMemsetAsync(xregion, 0, qw::kXRegionBytes, stream), "cudaMemsetAsync");
         if (rc) return rc;
     }
 
     // per call: the layer pointer table and this position's RoPE row (both copied from
-    // host memory into the array), and zeroed flags, keys and arrival counters
+    // host memory into the array), and zeroed flags, keys and the arrival counter
     std::vector<qw::DevLayer> layers((size_t)cfg->n_layers);
     for (int l = 0; l < cfg->n_layers; ++l) {
         const qw_layer_weights &lw = w->layers[l];
@@ -192,10 +189,7 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     if (!rc)
         rc = cuda_rc(cudaMemcpyAsync(base + kOffRope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice,
                                      stream), "cudaMemcpyAsync");
-    if (!rc) rc = cuda_rc(cudaMemsetAsync(base + kOffFlags, 0, kOffLayers, stream), "cudaMemsetAsync");
-    if (!rc)
-        rc = cuda_rc(cudaMemsetAsync(base + t.merge, 0, qw::merge_block_bytes(cfg->n_layers), stream),
-                     "cudaMemsetAsync");
+    if (!rc) rc = cuda_rc(cudaMemsetAsync(base + kOffFlags, 0, kOffRope - kOffFlags, stream), "cudaMemsetAsync");
     if (rc) return rc;
     // the two host sources are locals of this call: wait until the copies have run
     rc = cuda_rc(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
@@ -218,15 +212,15 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     a.kc = k_cache;
     a.vc = v_cache;
     a.kv_f32 = cfg->kv_format == QW_KV_F32 ? 1 : 0;
-    // the kernel reads row `pos` of a [max_ctx][head_dim/2] table; point that row at the copy
-    a.rope = (const float2 *)((uintptr_t)(base + kOffRope) - (uintptr_t)pos * half * sizeof(float2));
-    a.xa = (unsigned long long *)(base + t.xa);
-    a.xb = (unsigned long long *)(base + t.xb);
-    a.qkvt = (unsigned long long *)(base + t.qkvt);
-    a.actt = (unsigned long long *)(base + t.actt);
-    a.partt = (unsigned long long *)(base + t.partt);
-    a.ot = (unsigned long long *)(base + t.ot);
-    a.merge = (unsigned *)(base + t.merge);
+    a.rope = (const float2 *)(base + kOffRope);  // a one-row table holding this position's row
+    a.rope_row = 0;
+    const bool two = gp->D == 2;
+    a.D = two ? 2 : 1;
+    a.n_grp[0] = two ? gp->n[0] : gp->ncta;
+    a.n_grp[1] = two ? gp->n[1] : 0;
+    a.role = (const uint16_t *)(base + kOffRoles) + (two ? qw::kMaxSmIds : 0);
+    a.xplan = (const qw::XPlan *)(base + kOffPlans) + (two ? 1 : 0);
+    a.xr = (unsigned long long *)xregion;
     a.logits = logits_dev;
     a.hidden = nullptr;
     a.key = (unsigned long long *)(base + kOffStep);
@@ -236,12 +230,12 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     a.trace = nullptr;
     a.pos = pos;
     a.token = token;
-    a.n_split = qw::attn_splits(pos, cfg->kv_format == QW_KV_F32 ? 4 : 2, ncta, cfg->n_kv_heads);
+    a.n_split = qw::attn_splits(pos, cfg->kv_format == QW_KV_F32 ? 4 : 2, a);
     a.debug = 0;
-    a.step = 1;          // counters and keys were zeroed for this call
-    a.target = (unsigned)ncta;
+    a.step = 1;  // keys and the counter were zeroed for this call
+    a.target = (unsigned)gp->ncta;
     a.tag_base = seq * 512u;
-    rc = cuda_rc(qw::launch_decode(a, group, ncta, stream), "decode launch");
+    rc = cuda_rc(qw::launch_decode(a, gp->ncta, stream), "decode launch");
     if (rc || !wait) return rc;
     qw::StepFlags f;
     rc = cuda_rc(cudaMemcpyAsync(&f, base + kOffFlags, sizeof(f), cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync");

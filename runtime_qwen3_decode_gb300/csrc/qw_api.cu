@@ -25,8 +25,8 @@ constexpr size_t kAlign = 256;
 constexpr int kPrefillRowsMax = 2048;
 
 struct Layout {
-    size_t kc, vc, rope, layers, xa, xb, qkvt, actt, partt, ot, logits, hidden, step, merge, flags, trace;
-    size_t tagged_begin, tagged_end;
+    size_t kc, vc, rope, layers, logits, hidden, step, flags, trace;
+    size_t role, xplan1, xplan2, probe, xregion;  // SM roles, exchange plans, probe scratch, exchange pages
     size_t prefill, prefill_bytes;
     size_t sampler, sampler_bytes;  // PCG32 state (16 B) + sampling scratch
     size_t total;
@@ -51,11 +51,11 @@ int validate_config(const qw_config *c) {
     if (c->hidden % 32 || c->intermediate % 32 || (c->n_heads * c->head_dim) % 32) return QW_UNSUPPORTED_QUANTIZATION;
     if (c->head_dim != qw::kHeadDim) return QW_UNSUPPORTED_SHAPE;
     if (c->n_heads % c->n_kv_heads) return QW_UNSUPPORTED_SHAPE;
-    const int g = c->n_heads / c->n_kv_heads;
-    if (g != 1 && g != 2) return QW_UNSUPPORTED_SHAPE;
     const int qd = c->n_heads * c->head_dim;
     for (int k : {c->hidden, qd, c->intermediate})
         if (k % 1024 || k > 3072) return QW_UNSUPPORTED_SHAPE;
+    // the decode kernel is built for the Qwen3-0.6B block dims
+    if (!qw::block_shape_ok(c->hidden, c->n_heads, c->n_kv_heads, c->intermediate)) return QW_UNSUPPORTED_SHAPE;
     if (c->n_layers > qw::kMaxLayers || c->max_ctx > 131072 || c->vocab > (1 << 24)) return QW_UNSUPPORTED_SHAPE;
     return QW_OK;
 }
@@ -71,25 +71,22 @@ int make_layout(const qw_config *c, Layout *L) {
     const size_t esz = c->kv_format == QW_KV_F32 ? 4 : 2;
     if (!mul_ok((size_t)c->n_layers * c->n_kv_heads, (size_t)c->max_ctx * c->head_dim * esz, &kv))
         return QW_INTEGER_OVERFLOW;
-    const int g = c->n_heads / c->n_kv_heads;
     L->kc = take(kv);
     L->vc = take(kv);
     L->rope = take((size_t)c->max_ctx * (c->head_dim / 2) * sizeof(float2));
     L->layers = take((size_t)c->n_layers * sizeof(qw::DevLayer));
-    L->xa = take((size_t)c->hidden * 8);
-    L->tagged_begin = L->xa;
-    L->xb = take((size_t)c->hidden * 8);
-    L->qkvt = take((size_t)(c->n_heads + 2 * c->n_kv_heads) * c->head_dim * 8);
-    L->actt = take((size_t)c->intermediate * 8);
-    L->partt = take((size_t)kMaxCtas * g * qw::kPartStride * 8);
-    L->ot = take((size_t)c->n_heads * c->head_dim * 8);
-    L->tagged_end = off;
     L->logits = take((size_t)c->vocab * 4);
     L->hidden = take((size_t)(c->n_layers + 1) * c->hidden * 4);
-    L->step = take(qw::step_block_bytes(c->n_layers));
-    L->merge = take(qw::merge_block_bytes(c->n_layers));
+    L->step = take(qw::kStepBlockBytes);
     L->flags = take(sizeof(qw::StepFlags));
     L->trace = take(((size_t)qw::kPhasesPerLayer * c->n_layers + 1) * kMaxCtas * qw::kTraceStamps * 8);
+    L->role = take(2 * (size_t)qw::kMaxSmIds * sizeof(uint16_t));  // one table per layout
+    L->xplan1 = take(sizeof(qw::XPlan));
+    L->xplan2 = take(sizeof(qw::XPlan));
+    // the probe scratch and the exchange pages start on a 4 KB boundary of the device address;
+    // the workspace base is only 256-aligned, so each keeps 4 KB of slack
+    L->probe = take(qw::kProbeScratchBytes + 4096);
+    L->xregion = take(qw::kXRegionBytes + 4096);
     const int rows = c->max_ctx < kPrefillRowsMax ? c->max_ctx : kPrefillRowsMax;
     L->prefill_bytes = qw::prefill_workspace_bytes(*c, rows);
     L->prefill = take(L->prefill_bytes);
@@ -106,7 +103,10 @@ std::unordered_set<const void *> g_live;
 
 struct qw_model {
     qw_config cfg;
-    int group = 0, ncta = 0, nsm = 0, device = 0;
+    int ncta = 0, nsm = 0, device = 0;
+    int groups = 1;                       // SM groups of the decode step (2 = one per die)
+    int n_grp[qw::kMaxGroups] = {0, 0};
+    qw::XPlan *xplan_dev[2] = {nullptr, nullptr};  // exchange plans for one group and for two
     cudaStream_t stream = nullptr;
     uint8_t *ws = nullptr;
     Layout lay{};
@@ -123,6 +123,8 @@ struct qw_model {
     uint32_t csteps = 0;    // steps since the arrival counters were last zeroed
     float *logits = nullptr;
     float *hidden = nullptr;
+    const uint16_t *role_dev[2] = {nullptr, nullptr};  // role tables (by %smid) for one group and for two
+    float rt_near = 0.f, rt_far = 0.f;                 // measured same-die / cross-die round trips (ns)
 };
 
 namespace {
@@ -140,8 +142,14 @@ int cuda_status(cudaError_t e) {
 
 bool aligned(const void *p, size_t a) { return p && ((uintptr_t)p % a) == 0; }
 
-int split_for(const qw_model *m, int pos) {
-    return qw::attn_splits(pos, m->cfg.kv_format == QW_KV_F32 ? 4 : 2, m->ncta, m->cfg.n_kv_heads);
+// The decode arguments for the grouping in use (one group when QW_DEBUG_ONE_GROUP is set).
+void set_groups(const qw_model *m, qw::DecodeArgs &a) {
+    const bool two = m->groups == 2 && !(m->debug & QW_DEBUG_ONE_GROUP);
+    a.D = two ? 2 : 1;
+    a.n_grp[0] = two ? m->n_grp[0] : m->ncta;
+    a.n_grp[1] = two ? m->n_grp[1] : 0;
+    a.xplan = m->xplan_dev[two ? 1 : 0];
+    a.role = m->role_dev[two ? 1 : 0];
 }
 
 // One decode step at position len; token >= 0 or -1 (device-resident previous pick).
@@ -149,7 +157,9 @@ int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
     qw::DecodeArgs a = m->args;
     a.pos = m->len;
     a.token = token;
-    a.n_split = split_for(m, m->len);
+    set_groups(m, a);
+    a.rope_row = m->len;
+    a.n_split = qw::attn_splits(m->len, m->cfg.kv_format == QW_KV_F32 ? 4 : 2, a);
     a.debug = m->debug;
     a.tok_out = tok_out_dev;
     a.trace = (m->debug & QW_DEBUG_TRACE) ? (unsigned long long *)(m->ws + m->lay.trace) : nullptr;
@@ -165,7 +175,7 @@ int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
     }
     m->csteps += 1;
     a.target = m->csteps * (uint32_t)m->ncta;
-    rc = cuda_status(qw::launch_decode(a, m->group, m->ncta, m->stream));
+    rc = cuda_status(qw::launch_decode(a, m->ncta, m->stream));
     if (rc) return rc;
     m->len += 1;
     m->has_last = 1;
@@ -180,6 +190,9 @@ int read_flags(qw_model *m, int32_t *tok) {
     rc = cuda_status(cudaStreamSynchronize(m->stream));
     if (rc) return rc;
     if (f.err) {
+        if (f.err == QW_INTERNAL_INVARIANT && f.diag)
+            fprintf(stderr, "qw: a device wait expired (site %u, CTA %u, phase %u)\n", f.diag >> 24,
+                    (f.diag >> 12) & 0xfffu, f.diag & 0xfffu);
         m->failed = (int)f.err;
         return (int)f.err;
     }
@@ -267,30 +280,49 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
         fprintf(stderr, "qw: device compute capability %d.%d; this library is built for sm_103a only\n", major, minor);
         return QW_CUDA_ERROR;
     }
-    const int group = cfg->n_heads / cfg->n_kv_heads;
     int bps = 0;
-    rc = cuda_status(qw::decode_prepare(group, &bps));
+    rc = cuda_status(qw::decode_prepare(&bps));
     if (rc) return rc;
     if (bps < 1) {
         fprintf(stderr, "qw: decode kernel does not fit on an SM\n");
         return QW_CUDA_ERROR;
     }
-    const int ncta = nsm < kMaxCtas ? nsm : kMaxCtas;
-    if ((cfg->hidden + ncta - 1) / ncta > qw::kMaxOwnRows) return QW_UNSUPPORTED_SHAPE;
+    if (nsm > kMaxCtas) return QW_UNSUPPORTED_SHAPE;
     rc = cuda_status(qw::prefill_prepare());
     if (rc) return rc;
 
     qw_model *m = new (std::nothrow) qw_model();
     if (!m) return QW_OUT_OF_MEMORY;
     m->cfg = *cfg;
-    m->group = group;
-    m->ncta = ncta;
     m->nsm = nsm;
     m->device = dev;
     m->stream = (cudaStream_t)cuda_stream;
     m->ws = (uint8_t *)workspace;
     m->lay = L;
     uint8_t *ws = m->ws;
+    auto align4k = [](uint8_t *p) { return (uint8_t *)(((uintptr_t)p + 4095) & ~(uintptr_t)4095); };
+    uint8_t *probe = align4k(ws + L.probe), *xregion = align4k(ws + L.xregion);
+
+    // SM groups: which SMs and exchange pages sit on which die (measured once per device for the
+    // SMs, once per model for the pages); both layouts are kept, the two-group one is the default
+    qw::GroupPlans *gp = new (std::nothrow) qw::GroupPlans();
+    if (!gp) {
+        delete m;
+        return QW_OUT_OF_MEMORY;
+    }
+    if (qw::plan_groups(dev, probe, xregion, cfg->hidden, cfg->n_heads, cfg->n_kv_heads, cfg->intermediate,
+                        m->stream, gp)) {
+        fprintf(stderr, "qw: measuring the SM groups failed\n");
+        delete gp;
+        delete m;
+        return QW_CUDA_ERROR;
+    }
+    m->ncta = gp->ncta;
+    m->groups = gp->D;
+    m->n_grp[0] = gp->n[0];
+    m->n_grp[1] = gp->n[1];
+    m->rt_near = gp->rt_near;
+    m->rt_far = gp->rt_far;
 
     // RoPE table: cos/sin of pos * theta^(-2i/d), i < d/2, in double, rounded to f32.
     const int half = cfg->head_dim / 2;
@@ -302,19 +334,28 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
             rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
         }
     }
+    uint16_t *role_dev = (uint16_t *)(ws + L.role);
     rc = cuda_status(cudaMemcpyAsync(ws + L.rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice,
                                      m->stream));
     if (!rc)
         rc = cuda_status(cudaMemcpyAsync(ws + L.layers, host_layers.data(), host_layers.size() * sizeof(qw::DevLayer),
                                          cudaMemcpyHostToDevice, m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemcpyAsync(role_dev, gp->role1, sizeof(gp->role1), cudaMemcpyHostToDevice, m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemcpyAsync(role_dev + qw::kMaxSmIds, gp->role2, sizeof(gp->role2),
+                                         cudaMemcpyHostToDevice, m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemcpyAsync(ws + L.xplan1, &gp->plan1, sizeof(qw::XPlan), cudaMemcpyHostToDevice, m->stream));
+    if (!rc)
+        rc = cuda_status(cudaMemcpyAsync(ws + L.xplan2, &gp->plan2, sizeof(qw::XPlan), cudaMemcpyHostToDevice, m->stream));
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.flags, 0, sizeof(qw::StepFlags), m->stream));
     if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.sampler, 0, 256, m->stream));
-    if (!rc)
-        rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, L.merge + qw::merge_block_bytes(cfg->n_layers) - L.step,
-                                         m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.step, 0, qw::kStepBlockBytes, m->stream));
     // tagged exchange words start with tag 0, which no step ever uses
-    if (!rc) rc = cuda_status(cudaMemsetAsync(ws + L.tagged_begin, 0, L.tagged_end - L.tagged_begin, m->stream));
+    if (!rc) rc = cuda_status(cudaMemsetAsync(xregion, 0, qw::kXRegionBytes, m->stream));
     if (!rc) rc = cuda_status(cudaStreamSynchronize(m->stream));  // host staging buffers go out of scope
+    delete gp;
     if (rc) {
         delete m;
         return rc;
@@ -338,21 +379,19 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     a.vc = ws + L.vc;
     a.kv_f32 = cfg->kv_format == QW_KV_F32 ? 1 : 0;
     a.rope = (const float2 *)(ws + L.rope);
-    a.xa = (unsigned long long *)(ws + L.xa);
-    a.xb = (unsigned long long *)(ws + L.xb);
-    a.qkvt = (unsigned long long *)(ws + L.qkvt);
-    a.actt = (unsigned long long *)(ws + L.actt);
-    a.partt = (unsigned long long *)(ws + L.partt);
-    a.ot = (unsigned long long *)(ws + L.ot);
-    a.merge = (unsigned *)(ws + L.merge);
+    a.xr = (unsigned long long *)xregion;
     a.logits = (float *)(ws + L.logits);
     a.hidden = (float *)(ws + L.hidden);
     a.key = (unsigned long long *)(ws + L.step);
     a.sync = (unsigned *)(ws + L.step + 16);
     a.flags = (qw::StepFlags *)(ws + L.flags);
+    m->role_dev[0] = role_dev;
+    m->role_dev[1] = role_dev + qw::kMaxSmIds;
+    m->xplan_dev[0] = (qw::XPlan *)(ws + L.xplan1);
+    m->xplan_dev[1] = (qw::XPlan *)(ws + L.xplan2);
     m->flags = a.flags;
     m->step_block = ws + L.step;
-    m->step_bytes = L.merge + qw::merge_block_bytes(cfg->n_layers) - L.step;  // counters and merge counters
+    m->step_bytes = qw::kStepBlockBytes;
     m->logits = a.logits;
     m->hidden = a.hidden;
     if (qw::prefill_init(&m->pf, *cfg, host_layers.data(), ws + L.prefill, L.prefill_bytes,
@@ -511,7 +550,8 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos) {
 
 int qw_set_debug(qw_model *m, int32_t flags) {
     if (!live(m)) return QW_INVALID_HANDLE;
-    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN | QW_DEBUG_TRACE)) return QW_INVALID_ARGUMENT;
+    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN | QW_DEBUG_TRACE | QW_DEBUG_ONE_GROUP))
+        return QW_INVALID_ARGUMENT;
     m->debug = flags;
     return QW_OK;
 }
@@ -531,6 +571,11 @@ int qw_query(const qw_model *m, int32_t what, int64_t *out) {
             *out = ((int64_t)qw::kPhasesPerLayer * m->cfg.n_layers + 1) * m->ncta * qw::kTraceStamps;
             return QW_OK;
         case QW_QUERY_WORKSPACE_BYTES: *out = (int64_t)m->lay.total; return QW_OK;
+        case QW_QUERY_DECODE_GROUPS: *out = m->groups; return QW_OK;
+        case QW_QUERY_GROUP0_CTAS: *out = m->n_grp[0]; return QW_OK;
+        case QW_QUERY_RT_NEAR_NS: *out = (int64_t)(m->rt_near + 0.5f); return QW_OK;
+        case QW_QUERY_RT_FAR_NS: *out = (int64_t)(m->rt_far + 0.5f); return QW_OK;
+        case QW_QUERY_XREGION_OFFSET: *out = (int64_t)((uint8_t *)m->args.xr - m->ws); return QW_OK;
         default: return QW_INVALID_ARGUMENT;
     }
 }

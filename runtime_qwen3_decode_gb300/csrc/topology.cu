@@ -1,0 +1,303 @@
+// topology.cu - which SMs, and which 4 KB pages of device memory, belong to which die.
+//
+// A GB300 is two dies.  A store to a line becomes visible to a polling SM about twice as fast
+// when the writer, the reader and the line's home (every 4 KB page of device memory is homed by
+// one die) are on one die: about 0.5 us for a ping-pong round trip instead of about 0.9 us.  The
+// decode step therefore keeps most of its exchanges inside one die (qw_internal.h, "Two-group
+// layout").  Nothing reports the die of an SM or a page, so both are measured once: a ping-pong
+// between two SMs through one line is fast only when both SMs sit on the die that homes the
+// line.  The results only steer placement; a wrong or failed measurement makes the step slower,
+// never different, and a device on which no two-die structure shows runs as one group.
+//
+// Every kernel here is a cooperative launch with one CTA per SM (the dynamic shared memory
+// keeps a second CTA off every SM), so every SM named by the host has a CTA, and every wait is
+// bounded: on expiry the kernel records an error word and returns.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "qw_internal.h"
+
+namespace qw {
+namespace {
+
+constexpr int kProbeSmem = 150 * 1024;     // > half an SM's shared memory: one CTA per SM
+constexpr unsigned kProbePolls = 1u << 20;  // bound of every wait in these kernels
+
+__device__ __forceinline__ unsigned smid_now() {
+    unsigned s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+__device__ __forceinline__ unsigned ld_rlx(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_rlx(unsigned *p, unsigned v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__global__ void smid_kernel(unsigned *out) {
+    if (threadIdx.x == 0) out[blockIdx.x] = smid_now();
+}
+
+// The CTAs on SMs sa and sb pass `reps` tags back and forth through word 0 and word 16 (another
+// sector of the same line) of each line lines[i] = base + i * stride_words, i < nlines; sa
+// records the mean round trip of each line in ns (the first, cold, round trip excluded).
+__global__ void pingpong_kernel(unsigned *base, long long stride_words, int nlines, unsigned sa, unsigned sb,
+                                int reps, unsigned tag0, float *out, unsigned *err) {
+    if (threadIdx.x != 0) return;
+    const unsigned s = smid_now();
+    const int me = s == sa ? 0 : s == sb ? 1 : -1;
+    if (me < 0) return;
+    for (int li = 0; li < nlines; ++li) {
+        unsigned *f = base + (size_t)li * stride_words;
+        unsigned long long t0 = 0;
+        for (int i = 1; i <= reps; ++i) {
+            const unsigned t = tag0 + (unsigned)(li * (reps + 1) + i);
+            if (me == 0) {
+                if (i == 2) t0 = now_ns();
+                st_rlx(f, t);
+                for (unsigned n = 0; ld_rlx(f + 16) != t;)
+                    if (++n > kProbePolls) {
+                        atomicExch(err, 1u);
+                        return;
+                    }
+            } else {
+                for (unsigned n = 0; ld_rlx(f) != t;)
+                    if (++n > kProbePolls) {
+                        atomicExch(err, 2u);
+                        return;
+                    }
+                st_rlx(f + 16, t);
+            }
+        }
+        if (me == 0) out[li] = (float)(now_ns() - t0) / (float)(reps - 1);
+    }
+}
+
+cudaError_t coop(const void *fn, int nsm, void **args, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchCooperativeKernel(fn, nsm, 32, args, kProbeSmem, stream);
+}
+
+// Round trips between sa and sb through nlines lines; false on a CUDA error or an expired wait.
+bool measure(unsigned *base, long long stride_words, int nlines, unsigned sa, unsigned sb, int reps, int nsm,
+             float *d_out, unsigned *d_err, std::vector<float> &rt, cudaStream_t stream) {
+    static unsigned tag = 0x1000;
+    unsigned t0 = tag;
+    tag += (unsigned)(nlines * (reps + 1) + 16);
+    if (tag > 0x7fff0000u) tag = 0x1000;
+    int nl = nlines, r = reps;
+    void *args[] = {&base, &stride_words, &nl, &sa, &sb, &r, &t0, &d_out, &d_err};
+    if (coop((const void *)pingpong_kernel, nsm, args, stream) != cudaSuccess) return false;
+    rt.resize((size_t)nlines);
+    unsigned err = 0;
+    if (cudaMemcpyAsync(rt.data(), d_out, (size_t)nlines * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyAsync(&err, d_err, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return false;
+    return err == 0;
+}
+
+std::mutex g_topo_mu;
+bool g_topo_done[64];
+Topology g_topo[64];
+
+void one_group(Topology *t, const std::vector<unsigned> &smids) {
+    t->D = 1;
+    t->n[0] = (int)smids.size();
+    t->n[1] = 0;
+    for (int i = 0; i < kMaxSmIds; ++i) t->role[i] = kNoRole;
+    std::vector<unsigned> s = smids;
+    std::sort(s.begin(), s.end());
+    for (size_t i = 0; i < s.size(); ++i) t->role[s[i]] = (uint16_t)i;
+}
+
+}  // namespace
+
+int probe_topology(int device, uint8_t *scratch, cudaStream_t stream, Topology *out) {
+    std::lock_guard<std::mutex> lk(g_topo_mu);
+    if (device >= 0 && device < 64 && g_topo_done[device]) {
+        *out = g_topo[device];
+        return 0;
+    }
+    int nsm = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || nsm < 1 ||
+        nsm > kMaxSmIds)
+        return 1;
+    // scratch: [0, 32 KB) eight candidate lines 4 KB apart, then the output, error and smid words
+    unsigned *lines = reinterpret_cast<unsigned *>(scratch);
+    float *d_out = reinterpret_cast<float *>(scratch + 32768);
+    unsigned *d_err = reinterpret_cast<unsigned *>(scratch + 49152);
+    unsigned *d_smid = reinterpret_cast<unsigned *>(scratch + 49152 + 256);
+    if (nsm > (65536 - 49152 - 256) / 4) return 1;
+    if (cudaMemsetAsync(scratch, 0, 65536, stream) != cudaSuccess) return 1;
+    void *a1[] = {&d_smid};
+    if (coop((const void *)smid_kernel, nsm, a1, stream) != cudaSuccess) return 1;
+    std::vector<unsigned> smids((size_t)nsm);
+    if (cudaMemcpyAsync(smids.data(), d_smid, (size_t)nsm * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return 1;
+    {
+        std::vector<unsigned> s = smids;
+        std::sort(s.begin(), s.end());
+        if (std::adjacent_find(s.begin(), s.end()) != s.end() || s.back() >= (unsigned)kMaxSmIds) return 1;
+    }
+    Topology t;
+    one_group(&t, smids);
+    t.rt_near = t.rt_far = 0.f;
+    const unsigned ref = smids[0];
+    // A line homed on the die of `ref` shows the split (fast partners share its die); a line
+    // homed on the other die shows none, so try lines 4 KB apart until one does.
+    for (int cand = 0; cand < 8 && t.D == 1; ++cand) {
+        std::vector<float> rt((size_t)nsm, 0.f), one;
+        bool ok = true;
+        for (int k = 1; k < nsm && ok; ++k) {
+            ok = measure(lines + cand * 1024, 0, 1, ref, smids[(size_t)k], 12, nsm, d_out, d_err, one, stream);
+            if (ok) rt[(size_t)k] = one[0];
+        }
+        if (!ok) {
+            cudaMemsetAsync(d_err, 0, 4, stream);
+            continue;
+        }
+        std::vector<float> s(rt.begin() + 1, rt.end());
+        std::sort(s.begin(), s.end());
+        size_t cut = 0;
+        float gap = 0.f;
+        for (size_t i = 0; i + 1 < s.size(); ++i)
+            if (s[i + 1] - s[i] > gap) {
+                gap = s[i + 1] - s[i];
+                cut = i + 1;  // s[0, cut) fast
+            }
+        const int nfast = (int)cut + 1;  // + ref itself
+        if (gap < 0.25f * s[s.size() / 2] || nfast < nsm / 4 || nsm - nfast < nsm / 4) continue;
+        const float thr = 0.5f * (s[cut - 1] + s[cut]);
+        std::vector<unsigned> g0, g1;
+        double near = 0, far = 0;
+        for (int k = 0; k < nsm; ++k) {
+            if (k == 0 || rt[(size_t)k] < thr) {
+                g0.push_back(smids[(size_t)k]);
+                if (k) near += rt[(size_t)k];
+            } else {
+                g1.push_back(smids[(size_t)k]);
+                far += rt[(size_t)k];
+            }
+        }
+        std::sort(g0.begin(), g0.end());
+        std::sort(g1.begin(), g1.end());
+        t.D = 2;
+        t.n[0] = (int)g0.size();
+        t.n[1] = (int)g1.size();
+        for (int i = 0; i < kMaxSmIds; ++i) t.role[i] = kNoRole;
+        for (size_t i = 0; i < g0.size(); ++i) t.role[g0[i]] = (uint16_t)i;
+        for (size_t i = 0; i < g1.size(); ++i) t.role[g1[i]] = (uint16_t)((1u << 12) | i);
+        t.rt_near = (float)(near / (g0.size() - 1));
+        t.rt_far = (float)(far / g1.size());
+    }
+    if (device >= 0 && device < 64) {
+        g_topo[device] = t;
+        g_topo_done[device] = true;
+    }
+    *out = t;
+    return 0;
+}
+
+int probe_pages(const Topology &t, uint8_t *region, int npages, int8_t *page_group, uint8_t *scratch,
+                cudaStream_t stream) {
+    for (int i = 0; i < npages; ++i) page_group[i] = 0;
+    if (t.D == 1) return 0;
+    if (npages > 4096) return 1;
+    std::lock_guard<std::mutex> lk(g_topo_mu);
+    const int nsm = t.n[0] + t.n[1];
+    unsigned sa = kMaxSmIds, sb = kMaxSmIds;
+    for (unsigned s = 0; s < (unsigned)kMaxSmIds; ++s)
+        if (t.role[s] != kNoRole && (t.role[s] >> 12) == 0) {
+            if (sa == (unsigned)kMaxSmIds) sa = s;
+            else if (sb == (unsigned)kMaxSmIds) sb = s;
+        }
+    if (sb == (unsigned)kMaxSmIds) return 1;
+    // the line at byte 1024 of each page carries the ping-pong; results go to the scratch
+    float *d_out = reinterpret_cast<float *>(scratch);
+    unsigned *d_err = reinterpret_cast<unsigned *>(scratch + 16384 + 256);
+    std::vector<float> rt;
+    if (cudaMemsetAsync(region, 0, (size_t)npages * 4096, stream) != cudaSuccess ||
+        cudaMemsetAsync(d_err, 0, 4, stream) != cudaSuccess ||
+        !measure(reinterpret_cast<unsigned *>(region + 1024), 1024, npages, sa, sb, 12, nsm, d_out, d_err, rt, stream))
+        return 1;
+    const float thr = 0.5f * (t.rt_near + t.rt_far);
+    for (int i = 0; i < npages; ++i) page_group[i] = rt[(size_t)i] < thr ? 0 : 1;
+    return 0;
+}
+
+bool plan_exchange(const Topology &t, const int8_t *page_group, int npages, const size_t *words, XPlan *plan) {
+    std::memset(plan, 0, sizeof(*plan));
+    for (int g = 0; g < t.D; ++g) {
+        std::vector<uint32_t> pages;
+        for (int i = 0; i < npages; ++i)
+            if (t.D == 1 || page_group[i] == g) pages.push_back((uint32_t)i);
+        size_t used = 0;
+        for (int b = 0; b < kXBufs; ++b) {
+            const size_t np = (words[b] + kPageWords - 1) / kPageWords;
+            if (used + np > pages.size() || used + np > (size_t)kMaxXPages) return false;
+            plan->first[g][b] = (uint16_t)used;
+            for (size_t k = 0; k < np; ++k) plan->page[g][used + k] = pages[used + k];
+            used += np;
+        }
+    }
+    return true;
+}
+
+int plan_groups(int device, uint8_t *probe_scratch, uint8_t *xregion, int H, int Hq, int Hkv, int I,
+                cudaStream_t stream, GroupPlans *out) {
+    Topology t;
+    if (probe_topology(device, probe_scratch, stream, &t)) return 1;
+    // one group: every SM, ranked by %smid
+    Topology one;
+    one.D = 1;
+    one.n[0] = 0;
+    one.n[1] = 0;
+    one.rt_near = t.rt_near;
+    one.rt_far = t.rt_far;
+    for (int s = 0; s < kMaxSmIds; ++s) {
+        one.role[s] = t.role[s] == kNoRole ? kNoRole : (uint16_t)one.n[0]++;
+    }
+    const int npages = (int)(kXRegionBytes / 4096);
+    std::vector<int8_t> pg((size_t)npages, 0);
+    size_t words[kXBufs];
+    xbuf_words(H, Hq, Hkv, I, 1, max_attn_splits(Hkv, 1, one.n), words);
+    if (!plan_exchange(one, pg.data(), npages, words, &out->plan1)) return 1;
+    std::memcpy(out->role1, one.role, sizeof(out->role1));
+    out->ncta = one.n[0];
+    out->D = 1;
+    out->n[0] = one.n[0];
+    out->n[1] = 0;
+    out->rt_near = t.rt_near;
+    out->rt_far = t.rt_far;
+    std::memcpy(out->role2, one.role, sizeof(out->role2));
+    out->plan2 = out->plan1;
+    if (t.D == 2 && Hkv % 2 == 0 && t.n[0] >= Hkv / 2 && t.n[1] >= Hkv / 2 &&
+        probe_pages(t, xregion, npages, pg.data(), probe_scratch, stream) == 0) {
+        xbuf_words(H, Hq, Hkv, I, 2, max_attn_splits(Hkv, 2, t.n), words);
+        if (plan_exchange(t, pg.data(), npages, words, &out->plan2)) {
+            std::memcpy(out->role2, t.role, sizeof(out->role2));
+            out->D = 2;
+            out->n[0] = t.n[0];
+            out->n[1] = t.n[1];
+        } else {
+            out->plan2 = out->plan1;
+        }
+    }
+    return 0;
+}
+
+}  // namespace qw

@@ -36,9 +36,15 @@ KV_BF16 = 1
 DEBUG_HIDDEN = 1
 DEBUG_PREFILL_BY_TOKEN = 2
 DEBUG_TRACE = 4
+DEBUG_ONE_GROUP = 8
 QUERY_DECODE_CTAS = 1
 QUERY_TRACE_LEN = 2
 QUERY_WORKSPACE_BYTES = 3
+QUERY_DECODE_GROUPS = 4
+QUERY_GROUP0_CTAS = 5
+QUERY_RT_NEAR_NS = 6
+QUERY_RT_FAR_NS = 7
+QUERY_XREGION_OFFSET = 8
 MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 
 # every symbol include/qw.h declares
@@ -200,8 +206,28 @@ def weight_table(dev_weights: dict, int8: bool):
 
 def decode_step_noalloc(cfg: Config, dev_weights: dict, k_cache, v_cache, pos: int, token: int, logits_out,
                         next_token_out, stream=None, wait: bool = True):
-    """qw_decode_step_noalloc: one step over caller-owned K/V planes; no device allocation."""
+    """qw_decode_step_noalloc: one step over caller-owned K/V planes; no device allocation.
+
+    The library cannot see the sizes of the caller's buffers, so they are checked here:
+    CUDA, contiguous, K/V planes of the cache element type cfg.kv_format names holding
+    n_layers * n_kv_heads * max_ctx * head_dim elements each, f32 logits of at least
+    vocab elements, an int32 slot for the pick.
+    """
     import torch
+    kv_dtype = torch.float32 if cfg.kv_format == KV_F32 else torch.bfloat16
+    plane = cfg.n_layers * cfg.n_kv_heads * cfg.max_ctx * cfg.head_dim
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dtype != kv_dtype:
+            raise ValueError(f"{name} must be {kv_dtype} for this kv_format")
+        if t.numel() < plane:
+            raise ValueError(f"{name} holds {t.numel()} elements, the config needs {plane}")
+    if not (logits_out.is_cuda and logits_out.is_contiguous()) or logits_out.dtype != torch.float32 \
+            or logits_out.numel() < cfg.vocab:
+        raise ValueError("logits_out must be a contiguous CUDA float32 tensor of at least vocab elements")
+    if not next_token_out.is_cuda or next_token_out.dtype != torch.int32 or next_token_out.numel() < 1:
+        raise ValueError("next_token_out must be a CUDA int32 tensor")
     w, layers = weight_table(dev_weights, cfg.weight_format == W_INT8_G32)
     st = stream if stream is not None else torch.cuda.current_stream()
     _check(_lib().qw_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), k_cache.data_ptr(), v_cache.data_ptr(),
