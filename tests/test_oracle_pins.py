@@ -497,6 +497,82 @@ def test_zero_gate_silences_the_mlp():
         np.testing.assert_array_equal(a.step(t, want_hidden=True)[1], b.step(t, want_hidden=True)[1])
 
 
+def test_mlp_gate_takes_the_silu_and_up_scales_it():
+    # "Scalar-Native ..." section 5: a = (gate * sigmoid(gate)) * up.  Build a layer whose
+    # MLP input is the all-ones vector (embedding of ones, unit RMSNorm weights), whose gate
+    # rows give g = -2 and up rows u = 3, and whose down projection copies a[j] to x[j]; the
+    # attention contributes nothing (o_proj = 0).  Then x gains silu(-2) * 3 per element
+    # (scipy's expit, not the oracle), while the swapped roles silu(3) * -2 differ by 8x.
+    wl = small_wl(n_layers=1, hidden=64, intermediate=96)
+    H, I = wl.hidden, wl.intermediate
+    w = _structured(wl)
+    lw = w["layers"][0]
+    w["embed"][:] = bf16(np.ones((wl.vocab, H)))
+    lw["input_norm"][:] = bf16(np.ones(H))
+    lw["post_norm"][:] = bf16(np.ones(H))
+    lw["o"][:] = 0
+    lw["gate"][:] = bf16(np.full((I, H), -2.0 / H))
+    lw["up"][:] = bf16(np.full((I, H), 3.0 / H))
+    D = np.zeros((H, I), np.float32)
+    D[np.arange(H), np.arange(H)] = 1.0
+    lw["down"][:] = bf16(D)
+    m = _model(wl, w)
+    _, hid = m.step(3, want_hidden=True)
+    delta = hid[1].astype(np.float64) - hid[0]
+    h2 = 1.0 / math.sqrt(1.0 + wl.rms_eps)          # RMSNorm of the all-ones vector
+    g, u = -2.0 * h2, 3.0 * h2
+    want = g * scipy.special.expit(g) * u
+    swapped = u * scipy.special.expit(u) * g
+    np.testing.assert_allclose(delta, want, rtol=2e-6)
+    assert abs(want - swapped) > 1.0
+
+
+def _norm_routing_model(wl, q_first_half: bool):
+    """A one-layer model where, at position 1, the query and the two keys are all-ones
+    vectors before QK-Norm; q_norm keeps the first half of each head's dims, k_norm the
+    second (or the other way round); v is -1 at position 0 and +1 at position 1; o_proj
+    averages every head's output into each x element and the MLP is off."""
+    H, d = wl.hidden, wl.head_dim
+    w = _structured(wl)
+    lw = w["layers"][0]
+    E = np.ones((wl.vocab, H), np.float32)
+    E[0, H // 2:] = -1.0                      # token 0: v = -1 ; token 1: v = +1
+    w["embed"][:] = bf16(E)
+    lw["input_norm"][:] = bf16(np.ones(H))
+    first = np.zeros((1, H), np.float32)
+    first[0, :H // 2] = 2.0 / H
+    second = np.zeros((1, H), np.float32)
+    second[0, H // 2:] = 2.0 / H
+    lw["q"][:] = bf16(np.repeat(first, wl.n_heads * d, axis=0))
+    lw["k"][:] = bf16(np.repeat(first, wl.n_kv_heads * d, axis=0))
+    lw["v"][:] = bf16(np.repeat(second, wl.n_kv_heads * d, axis=0))
+    half = np.r_[np.ones(d // 2), np.zeros(d // 2)].astype(np.float32)
+    qn, kn = (half, half[::-1].copy()) if q_first_half else (half[::-1].copy(), half)
+    lw["q_norm"][:] = bf16(qn)
+    lw["k_norm"][:] = bf16(kn)
+    lw["o"][:] = bf16(np.full((H, wl.n_heads * d), 1.0 / (wl.n_heads * d)))
+    lw["down"][:] = 0
+    return _model(wl, w)
+
+
+def test_query_and_key_norms_route_and_keys_are_rotated():
+    # QK-Norm then RoPE ("Scalar-Native ..." section 2 steps 3-4).  With q_norm on the first
+    # half of the dims and k_norm on the second, each RoPE pair (i, i + d/2) holds q = (1, 0)
+    # rotated by theta_i and k_0 = (0, 1) unrotated, k_1 = (0, 1) rotated by theta_i, so
+    # s_0 = sum_i sin(theta_i) / sqrt(d) > 0 and s_1 = 0: the query prefers position 0 and the
+    # layer adds p_1 - p_0 < 0.  Swapping which norm goes to queries and which to keys flips
+    # the sign of s_0 (the layer adds a positive amount), and leaving the keys unrotated makes
+    # s_1 = s_0 (the layer adds exactly 0).
+    wl = small_wl(n_layers=1, hidden=64, n_heads=4, n_kv_heads=2, head_dim=16)
+    for q_first, sign in ((True, -1.0), (False, 1.0)):
+        m = _norm_routing_model(wl, q_first)
+        m.step(0)                               # position 0: token 0 (v = -1)
+        _, hid = m.step(1, want_hidden=True)    # position 1: token 1 (v = +1)
+        delta = hid[1].astype(np.float64) - hid[0]
+        assert np.all(np.abs(delta - delta[0]) < 1e-6)
+        assert sign * delta[0] > 0.01, (q_first, delta[0])
+
+
 def test_context_overflow_leaves_length_unchanged():
     wl = small_wl(n_layers=1)
     w = _structured(wl)
