@@ -149,22 +149,25 @@ def prefill_flops(wl, T: int) -> int:
     return gemm + attn + 2 * V * H
 
 
-def kernel_traffic():
-    """Per-launch DRAM bytes from the committed ncu capture, if the kernel source is unchanged."""
+DECODE_SOURCES = ("decode.cu", "decode_g1.cu", "decode_g2.cu", "decode_kernel.cuh", "topology.cu", "qw_internal.h")
+
+
+def kernel_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu capture of this
+    workload, if the kernel's sources are unchanged since."""
     p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    if d.get("source_sha256_16") != decode_source_sha():
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("source_sha256_16") != decode_source_sha():
         return None
     return d.get("dram_bytes_per_launch")
 
 
 def decode_source_sha():
-    """First 16 hex digits of the SHA-256 over the decode kernel's sources (its .cu and the
-    shared constants header), in this order."""
+    """First 16 hex digits of the SHA-256 over the decode kernel's sources, in DECODE_SOURCES order."""
     h = hashlib.sha256()
-    for f in ("decode.cu", "qw_internal.h"):
+    for f in DECODE_SOURCES:
         h.update(open(os.path.join(ROOT, "runtime_qwen3_decode_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -176,26 +179,71 @@ def dist_info():
     return ws, rank, local
 
 
-def oracle_decode_rate(wl, host, n_ctx: int, n_steps: int, warmup: int = 1):
-    """Time the CPU oracle's decode steps after importing an n_ctx-position synthetic cache."""
+def cpu_threads() -> int:
+    """Host cores this process may run on (the oracle's explicit thread count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_plan(n_decode: int, warmup: int, nthreads: int) -> dict:
+    """The CPU oracle on the plan the bench states: the whole tiny workload (8-token prompt,
+    8 greedy steps), then the Qwen3-0.6B-shape decode workload's 128-token prompt token by
+    token and `warmup` + `n_decode` greedy decode steps after it.  Weight generation is not
+    timed.  Runs in a process of its own (see cpu_plan_child) so that no CUDA context, torch
+    thread pool or clock sampler shares the cores with it."""
     import oracle
 
-    ref = oracle.OracleModel(wl, host, max_ctx=n_ctx + warmup + n_steps + 1)
-    k, v = qi.kv_fill(wl, n_ctx)
-    ref.kv_import(k, v, n_ctx)
-    del k, v
-    tok = qi.first_decode_token(wl)
+    out = {"cores": nthreads}
+    tiny = qi.WORKLOADS["tiny"]
+    ref = oracle.OracleModel(tiny, qi.make_weights(tiny), nthreads=nthreads)
+    t = time.perf_counter()
+    oracle.run_sequence(ref, qi.prompt(tiny), tiny.decode_steps)
+    out["tiny_whole_s"] = time.perf_counter() - t
+    ref.close()
+
+    wl = qi.WORKLOADS["qwen3_0p6b_decode"]
+    ref = oracle.OracleModel(wl, qi.make_weights(wl), max_ctx=wl.prompt_len + warmup + n_decode + 1,
+                             nthreads=nthreads)
+    prompt = qi.prompt(wl)
+    t = time.perf_counter()
+    for i, tok in enumerate(prompt):
+        lg, _ = ref.step(int(tok), want_logits=i == len(prompt) - 1)
+    out["prefill_s"] = time.perf_counter() - t
+    out["prefill_tokens"] = len(prompt)
+    tok = oracle.argmax(lg)
     for _ in range(warmup):
         lg, _ = ref.step(tok)
         tok = oracle.argmax(lg)
-    t0 = time.perf_counter()
-    for _ in range(n_steps):
+    t = time.perf_counter()
+    for _ in range(n_decode):
         lg, _ = ref.step(tok)
         tok = oracle.argmax(lg)
-    dt = time.perf_counter() - t0
-    cores = int(ref.cfg.nthreads)
+    out["decode_s"] = time.perf_counter() - t
+    out["decode_steps"] = n_decode
+    out["decode_positions"] = [wl.prompt_len + warmup, wl.prompt_len + warmup + n_decode - 1]
+    out["value"] = n_decode / out["decode_s"]
     ref.close()
-    return n_steps / dt, dt, cores
+    return out
+
+
+def cpu_plan_child(n_decode: int, warmup: int) -> dict:
+    """oracle_plan in a fresh interpreter (no torch, no CUDA): the same program the reference
+    arm runs, so the two CPU numbers come from identical conditions."""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-plan", "--steps", str(n_decode),
+                        "--warmup", str(warmup)], capture_output=True, text=True, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"CPU oracle plan failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def plan_sample(plan: dict) -> str:
+    return (f"oracle on {plan['cores']} host threads: tiny workload whole ({plan['tiny_whole_s']:.2f} s); "
+            f"Qwen3-0.6B shape {plan['prefill_tokens']}-token prompt token by token "
+            f"({plan['prefill_s']:.1f} s, {plan['prefill_tokens'] / plan['prefill_s']:.2f} tok/s) then "
+            f"{plan['decode_steps']} timed greedy decode steps at positions {plan['decode_positions'][0]}.."
+            f"{plan['decode_positions'][1]} ({plan['decode_s']:.1f} s)")
 
 
 # -------------------------------------------------------------------- arms
@@ -204,16 +252,15 @@ def run_reference(args, wl):
     ws, rank, _ = dist_info()
     if rank != 0:
         return 0
-    host = qi.make_weights(wl)
-    steps = args.steps
-    rate, dt, cores = oracle_decode_rate(wl, host, wl.prompt_len, steps, warmup=max(1, min(args.warmup, 2)))
-    sample = (f"{steps} oracle decode steps at positions {wl.prompt_len}.. after importing a "
-              f"{wl.prompt_len}-position synthetic bf16 K/V cache; full Qwen3-0.6B shape")
+    plan = oracle_plan(args.steps, args.warmup, cpu_threads())
+    rate = plan["value"]
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "prompt": wl.prompt_len, "decode_steps": wl.decode_steps},
-            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * plan["decode_s"] / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "qwen3_0p6b_decode", "prompt": 128, "decode_steps": 384},
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": plan["cores"], "kind": "oracle",
+                             "sample": plan_sample(plan), "plan": plan},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -268,27 +315,23 @@ def measure_prefill(qw, wl, reps: int, warmup: int, gpu: int):
             "clocks": clk}
 
 
-def run_ours(args, wl):
+def measure_decode(qw, wl, K: int, W: int, gpu: int, ws: int = 1, with_e2e: bool = True):
+    """Decode of one workload: W warm-up tokens, then exactly K timed tokens (CUDA events on the
+    model's stream, a barrier and a synchronize on both sides).  A new sequence starts (reset +
+    prefill or K/V import, inside the timed region) whenever the workload's decode budget is
+    used up.  Returns the measured numbers and the model's byte accounting."""
     import torch
 
-    ws, rank, local = dist_info()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    from runtime_qwen3_decode_gb300 import build as qbuild
-    from runtime_qwen3_decode_gb300 import qw
-
-    qbuild.build()
     host = qi.make_weights(wl)
     dev = qw.weights_to_device(host, int8=wl.weight_format == "int8_g32")
+    del host
     prompt = qi.prompt(wl)
-    W, K = args.warmup, args.steps
     per_seq = wl.decode_steps
     n0 = wl.kv_prefill + wl.prompt_len  # positions in the cache when decoding starts
     max_ctx = n0 + per_seq + 1
     model = qw.Model(wl, dev, max_ctx=max_ctx)
     stream = torch.cuda.current_stream()
+    kd = vd = None
     if wl.kv_prefill:
         kh, vh = qi.kv_fill(wl, wl.kv_prefill)
         kd = torch.from_numpy(kh.view(np.int16)).cuda()
@@ -310,31 +353,27 @@ def run_ours(args, wl):
             import torch.distributed as dist
             dist.barrier()
 
-    # decode: W warm-up tokens, then exactly K timed tokens; a new sequence starts (reset +
-    # prefill or K/V import, inside the timed region) whenever the decode budget is used up
     toks = torch.zeros(max(K, 1), dtype=torch.int32, device="cuda")
     positions = []
-    next_in = start_sequence()
-    done_in_seq = 0
+    state = {"next_in": start_sequence(), "done": 0}
 
     def run_tokens(n, out=None, record=False):
-        nonlocal done_in_seq, next_in
         i = 0
         while i < n:
-            if done_in_seq == per_seq:
-                next_in = start_sequence()
-                done_in_seq = 0
-            m = min(n - i, per_seq - done_in_seq)
+            if state["done"] == per_seq:
+                state["next_in"] = start_sequence()
+                state["done"] = 0
+            m = min(n - i, per_seq - state["done"])
             if record:
                 positions.extend(range(model.kv_length, model.kv_length + m))
-            model.generate(m, next_in, out[i:i + m] if out is not None else None)
-            next_in = -1
-            done_in_seq += m
+            model.generate(m, state["next_in"], out[i:i + m] if out is not None else None)
+            state["next_in"] = -1
+            state["done"] += m
             i += m
 
     run_tokens(W)
     model.sync()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(gpu)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
@@ -353,63 +392,99 @@ def run_ours(args, wl):
         tt = torch.tensor([ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    value = K * ws / (ms / 1000.0)
 
-    # end to end through the public call: host token in, host token out, every step
-    model.kv_reset()
-    tok = qi.first_decode_token(wl)
-    if wl.kv_prefill:
-        model.kv_import(kd, vd, wl.kv_prefill)
-    if wl.prompt_len:
-        tok = model.prefill(prompt)
-    n_e2e = min(K, per_seq)
-    torch.cuda.synchronize()
-    t_e = time.perf_counter()
-    for _ in range(n_e2e):
-        tok = model.decode_step(tok)
-    e2e_s = time.perf_counter() - t_e
-    e2e_val = n_e2e / e2e_s
-
-    if rank != 0:
-        model.close()
-        return 0
-
+    e2e = None
+    if with_e2e:
+        # end to end through the public call: host token in, host token out, every step
+        model.kv_reset()
+        tok = qi.first_decode_token(wl)
+        if wl.kv_prefill:
+            model.kv_import(kd, vd, wl.kv_prefill)
+        if wl.prompt_len:
+            tok = model.prefill(prompt)
+        n_e2e = min(K, per_seq)
+        torch.cuda.synchronize()
+        t_e = time.perf_counter()
+        for _ in range(n_e2e):
+            tok = model.decode_step(tok)
+        e2e = {"value": n_e2e / (time.perf_counter() - t_e), "unit": UNIT, "h2d_bytes_per_step": 4,
+               "d2h_bytes_per_step": 16,
+               "how": "qw_decode_step(token_from_host, &next_token_host) per token, host-synchronous"}
+    model.close()
+    del kd, vd, dev
+    torch.cuda.empty_cache()
     peak, peak_kind = measured_peaks()
     bytes_timed = sum(token_bytes(wl, p) for p in positions)
     achieved = bytes_timed / (ms / 1000.0) / 1e9
+    return {"ms": ms, "K": K, "W": W, "positions": positions, "value": K * ws / (ms / 1000.0),
+            "bytes_per_token_mean": bytes_timed / max(1, len(positions)), "achieved": achieved, "peak": peak,
+            "peak_kind": peak_kind, "clocks": clk, "e2e": e2e, "n0": n0}
+
+
+def decode_sub(qw, wl, K: int, W: int, gpu: int) -> dict:
+    """A secondary decode workload's figures for the bench line (same method as the headline)."""
+    r = measure_decode(qw, wl, K, W, gpu, with_e2e=False)
+    return {"workload": wl.name, "value": r["value"], "unit": UNIT, "steps": K, "warmup": W,
+            "ms_per_step": r["ms"] / K, "positions_timed": [r["positions"][0], r["positions"][-1]],
+            "weights": wl.weight_format, "kv_cache": wl.kv_format,
+            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                         "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
+                         "bytes_per_token": r["bytes_per_token_mean"],
+                         "bytes_per_token_at_first_pos": token_bytes(wl, r["positions"][0]),
+                         "traffic": kernel_traffic(wl.name)},
+            "clocks": r["clocks"]}
+
+
+def run_ours(args, wl):
+    import torch
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from runtime_qwen3_decode_gb300 import build as qbuild
+    from runtime_qwen3_decode_gb300 import qw
+
+    qbuild.build()
+    W, K = args.warmup, args.steps
+    r = measure_decode(qw, wl, K, W, local, ws)
+    if rank != 0:
+        return 0
+    positions = r["positions"]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
-        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.weight_format == "bf16" else "int8",
         "data": "synthetic (seeded random-init weights, uniform-random prompt)",
-        "config": {"workload": wl.name, "prompt": wl.prompt_len, "decode_steps": per_seq,
+        "config": {"workload": wl.name, "prompt": wl.prompt_len, "decode_steps": wl.decode_steps,
                    "positions_timed": [positions[0], positions[-1]] if positions else None,
                    "compute": "bf16 weights x f32 activations, f32 accumulation",
                    "l2": "no flush: inputs larger than L2 (weights streamed per token)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "frac_of_nominal_7.9TBs": achieved / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                     "frac": r["achieved"] / r["peak"], "peak_kind": r["peak_kind"],
+                     "frac_of_nominal_7.9TBs": r["achieved"] / NOMINAL_HBM_GBS,
+                     "bytes_per_token_mean": r["bytes_per_token_mean"],
                      "bytes_per_token_at_first_pos": token_bytes(wl, positions[0]) if positions else None,
                      "kernel": "qw::decode_kernel (one persistent launch per token)",
-                     "traffic": kernel_traffic()},
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 16,
-                "how": "qw_decode_step(token_from_host, &next_token_host) per token, host-synchronous"},
+                     "traffic": kernel_traffic(wl.name)},
+        "e2e": r["e2e"],
         "gpu_launches": K,
-        "clocks": clk,
+        "clocks": r["clocks"],
     }
-    model.close()
-    if wl.kv_prefill:
-        del kd, vd
+    if not args.no_extra and ws == 1:
+        for key, name, k_sub in (("decode_ctx32k", "qwen3_0p6b_ctx32k", 56), ("decode_int8", "qwen3_0p6b_int8", 248)):
+            sub = qi.WORKLOADS[name]
+            if sub.name != wl.name:
+                line[key] = decode_sub(qw, sub, min(k_sub, sub.decode_steps - W), W, local)
     if not args.no_prefill:
         line["prefill"] = measure_prefill(qw, qi.WORKLOADS[args.prefill_workload], args.prefill_reps,
                                           max(3, min(W, 5)), local)
     if not args.no_cpu_baseline and ws == 1:
-        n = args.cpu_steps
-        rate, dt, cores = oracle_decode_rate(wl, host, n0, n)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{n} oracle decode steps after a {n0}-position synthetic "
-                                          f"K/V import, full shape ({dt:.1f} s of CPU)"}
+        plan = cpu_plan_child(args.cpu_steps, 2)
+        line["cpu_baseline"] = {"value": plan["value"], "unit": UNIT, "cores": plan["cores"], "kind": "oracle",
+                                "sample": plan_sample(plan), "plan": plan}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -422,12 +497,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_0p6b_decode", choices=sorted(qi.WORKLOADS))
-    ap.add_argument("--cpu-steps", type=int, default=64)
+    ap.add_argument("--cpu-steps", type=int, default=32, help="timed oracle decode steps of the CPU baseline")
+    ap.add_argument("--cpu-plan", action="store_true", help=argparse.SUPPRESS)  # the baseline's child process
+    ap.add_argument("--no-extra", action="store_true", help="skip the 32K-context and int8 decode sub-objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-workload", default="qwen3_0p6b_prefill2048", choices=sorted(qi.WORKLOADS))
     ap.add_argument("--prefill-reps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
+    if args.cpu_plan:
+        print(json.dumps(oracle_plan(args.steps, args.warmup, cpu_threads())), flush=True)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     wl = qi.WORKLOADS[args.workload]

@@ -227,8 +227,19 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos);
  * QW_DEBUG_ONE_GROUP: decode steps run with every SM in one group instead of one
  * group per die (the layout used where no two-die structure is measured; o_proj
  * and down then sum all columns in one dot product instead of two halves).
+ * QW_DEBUG_WITHHOLD: the failure path's test.  In each decode step the first SM
+ * of group 0 withholds its q|k|v rows of layer 0, and every device-side wait
+ * gives up after 1 ms instead of 1 s, so the step ends with
+ * QW_INTERNAL_INVARIANT (every CTA returns on its own; nothing faults or hangs).
+ * The model then refuses every call with that status until qw_kv_reset.
  */
-enum { QW_DEBUG_HIDDEN = 1, QW_DEBUG_PREFILL_BY_TOKEN = 2, QW_DEBUG_TRACE = 4, QW_DEBUG_ONE_GROUP = 8 };
+enum {
+    QW_DEBUG_HIDDEN = 1,
+    QW_DEBUG_PREFILL_BY_TOKEN = 2,
+    QW_DEBUG_TRACE = 4,
+    QW_DEBUG_ONE_GROUP = 8,
+    QW_DEBUG_WITHHOLD = 16
+};
 int qw_set_debug(qw_model *m, int32_t flags);
 
 /*

@@ -188,7 +188,7 @@ __device__ __forceinline__ bool poll_more(unsigned i, unsigned long long &t0, St
     const unsigned long long t = gtime();
     if (t0 == 0) {
         t0 = t;
-    } else if (t - t0 > kWaitLimitNs) {
+    } else if (t - t0 > smem().args.wait_ns) {
         const Smem &sm = smem();
         const int ph = threadIdx.x >= kConsumerThreads ? sm.pph : sm.ph;
         atomicCAS(&f->diag, 0u, ((unsigned)site << 24) | ((blockIdx.x & 0xfffu) << 12) | ((unsigned)ph & 0xfffu));
@@ -741,6 +741,8 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
 template <bool PAIR>
 __device__ __forceinline__ void emit_row(const Smem &sm, int buf, int row, const float (&o)[PAIR ? 2 : 1],
                                          unsigned out_tag) {
+    // failure-path test: the first CTA of group 0 withholds its rows of the step's first phase
+    if ((sm.args.debug & kDebugWithhold) && sm.ph == 0 && sm.g == 0 && sm.r == 0) return;
     float v = o[0];
     if constexpr (PAIR) v = (o[0] / (1.0f + __expf(-o[0]))) * o[1];  // silu(gate) * up
     st_tag(xw(sm, sm.g, buf, row), v, out_tag);

@@ -232,6 +232,7 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     a.token = token;
     a.n_split = qw::attn_splits(pos, cfg->kv_format == QW_KV_F32 ? 4 : 2, a);
     a.debug = 0;
+    a.wait_ns = qw::kWaitLimitNs;
     a.step = 1;  // keys and the counter were zeroed for this call
     a.target = (unsigned)gp->ncta;
     a.tag_base = seq * 512u;

@@ -18,6 +18,8 @@
 #include "qw_prefill.h"
 #include "qw_sample.h"
 
+static_assert(qw::kDebugWithhold == QW_DEBUG_WITHHOLD, "debug flag value shared with the kernel");
+
 namespace {
 
 constexpr int kMaxCtas = 1024;  // upper bound on SMs, for the split-attention partials
@@ -161,10 +163,15 @@ int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
     a.rope_row = m->len;
     a.n_split = qw::attn_splits(m->len, m->cfg.kv_format == QW_KV_F32 ? 4 : 2, a);
     a.debug = m->debug;
+    a.wait_ns = (m->debug & QW_DEBUG_WITHHOLD) ? qw::kDebugWaitLimitNs : qw::kWaitLimitNs;
     a.tok_out = tok_out_dev;
     a.trace = (m->debug & QW_DEBUG_TRACE) ? (unsigned long long *)(m->ws + m->lay.trace) : nullptr;
     m->step_seq += 1;
-    if (m->step_seq >= (1u << 23)) m->step_seq = 1;  // tag_base stays below 2^32
+    if (m->step_seq >= (1u << 23)) {  // tag_base stays below 2^32: restart the tags on a clean region
+        m->step_seq = 1;
+        const int zr = cuda_status(cudaMemsetAsync(m->args.xr, 0, qw::kXRegionBytes, m->stream));
+        if (zr) return zr;
+    }
     a.step = m->step_seq;
     a.tag_base = m->step_seq * 512u;
     int rc = QW_OK;
@@ -550,7 +557,8 @@ int qw_kv_export(qw_model *m, void *k_dev, void *v_dev, int32_t n_pos) {
 
 int qw_set_debug(qw_model *m, int32_t flags) {
     if (!live(m)) return QW_INVALID_HANDLE;
-    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN | QW_DEBUG_TRACE | QW_DEBUG_ONE_GROUP))
+    if (flags & ~(QW_DEBUG_HIDDEN | QW_DEBUG_PREFILL_BY_TOKEN | QW_DEBUG_TRACE | QW_DEBUG_ONE_GROUP |
+                  QW_DEBUG_WITHHOLD))
         return QW_INVALID_ARGUMENT;
     m->debug = flags;
     return QW_OK;

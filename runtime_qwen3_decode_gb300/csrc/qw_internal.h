@@ -85,6 +85,8 @@ constexpr uint16_t kNoRole = 0xffff;
 constexpr int kTraceStamps = 8;
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // every device-side wait gives up after 1 s
+constexpr unsigned long long kDebugWaitLimitNs = 1000000ull; // ... or after 1 ms under the withholding debug flag
+constexpr int kDebugWithhold = 16;                            // QW_DEBUG_WITHHOLD
 
 // Status values written by device code (same numbers as qw.h).
 constexpr unsigned kErrInvalidArgument = 1;
@@ -138,6 +140,7 @@ struct DecodeArgs {
     unsigned long long *trace;       // debug timeline [phase][cta][kTraceStamps] (%globaltimer ns) or null
     // step
     int pos, token, n_split, debug;
+    unsigned long long wait_ns;      // limit of every device-side wait of the step
     unsigned step;                   // step sequence number (never 0 after creation)
     unsigned tag_base;               // step * 512: tags of this step are tag_base + 8 layer + kind + 1
 };

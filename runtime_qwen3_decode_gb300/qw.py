@@ -37,6 +37,7 @@ DEBUG_HIDDEN = 1
 DEBUG_PREFILL_BY_TOKEN = 2
 DEBUG_TRACE = 4
 DEBUG_ONE_GROUP = 8
+DEBUG_WITHHOLD = 16
 QUERY_DECODE_CTAS = 1
 QUERY_TRACE_LEN = 2
 QUERY_WORKSPACE_BYTES = 3

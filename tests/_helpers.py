@@ -10,7 +10,8 @@ import numpy as np
 HIDDEN_REL_L2 = 2e-3
 LOGITS_MAX_ABS = 5e-2
 MARGIN = 0.1
-# A bf16 K/V cache on both sides (not one of the workloads' prefill configurations): each
+# DIAGNOSTIC bar, used by one labelled diagnostic test only (never a workload's parity):
+# a bf16 K/V cache on both sides (not one of the workloads' prefill configurations): each
 # side rounds its own K/V rows to bf16, and an element whose two unrounded values straddle
 # a rounding boundary ends one bf16 ulp (2^-8 relative) apart.  With only one side rounding
 # the cache, the per-layer hidden error was measured at 2.6e-3 to 4.3e-3 on the tiny

@@ -170,8 +170,13 @@ def test_prefill_after_decode_steps(qw):
     m.close()
 
 
-def test_tiny_prefill_bf16_cache(qw):
-    # a bf16 cache rounds every appended row; the oracle rounds its rows the same way
+def test_diagnostic_bf16_cache_prefill(qw):
+    # DIAGNOSTIC, not a parity case of any workload (none prefills into a bf16 cache): it only
+    # shows that the prefill's bf16 cache stores work.  The oracle is switched to round its
+    # own K/V rows to bf16 like the cache does, and the hidden-state bar is the doubled
+    # diagnostic one (HIDDEN_REL_L2_BF16_KV in _helpers): both sides round rows whose
+    # unrounded values differ, so an element can end one bf16 ulp apart.  Logits and greedy
+    # picks keep the standard bar.
     run_prefill(qw, qi.WORKLOADS["tiny"].with_(kv_format="bf16"), [200], kv_bf16_oracle=True, check_kv=False)
 
 

@@ -3,8 +3,9 @@
 Both sides take the same seeded synthetic logits, history and PCG32 state.  The PCG32
 state after every draw must match bit for bit, and so must the picked token.  The one
 allowed exception is a draw u that falls within 1e-5 of a cumulative-probability
-boundary of the oracle's retained candidates: the two sides compute exp in different
-libraries (a few ulp apart), so there either neighbour of the boundary is a correct pick.
+boundary of the oracle's retained candidates, or a top-p cut whose cumulative probability
+lies within 1e-5 of top_p: the two sides compute exp in different libraries (a few ulp
+apart), so there either neighbour of the boundary, or either cut, gives a correct pick.
 """
 import numpy as np
 import pytest
@@ -35,10 +36,30 @@ def rng_host(t) -> np.ndarray:
     return t.cpu().numpy().view(np.uint64)
 
 
-def check_pick(gpu_tok, ora, what):
+def top_p_alternatives(x, state_before, T, k, p, pen, hist, u):
+    """Picks the oracle would make had its top-p cut kept one candidate more or fewer, for
+    cuts whose cumulative probability lies within BOUNDARY of top_p (the two sides sum exp
+    values from different libraries, so such a cut may fall on either side)."""
+    if p >= 1.0:
+        return set()
+    st = state_before.copy()
+    _, ids, cum, _ = oracle.sample(x, st, T, top_k=k, top_p=1.0, penalty=pen, history=hist)
+    out = set()
+    for n in range(1, len(ids) + 1):
+        if abs(float(cum[n - 1]) - p) > BOUNDARY and not (n >= 2 and abs(float(cum[n - 2]) - p) <= BOUNDARY):
+            continue
+        z = float(cum[n - 1])
+        j = next((i for i in range(n) if float(cum[i]) / z > u), n - 1)
+        out.add(int(ids[j]))
+    return out
+
+
+def check_pick(gpu_tok, ora, what, alternatives=()):
     tok, ids, cum, u = ora
     if gpu_tok == tok:
         return 0
+    if gpu_tok in alternatives:
+        return 1
     near = [j for j in range(len(cum)) if abs(float(cum[j]) - u) <= BOUNDARY]
     assert near, f"{what}: GPU picked {gpu_tok}, oracle {tok} (u={u:.7f} not at a boundary)"
     j = near[0]
@@ -67,12 +88,15 @@ def test_sample_logits_matches_oracle(qw, V, params):
     for step in range(25):
         x = (g.standard_normal(V) * 2.0).astype(np.float32)
         hist = g.integers(0, V, size=int(g.integers(0, 40))).astype(np.int32)
+        before = state.copy()
         ora = oracle.sample(x, state, T, top_k=k, top_p=p, penalty=pen, history=hist)
         qw.sample_logits(torch.from_numpy(x).cuda(), sp, rng, tok,
                          history=torch.from_numpy(hist).cuda() if hist.size else None, scratch=scratch)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(rng_host(rng), state)  # one word per sampled step, none for greedy
-        boundary += check_pick(int(tok.item()), ora, f"V={V} {params} step {step}")
+        got = int(tok.item())
+        alt = top_p_alternatives(x, before, T, k, p, pen, hist, ora[3]) if got != ora[0] else set()
+        boundary += check_pick(got, ora, f"V={V} {params} step {step}", alt)
     assert boundary <= 2
 
 
