@@ -14,8 +14,9 @@
 //   DOWN    partial down over the group's columns: Wd[:, group] a[group]
 //   LMHEAD  x += both groups' down partials; logits = E RMSNorm(x); packed-key argmax
 //
-// Layout on the GPU: one CTA per SM (cooperative launch, so all CTAs are resident), 15
-// consumer warps and 1 producer warp; the kernel is built for the Qwen3-0.6B block dims
+// Layout on the GPU: one CTA per SM (cooperative launch, so all CTAs are resident), 7
+// consumer warps and 1 producer warp (two warps per SM sub-partition, so each thread may
+// hold 255 registers); the kernel is built for the Qwen3-0.6B block dims
 // (kBlockH ... in qw_internal.h), one instantiation per (group count, weight format, cache
 // element type).  The SMs form D groups (one per die of the GB300, or a
 // single group): group g owns the KV heads [g Hkv/D, (g+1) Hkv/D) with their query heads, the
@@ -23,7 +24,9 @@
 // matching column halves.  So per layer only two exchanges cross groups (the partial sums of
 // o_proj and of down, which every CTA adds into its own full copy of the residual stream, in
 // the same order everywhere); q|k|v, the attention partials, the attention output and the
-// SwiGLU output stay inside the group, in pages of device memory its die homes.
+// SwiGLU output stay inside the group, in pages of device memory its die homes.  The two
+// partial sums are written twice, once into pages each die homes, so every reader polls
+// words on its own die.
 //
 // The producer streams, with bulk async copies (cp.async.bulk + mbarrier transaction counts),
 // every weight row (segment) and cached K/V row its CTA will consume during the whole step into
@@ -482,7 +485,6 @@ template <int NB, int NI>
 __device__ __forceinline__ bool poll_vec_n(const int (&gg)[NB], int b, int n4, unsigned tag, float4 (&v)[NB][NI],
                                            StepFlags *f) {
     const Smem &sm = smem();
-    unsigned long long w[NB][NI][4];
     unsigned long long t0 = 0;
     for (unsigned i = 0;; ++i) {
         bool ok = true;
@@ -493,21 +495,17 @@ __device__ __forceinline__ bool poll_vec_n(const int (&gg)[NB], int b, int n4, u
 #pragma unroll
                 for (int q = 0; q < NB; ++q) {
                     const unsigned long long *p = xw(sm, gg[q], b, 4 * idx);
-                    ld_tag2(p, w[q][k][0], w[q][k][1]);
-                    ld_tag2(p + 2, w[q][k][2], w[q][k][3]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) ok &= tag_is(w[q][k][e], tag);
+                    unsigned long long w0, w1, w2, w3;
+                    ld_tag2(p, w0, w1);
+                    ld_tag2(p + 2, w2, w3);
+                    ok &= tag_is(w0, tag) & tag_is(w1, tag) & tag_is(w2, tag) & tag_is(w3, tag);
+                    v[q][k] = make_float4(tag_val(w0), tag_val(w1), tag_val(w2), tag_val(w3));
                 }
             }
         }
         if (ok) break;
         if (!poll_more(i, t0, f, WS_VEC)) return false;
     }
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int k = 0; k < NI; ++k)
-            v[q][k] = make_float4(tag_val(w[q][k][0]), tag_val(w[q][k][1]), tag_val(w[q][k][2]), tag_val(w[q][k][3]));
     return true;
 }
 
@@ -515,13 +513,13 @@ __device__ __forceinline__ bool poll_vec_n(const int (&gg)[NB], int b, int n4, u
 template <int K>
 __host__ __device__ constexpr int vec_iters() { return (K / 4 + kConsumerThreads - 1) / kConsumerThreads; }
 
-// Poll the float4 slots tid + NT i (< K/4) of NB tagged buffers (buffer kind b of groups gg[k]).
+// Poll the float4 slots tid + NT i (< K/4) of NB tagged buffers (buffer kind bb[k] of groups gg[k]).
+// Each word's value is taken as it is loaded, so only floats stay live across the retries.
 template <int NB, int K>
-__device__ __forceinline__ bool poll_vec(const int (&gg)[NB], int b, unsigned tag, float4 (&v)[NB][vec_iters<K>()],
-                                         StepFlags *f) {
+__device__ __forceinline__ bool poll_vec(const int (&gg)[NB], const int (&bb)[NB], unsigned tag,
+                                         float4 (&v)[NB][vec_iters<K>()], StepFlags *f) {
     constexpr int NI = vec_iters<K>();
     const Smem &sm = smem();
-    unsigned long long w[NB][NI][4];
     unsigned long long t0 = 0;
     for (unsigned i = 0;; ++i) {
         bool ok = true;
@@ -531,43 +529,18 @@ __device__ __forceinline__ bool poll_vec(const int (&gg)[NB], int b, unsigned ta
             if (idx < K / 4) {
 #pragma unroll
                 for (int q = 0; q < NB; ++q) {
-                    const unsigned long long *p = xw(sm, gg[q], b, 4 * idx);
-                    ld_tag2(p, w[q][k][0], w[q][k][1]);
-                    ld_tag2(p + 2, w[q][k][2], w[q][k][3]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) ok &= tag_is(w[q][k][e], tag);
+                    const unsigned long long *p = xw(sm, gg[q], bb[q], 4 * idx);
+                    unsigned long long w0, w1, w2, w3;
+                    ld_tag2(p, w0, w1);
+                    ld_tag2(p + 2, w2, w3);
+                    ok &= tag_is(w0, tag) & tag_is(w1, tag) & tag_is(w2, tag) & tag_is(w3, tag);
+                    v[q][k] = make_float4(tag_val(w0), tag_val(w1), tag_val(w2), tag_val(w3));
                 }
             }
         }
         if (ok) break;
-        if (!poll_more(i, t0, f, WS_VEC)) {
-            // debug timeline: record the first word this thread still misses (group, word, tag seen)
-            const DecodeArgs &a = sm.args;
-            if (a.trace) {
-                unsigned long long *tr = a.trace + ((size_t)sm.ph * gridDim.x + blockIdx.x) * kTraceStamps;
-                for (int k = 0; k < NI; ++k) {
-                    const int idx = ctid() + kConsumerThreads * k;
-                    if (idx >= K / 4) continue;
-                    for (int q = 0; q < NB; ++q)
-                        for (int e = 0; e < 4; ++e)
-                            if (!tag_is(w[q][k][e], tag)) {
-                                atomicCAS(tr + 6, 0ull,
-                                          ((unsigned long long)(((unsigned)gg[q] << 28) | ((unsigned)b << 24) |
-                                                                (unsigned)(4 * idx + e))
-                                           << 32) |
-                                              (unsigned)(w[q][k][e] >> 32));
-                                atomicCAS(tr + 7, 0ull, (unsigned long long)tag);
-                            }
-                }
-            }
-            return false;
-        }
+        if (!poll_more(i, t0, f, WS_VEC)) return false;
     }
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-#pragma unroll
-        for (int k = 0; k < NI; ++k)
-            v[q][k] = make_float4(tag_val(w[q][k][0]), tag_val(w[q][k][1]), tag_val(w[q][k][2]), tag_val(w[q][k][3]));
     return true;
 }
 
@@ -685,10 +658,14 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
         if (!(kind == T_QKV && l == 0)) {  // at layer 0 x is the embedding, already staged
             const int b = kind == T_GATEUP ? XB_PO : XB_PD;
             const unsigned tg = kind == T_GATEUP ? xtag(a, l, TK_PO) : xtag(a, l - 1, TK_PD);
-            int gg[D];
+            // every group's partial sums, each from the copy in pages this CTA's die homes
+            int gg[D], bb[D];
 #pragma unroll
-            for (int q = 0; q < D; ++q) gg[q] = q;
-            ok = poll_vec<D, kBlockH>(gg, b, tg, pv, a.flags);
+            for (int q = 0; q < D; ++q) {
+                gg[q] = q;
+                bb[q] = q == sm.g ? b : b + kXFar;
+            }
+            ok = poll_vec<D, kBlockH>(gg, bb, tg, pv, a.flags);
         }
         if (tr && tid == 0) tr[1] = gtime();
         float ss = 0.f;
@@ -746,10 +723,13 @@ __device__ __forceinline__ void emit_row(const Smem &sm, int buf, int row, const
     float v = o[0];
     if constexpr (PAIR) v = (o[0] / (1.0f + __expf(-o[0]))) * o[1];  // silu(gate) * up
     st_tag(xw(sm, sm.g, buf, row), v, out_tag);
+    // two groups: the partial sums also go to the other die's copy, so every reader polls
+    // words its own die homes
+    if (sm.args.D == 2 && (buf == XB_PO || buf == XB_PD)) st_tag(xw(sm, sm.g, buf + kXFar, row), v, out_tag);
 }
 
 // A layer phase over rows [p.r0, p.r1) with K = 256 NP columns (K <= 1536), all chunks already
-// taken: warp w owns rows w, w + 15, ... (gate/up: pairs).  The weight pieces of its first PR
+// taken: warp w owns rows w, w + 7, ... (gate/up: pairs).  The weight pieces of its first PR
 // rows are loaded into registers before the phase input is waited for (they do not depend on
 // it); after the input is staged only the activation read, the paired FMAs and one warp
 // reduction per row remain.
@@ -994,14 +974,14 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (!all_ok(!dead)) return kFailed;
     const unsigned out_tag =
         xtag(a, l, kind == T_QKV ? TK_QKV : kind == T_OPROJ ? TK_PO : kind == T_GATEUP ? TK_ACT : TK_PD);
-    bool ok;
+    bool ok = false;
     if (kind == T_GATEUP) {
         ok = gemv_rows_pre<4, I8, true, D>(p, kind, it, out_tag, tr);
     } else if (kind == T_QKV || (kind == T_OPROJ && KO == kBlockH)) {
         ok = gemv_rows_pre<4, I8, false, D>(p, kind, it, out_tag, tr);
     } else if (kind == T_DOWN && KD == 1536) {
         ok = gemv_rows_pre<6, I8, false, D>(p, kind, it, out_tag, tr);
-    } else {  // one group: o_proj and down rows of 2048 / 3072 columns, split over the warps
+    } else if constexpr (D == 1) {  // one group: o_proj and down rows of 2048 / 3072 columns, split over the warps
         float scale;
         ok = stage_input<D, vec_iters<KMAX>()>(kind, l, p.K, a, tr, &scale, [] {});
         if (ok) {

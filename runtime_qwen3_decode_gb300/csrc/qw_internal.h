@@ -60,16 +60,19 @@ enum {
     XB_ACT = 3,   // SwiGLU output of the group's rows            [I/D]
     XB_PO = 4,    // o_proj partial sum over the group's columns  [H]  (read by every group)
     XB_PD = 5,    // down partial sum over the group's columns    [H]  (read by every group)
-    kXBufs = 6
+    XB_POX = 6,   // copy of XB_PO in pages the other group's die homes (two groups only)
+    XB_PDX = 7,   // copy of XB_PD in pages the other group's die homes (two groups only)
+    kXBufs = 8
 };
+constexpr int kXFar = XB_POX - XB_PO;  // a partial-sum buffer's far copy: b + kXFar
 
 // Where each group's exchange buffers live: word i of buffer b of group g is at
 // region + page[g][first[g][b] + i / kPageWords] * 4096 + (i % kPageWords) * 8.
 struct XPlan {
     uint32_t page[kMaxGroups][kMaxXPages];  // page offsets (4 KB units) from the region base
     uint16_t first[kMaxGroups][kXBufs];
-    uint16_t pad[4];
 };
+static_assert(sizeof(XPlan) % 16 == 0, "XPlan is copied in 16-byte units");
 
 // Host view of the SM groups of one device.
 struct Topology {
@@ -179,6 +182,8 @@ inline void xbuf_words(int H, int Hq, int Hkv, int I, int D, int smax, size_t *w
     words[XB_ACT] = (size_t)I / D;
     words[XB_PO] = (size_t)H;
     words[XB_PD] = (size_t)H;
+    words[XB_POX] = D == 2 ? (size_t)H : 0;
+    words[XB_PDX] = D == 2 ? (size_t)H : 0;
 }
 
 // Step bookkeeping: two argmax keys then the head-phase arrival counter (zeroed at creation,

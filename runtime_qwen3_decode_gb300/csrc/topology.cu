@@ -241,16 +241,22 @@ int probe_pages(const Topology &t, uint8_t *region, int npages, int8_t *page_gro
 
 bool plan_exchange(const Topology &t, const int8_t *page_group, int npages, const size_t *words, XPlan *plan) {
     std::memset(plan, 0, sizeof(*plan));
+    // the candidate pages each die homes, handed out in order; a group's buffers come from its
+    // own die's pages except the far copies of its partial sums, which the other die homes
+    std::vector<uint32_t> pool[kMaxGroups];
+    size_t next[kMaxGroups] = {0, 0};
+    for (int i = 0; i < npages; ++i) {
+        if (t.D == 2 && page_group[i] != 0 && page_group[i] != 1) return false;
+        pool[t.D == 2 ? page_group[i] : 0].push_back((uint32_t)i);
+    }
     for (int g = 0; g < t.D; ++g) {
-        std::vector<uint32_t> pages;
-        for (int i = 0; i < npages; ++i)
-            if (t.D == 1 || page_group[i] == g) pages.push_back((uint32_t)i);
         size_t used = 0;
         for (int b = 0; b < kXBufs; ++b) {
             const size_t np = (words[b] + kPageWords - 1) / kPageWords;
-            if (used + np > pages.size() || used + np > (size_t)kMaxXPages) return false;
+            const int die = (t.D == 2 && (b == XB_POX || b == XB_PDX)) ? 1 - g : g;
+            if (used + np > (size_t)kMaxXPages || next[die] + np > pool[die].size()) return false;
             plan->first[g][b] = (uint16_t)used;
-            for (size_t k = 0; k < np; ++k) plan->page[g][used + k] = pages[used + k];
+            for (size_t k = 0; k < np; ++k) plan->page[g][used + k] = pool[die][next[die]++];
             used += np;
         }
     }
