@@ -250,11 +250,14 @@ int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
 
 /*
  * Timeline of the last decode step (needs QW_DEBUG_TRACE): uint64 %globaltimer
- * nanoseconds [phase][cta][8], phase = 5*layer + {0 QKV, 1 attention, 2 o_proj,
+ * nanoseconds [phase][cta][16], phase = 5*layer + {0 QKV, 1 attention, 2 o_proj,
  * 3 gate/up, 4 down} and 5*n_layers for the head; stamps 0..3 = consumer entering
  * the phase, its inputs arrived, inputs staged (compute starts), phase done; 4, 5 =
- * producer's first and last copy issue of the phase.  n must equal
- * QW_QUERY_TRACE_LEN.
+ * producer's first and last copy issue of the phase; 6, 7 = row phases: weight chunks
+ * taken, compute done; attention: cached chunks done, merge inputs arrived; 8..12 =
+ * row phases, first consumer warp: activation loaded, preloaded rows reduced, their
+ * outputs stored, further rows done, chunks released (0 where a stamp does not apply).
+ * n must equal QW_QUERY_TRACE_LEN.
  */
 int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n);
 

@@ -450,7 +450,7 @@ __device__ __noinline__ void producer() {
 
 constexpr int kFailed = -1;                 // uniform: the step is aborting
 constexpr unsigned kDeadBit = 0x80000000u;  // this warp gave up inside a chunk loop
-constexpr int kFusedChunks = kSlots - 2;    // phases with at most this many chunks take them all at once
+constexpr int kHeadBatch = 1;               // head chunks a warp holds at once (the rest stay in flight)
 
 __device__ __forceinline__ int ctid() { return threadIdx.x; }
 __device__ __forceinline__ int cwarp() { return threadIdx.x >> 5; }
@@ -779,6 +779,7 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
     float2 act[NP][4];
 #pragma unroll
     for (int s = 0; s < NP; ++s) load_slice(sm.u.vec, s, lane, act[s]);
+    if (tr && ctid() == 0) tr[8] = gtime();
     const int buf = kind == T_QKV ? XB_QKV : kind == T_OPROJ ? XB_PO : kind == T_GATEUP ? XB_ACT : XB_PD;
     // the preloaded rows
     {
@@ -798,6 +799,7 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
             for (int q = 0; q < PR; ++q)
 #pragma unroll
                 for (int r = 0; r < NR; ++r) o[q][r] += __shfl_xor_sync(0xffffffffu, o[q][r], off);
+        if (tr && ctid() == 0) tr[9] = gtime();
         if (lane == 0) {
 #pragma unroll
             for (int q = 0; q < PR; ++q) {
@@ -810,6 +812,7 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
                 }
             }
         }
+        if (tr && ctid() == 0) tr[10] = gtime();
     }
     // any further rows of this warp
     for (int j = warp + PR * kConsumerWarps; j < R; j += kConsumerWarps) {
@@ -838,6 +841,7 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
             emit_row<PAIR>(sm, buf, p.r0 + j, o, out_tag);
         }
     }
+    if (tr && ctid() == 0) tr[11] = gtime();
     return true;
 }
 
@@ -896,8 +900,9 @@ __device__ __forceinline__ void gemv_ksplit(const Phase &p, int kind, unsigned i
     }
 }
 
-// The head: rows [p.r0, p.r1) of the tied lm_head streamed through the ring in batches of up to
-// kFusedChunks chunks; each warp owns whole rows (full K = H, the activation in registers) and
+// The head: rows [p.r0, p.r1) of the tied lm_head streamed through the ring in batches of
+// kHeadBatch chunks, which each warp takes and releases on its own, so the other slots stay in
+// flight; each warp owns whole rows (full K = H, the activation in registers) and
 // keeps the best packed (logit, id) key it has seen.  Returns the new ring position (kDeadBit
 // set if this warp gave up).
 __device__ __forceinline__ int gemv_head(const Phase &p, unsigned it, float scale) {
@@ -911,8 +916,8 @@ __device__ __forceinline__ int gemv_head(const Phase &p, unsigned it, float scal
     for (int s = 0; s < NS; ++s) load_slice(sm.u.vec, s, lane, act[s]);
     unsigned long long best = 0;
     bool bad = false, dead = false;
-    for (int c0 = 0; c0 < p.nchunks && !dead; c0 += kFusedChunks) {
-        const int nb = min(kFusedChunks, p.nchunks - c0);
+    for (int c0 = 0; c0 < p.nchunks && !dead; c0 += kHeadBatch) {
+        const int nb = min(kHeadBatch, p.nchunks - c0);
         for (int c = 0; c < nb && !dead; ++c) dead = !take_slot((it + c) % kSlots, ((it + c) / kSlots) & 1u);
         if (dead) break;
         const int g1 = min(R, (c0 + nb) * p.rpc);
@@ -992,6 +997,7 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (!ok) return kFailed;
     if (tr && ctid() == 0) tr[7] = gtime();
     for (int c = 0; c < p.nchunks; ++c) release_slot((it + c) % kSlots);
+    if (tr && ctid() == 0) tr[12] = gtime();
     it += p.nchunks;
     return (int)it;
 }

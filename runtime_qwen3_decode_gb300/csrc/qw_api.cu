@@ -165,7 +165,13 @@ int launch_step(qw_model *m, int32_t token, int32_t *tok_out_dev) {
     a.debug = m->debug;
     a.wait_ns = (m->debug & QW_DEBUG_WITHHOLD) ? qw::kDebugWaitLimitNs : qw::kWaitLimitNs;
     a.tok_out = tok_out_dev;
-    a.trace = (m->debug & QW_DEBUG_TRACE) ? (unsigned long long *)(m->ws + m->lay.trace) : nullptr;
+    a.trace = nullptr;
+    if (m->debug & QW_DEBUG_TRACE) {  // a fresh timeline per step: stamps a phase does not set stay 0
+        a.trace = (unsigned long long *)(m->ws + m->lay.trace);
+        const size_t n = ((size_t)qw::kPhasesPerLayer * m->cfg.n_layers + 1) * m->ncta * qw::kTraceStamps * 8;
+        const int zr = cuda_status(cudaMemsetAsync(a.trace, 0, n, m->stream));
+        if (zr) return zr;
+    }
     m->step_seq += 1;
     if (m->step_seq >= (1u << 23)) {  // tag_base stays below 2^32: restart the tags on a clean region
         m->step_seq = 1;

@@ -85,7 +85,7 @@ constexpr uint16_t kNoRole = 0xffff;
 
 // Debug timeline stamps per (phase, CTA): consumer before wait, after wait, after
 // compute, after its outputs are written; producer first issue, last issue of the phase.
-constexpr int kTraceStamps = 8;
+constexpr int kTraceStamps = 16;
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // every device-side wait gives up after 1 s
 constexpr unsigned long long kDebugWaitLimitNs = 1000000ull; // ... or after 1 ms under the withholding debug flag

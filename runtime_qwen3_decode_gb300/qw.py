@@ -388,13 +388,13 @@ class Model:
         return int(v.value)
 
     def debug_trace(self):
-        """[phase, cta, 8] uint64 ns timeline of the last decode step (needs DEBUG_TRACE)."""
+        """[phase, cta, 16] uint64 ns timeline of the last decode step (needs DEBUG_TRACE)."""
         import torch
         n = self.query(QUERY_TRACE_LEN)
         ncta = self.query(QUERY_DECODE_CTAS)
         out = torch.zeros(n, dtype=torch.int64, device="cuda")
         _check(_lib().qw_debug_trace(self._h, out.data_ptr(), n), "qw_debug_trace")
-        return out.view(-1, ncta, 8)
+        return out.view(-1, ncta, 16)
 
     def debug_hidden(self):
         import torch
