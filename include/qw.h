@@ -254,9 +254,11 @@ int qw_debug_hidden(qw_model *m, float *dst_dev, int64_t n);
  * 3 gate/up, 4 down} and 5*n_layers for the head; stamps 0..3 = consumer entering
  * the phase, its inputs arrived, inputs staged (compute starts), phase done; 4, 5 =
  * producer's first and last copy issue of the phase; 6, 7 = row phases: weight chunks
- * taken, compute done; attention: cached chunks done, merge inputs arrived; 8..12 =
- * row phases, first consumer warp: activation loaded, preloaded rows reduced, their
- * outputs stored, further rows done, chunks released (0 where a stamp does not apply).
+ * taken, compute done; attention: cached chunks done, merge inputs arrived; 8..14 =
+ * SM clock cycles (clock64, comparable within one CTA only) of the first consumer warp
+ * in the row phases: 13 compute entered, 8 weights and activation in registers, 9 its
+ * rows reduced and stored, 11 further rows done, 12 chunks released, 14 phase done
+ * (0 where a stamp does not apply).
  * n must equal QW_QUERY_TRACE_LEN.
  */
 int qw_debug_trace(qw_model *m, uint64_t *dst_dev, int64_t n);

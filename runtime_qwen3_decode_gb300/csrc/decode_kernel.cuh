@@ -451,6 +451,12 @@ __device__ __noinline__ void producer() {
 constexpr int kFailed = -1;                 // uniform: the step is aborting
 constexpr unsigned kDeadBit = 0x80000000u;  // this warp gave up inside a chunk loop
 constexpr int kHeadBatch = 1;               // head chunks a warp holds at once (the rest stay in flight)
+// rows (gate/up: pairs) a warp keeps in registers in the row phases: the Qwen3-0.6B block over
+// 76 SMs per group (152 in one group) gives q|k|v 27, gate/up 21 pairs, o_proj and down 14 rows
+// per CTA, i.e. at most 4, 3 and 2 per warp
+constexpr int kPreQkv = 4;
+constexpr int kPreGateUp = 3;
+constexpr int kPreDown = 2;
 
 __device__ __forceinline__ int ctid() { return threadIdx.x; }
 __device__ __forceinline__ int cwarp() { return threadIdx.x >> 5; }
@@ -471,6 +477,11 @@ __device__ __forceinline__ void release_slot(unsigned slot) {
     __syncwarp();
     if (clane() == 0) mbar_arrive(&smem().empty[slot]);
 }
+
+// The staging hook of phases with nothing to overlap with the input barrier.
+struct NoPre {
+    __device__ __forceinline__ void operator()() const {}
+};
 
 // Make a per-thread poll result uniform over the consumer threads (one barrier).
 __device__ __forceinline__ bool all_ok(bool ok) {
@@ -713,36 +724,72 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
     return all_ok(ok);
 }
 
-// Output of one finished row (lane 0): the tagged word of the row (silu(gate) * up for a
-// gate/up pair), both dot products already scaled.
-template <bool PAIR>
-__device__ __forceinline__ void emit_row(const Smem &sm, int buf, int row, const float (&o)[PAIR ? 2 : 1],
-                                         unsigned out_tag) {
-    // failure-path test: the first CTA of group 0 withholds its rows of the step's first phase
-    if ((sm.args.debug & kDebugWithhold) && sm.ph == 0 && sm.g == 0 && sm.r == 0) return;
-    float v = o[0];
-    if constexpr (PAIR) v = (o[0] / (1.0f + __expf(-o[0]))) * o[1];  // silu(gate) * up
-    st_tag(xw(sm, sm.g, buf, row), v, out_tag);
-    // two groups: the partial sums also go to the other die's copy, so every reader polls
-    // words its own die homes
-    if (sm.args.D == 2 && (buf == XB_PO || buf == XB_PD)) st_tag(xw(sm, sm.g, buf + kXFar, row), v, out_tag);
+// Where a phase's output words go: rows [r0, r1) of one exchange buffer of the CTA's group (and,
+// for the two partial sums with two groups, of its far-die copy), resolved to at most two page
+// runs before the phase waits for its input, so storing a result needs no table lookup.
+struct OutRows {
+    unsigned long long *lo, *hi, *flo, *fhi;  // first page run, the next one; far copy (or null)
+    int split;                                // rows of the first run
+    bool mute;                                // failure-path test: this CTA withholds its rows
+    __device__ __forceinline__ void init(const Smem &sm, int buf, int r0, int r1) {
+        const int first = kPageWords - (r0 & (kPageWords - 1));
+        split = first;
+        lo = xw(sm, sm.g, buf, r0);
+        hi = r1 - r0 > first ? xw(sm, sm.g, buf, r0 + first) : lo;
+        const bool far = sm.args.D == 2 && (buf == XB_PO || buf == XB_PD);
+        flo = far ? xw(sm, sm.g, buf + kXFar, r0) : nullptr;
+        fhi = far && r1 - r0 > first ? xw(sm, sm.g, buf + kXFar, r0 + first) : flo;
+        mute = (sm.args.debug & kDebugWithhold) && sm.ph == 0 && sm.g == 0 && sm.r == 0;
+    }
+    __device__ __forceinline__ void put(int jl, float v, unsigned tag) const {
+        if (mute) return;
+        const bool a = jl < split;
+        st_tag(a ? lo + jl : hi + (jl - split), v, tag);
+        if (flo) st_tag(a ? flo + jl : fhi + (jl - split), v, tag);
+    }
+};
+
+// Warp sums of RP values at once (RP a power of two, at most 32): the first log2(RP) exchange
+// levels halve the values each lane carries, so the whole reduction takes RP - 1 + 5 - log2(RP)
+// shuffles instead of 5 RP.  Afterwards every lane holds the total of value lane / (32 / RP).
+template <int RP>
+__device__ __forceinline__ float warp_sum_many(float (&v)[RP], int lane) {
+#pragma unroll
+    for (int h = RP / 2, o = 16; h >= 1; h >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h], keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 / RP; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
 }
 
-// A layer phase over rows [p.r0, p.r1) with K = 256 NP columns (K <= 1536), all chunks already
-// taken: warp w owns rows w, w + 7, ... (gate/up: pairs).  The weight pieces of its first PR
-// rows are loaded into registers before the phase input is waited for (they do not depend on
-// it); after the input is staged only the activation read, the paired FMAs and one warp
-// reduction per row remain.
-template <int NP, bool I8, bool PAIR, int D>
-__device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned it0, unsigned out_tag,
-                                              unsigned long long *tr) {
+template <int N>
+__host__ __device__ constexpr int pow2_at_least(int n = 1) { return n >= N ? n : pow2_at_least<N>(2 * n); }
+
+// A layer phase over rows [p.r0, p.r1) with K = 256 NP columns (K <= 1536), all chunks taken and
+// the input staged (scale: the deferred RMSNorm factor): warp w owns rows w, w + 7, ... (gate/up:
+// pairs).  It loads the weight pieces of its first PR rows from the ring into registers at once,
+// reads the activation, runs the paired FMAs of all its rows and one transposed warp reduction
+// for all of them, and stores the results through precomputed addresses.  Rows beyond PR per
+// warp (only with fewer SMs than the block is laid out for) follow one at a time.
+template <int NP, bool I8, bool PAIR, int PR>
+__device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0, unsigned out_tag, float scale,
+                                          unsigned long long *tr) {
     constexpr int NR = PAIR ? 2 : 1;
-    constexpr int PR = 8 / (NP * NR) > 0 ? 8 / (NP * NR) : 1;  // rows preloaded: at most 8 pieces (32 registers)
+    constexpr int NV = PR * NR;               // values a lane accumulates
+    constexpr int RP = pow2_at_least<NV>();   // padded to a power of two for the reduction
+    constexpr int LW = 32 / RP;               // lanes per reduced value
     constexpr int K = 256 * NP;
     Smem &sm = smem();
-    const DecodeArgs &a = sm.args;
     const int warp = cwarp(), lane = clane();
     const int R = p.r1 - p.r0;
+    const int buf = kind == T_QKV ? XB_QKV : kind == T_OPROJ ? XB_PO : kind == T_GATEUP ? XB_ACT : XB_PD;
     auto piece_rows = [&](int j, const uint8_t *(&rp)[NR], const uint8_t *(&sc)[NR]) {
         const int c = j / p.rpc, jj = j - c * p.rpc;
         const int n = min(p.rpc, R - c * p.rpc), ns = PAIR ? 2 * n : n;
@@ -754,36 +801,26 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
             sc[1] = slot_scales<I8>(sp, K, ns, n + jj);
         }
     };
-    // this warp's first PR rows: loaded once its own share of the input poll is done, so the
-    // loads overlap the block barrier instead of following it
+    if (tr && ctid() == 0) tr[13] = clock64();
     WPiece<I8> pre[PR][NR][NP];
-    auto preload = [&]() {
 #pragma unroll
-        for (int q = 0; q < PR; ++q) {
-            const int j = warp + q * kConsumerWarps;
-            if (j < R) {
-                const uint8_t *rp[NR], *sc[NR];
-                piece_rows(j, rp, sc);
+    for (int q = 0; q < PR; ++q) {
+        const int j = warp + q * kConsumerWarps;
+        const uint8_t *rp[NR], *sc[NR];
+        piece_rows(j < R ? j : 0, rp, sc);
 #pragma unroll
-                for (int r = 0; r < NR; ++r)
+        for (int r = 0; r < NR; ++r)
 #pragma unroll
-                    for (int s = 0; s < NP; ++s) pre[q][r][s].load(rp[r], sc[r], 32 * s + lane);
-            }
-        }
-    };
-    float scale;
-    if (!stage_input<D, vec_iters<(kBlockHq * kHeadDim / D > kBlockI / D ? kBlockHq * kHeadDim / D : kBlockI / D)>()>(
-            kind, p.l, K, a, tr, &scale, preload))
-        return false;
-    if (tr && ctid() == 0) tr[2] = gtime();
+            for (int s = 0; s < NP; ++s) pre[q][r][s].load(rp[r], sc[r], 32 * s + lane);
+    }
+    OutRows out;
+    out.init(sm, buf, p.r0, p.r1);
     float2 act[NP][4];
 #pragma unroll
     for (int s = 0; s < NP; ++s) load_slice(sm.u.vec, s, lane, act[s]);
-    if (tr && ctid() == 0) tr[8] = gtime();
-    const int buf = kind == T_QKV ? XB_QKV : kind == T_OPROJ ? XB_PO : kind == T_GATEUP ? XB_ACT : XB_PD;
-    // the preloaded rows
+    if (tr && ctid() == 0) tr[8] = clock64();
     {
-        float o[PR][NR];
+        float v[RP];  // value q NR + r = this lane's part of row (q, r)
 #pragma unroll
         for (int q = 0; q < PR; ++q)
 #pragma unroll
@@ -791,58 +828,47 @@ __device__ __forceinline__ bool gemv_rows_pre(const Phase &p, int kind, unsigned
                 float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int s = 0; s < NP; ++s) piece_fma<I8>(pre[q][r][s], act[s], acc[s & 1]);
-                o[q][r] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                v[q * NR + r] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
             }
 #pragma unroll
-        for (int off = 16; off; off >>= 1)
-#pragma unroll
-            for (int q = 0; q < PR; ++q)
-#pragma unroll
-                for (int r = 0; r < NR; ++r) o[q][r] += __shfl_xor_sync(0xffffffffu, o[q][r], off);
-        if (tr && ctid() == 0) tr[9] = gtime();
-        if (lane == 0) {
-#pragma unroll
-            for (int q = 0; q < PR; ++q) {
-                const int j = warp + q * kConsumerWarps;
-                if (j < R) {
-                    float v[NR];
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) v[r] = o[q][r] * scale;
-                    emit_row<PAIR>(sm, buf, p.r0 + j, v, out_tag);
-                }
-            }
+        for (int i = NV; i < RP; ++i) v[i] = 0.f;
+        const float t = warp_sum_many<RP>(v, lane) * scale;
+        const int vi = lane / LW;  // the value this lane now holds
+        if constexpr (PAIR) {
+            const float up = __shfl_xor_sync(0xffffffffu, t, LW);  // value vi + 1: the pair's up row
+            const int j = warp + (vi >> 1) * kConsumerWarps;
+            if ((lane & (2 * LW - 1)) == 0 && vi < NV && j < R)
+                out.put(j, (t / (1.0f + __expf(-t))) * up, out_tag);  // silu(gate) * up
+        } else {
+            const int j = warp + vi * kConsumerWarps;
+            if ((lane & (LW - 1)) == 0 && vi < NV && j < R) out.put(j, t, out_tag);
         }
-        if (tr && ctid() == 0) tr[10] = gtime();
+        if (tr && ctid() == 0) tr[9] = clock64();
     }
-    // any further rows of this warp
+    // any further rows of this warp (fewer SMs than the block is laid out for)
+#pragma unroll 1
     for (int j = warp + PR * kConsumerWarps; j < R; j += kConsumerWarps) {
         const uint8_t *rp[NR], *sc[NR];
         piece_rows(j, rp, sc);
-        WPiece<I8> wp[NR][NP];
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int s = 0; s < NP; ++s) wp[r][s].load(rp[r], sc[r], 32 * s + lane);
         float o[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int s = 0; s < NP; ++s) piece_fma<I8>(wp[r][s], act[s], acc[s & 1]);
-            o[r] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+            for (int s = 0; s < NP; ++s) {
+                WPiece<I8> wp;
+                wp.load(rp[r], sc[r], 32 * s + lane);
+                piece_fma<I8>(wp, act[s], acc[s & 1]);
+            }
+            o[r] = warp_sum((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) * scale;
         }
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) o[r] += __shfl_xor_sync(0xffffffffu, o[r], off);
         if (lane == 0) {
-#pragma unroll
-            for (int r = 0; r < NR; ++r) o[r] *= scale;
-            emit_row<PAIR>(sm, buf, p.r0 + j, o, out_tag);
+            float val = o[0];
+            if constexpr (PAIR) val = (o[0] / (1.0f + __expf(-o[0]))) * o[1];
+            out.put(j, val, out_tag);
         }
     }
-    if (tr && ctid() == 0) tr[11] = gtime();
-    return true;
+    if (tr && ctid() == 0) tr[11] = clock64();
 }
 
 // A layer phase over rows [p.r0, p.r1) of K stored columns whose chunks (all of them) are
@@ -968,7 +994,7 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (tr && ctid() == 0) tr[0] = gtime();
     if (kind == T_LMHEAD) {
         float scale;
-        if (!stage_input<D, vec_iters<KMAX>()>(kind, l, p.K, a, tr, &scale, [] {})) return kFailed;
+        if (!stage_input<D, vec_iters<KMAX>()>(kind, l, p.K, a, tr, &scale, NoPre{})) return kFailed;
         if (tr && ctid() == 0) tr[2] = gtime();
         return gemv_head(p, it, scale);
     }
@@ -979,25 +1005,25 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (!all_ok(!dead)) return kFailed;
     const unsigned out_tag =
         xtag(a, l, kind == T_QKV ? TK_QKV : kind == T_OPROJ ? TK_PO : kind == T_GATEUP ? TK_ACT : TK_PD);
-    bool ok = false;
-    if (kind == T_GATEUP) {
-        ok = gemv_rows_pre<4, I8, true, D>(p, kind, it, out_tag, tr);
-    } else if (kind == T_QKV || (kind == T_OPROJ && KO == kBlockH)) {
-        ok = gemv_rows_pre<4, I8, false, D>(p, kind, it, out_tag, tr);
-    } else if (kind == T_DOWN && KD == 1536) {
-        ok = gemv_rows_pre<6, I8, false, D>(p, kind, it, out_tag, tr);
-    } else if constexpr (D == 1) {  // one group: o_proj and down rows of 2048 / 3072 columns, split over the warps
-        float scale;
-        ok = stage_input<D, vec_iters<KMAX>()>(kind, l, p.K, a, tr, &scale, [] {});
-        if (ok) {
-            if (tr && ctid() == 0) tr[2] = gtime();
+    // one staging copy for every row phase (and the head): the phase's input vector in shared memory
+    float scale;
+    const bool ok = stage_input<D, vec_iters<KMAX>()>(kind, l, p.K, a, tr, &scale, NoPre{});
+    if (ok) {
+        if (tr && ctid() == 0) tr[2] = gtime();
+        if (kind == T_GATEUP) {
+            gemv_rows<4, I8, true, kPreGateUp>(p, kind, it, out_tag, scale, tr);
+        } else if (kind == T_QKV || (kind == T_OPROJ && KO == kBlockH)) {
+            gemv_rows<4, I8, false, kPreQkv>(p, kind, it, out_tag, scale, tr);
+        } else if (kind == T_DOWN && KD == 1536) {
+            gemv_rows<6, I8, false, kPreDown>(p, kind, it, out_tag, scale, tr);
+        } else if constexpr (D == 1) {  // one group: o_proj and down rows of 2048 / 3072 columns, split over the warps
             gemv_ksplit<I8, false>(p, kind, it, out_tag);
         }
     }
     if (!ok) return kFailed;
     if (tr && ctid() == 0) tr[7] = gtime();
     for (int c = 0; c < p.nchunks; ++c) release_slot((it + c) % kSlots);
-    if (tr && ctid() == 0) tr[12] = gtime();
+    if (tr && ctid() == 0) tr[12] = clock64();
     it += p.nchunks;
     return (int)it;
 }
@@ -1388,7 +1414,10 @@ __device__ void consumer() {
         if (tid == 0) {
             sm.ph = ph + 1;  // read by expiring waits of the next phase
             unsigned long long *tr = trace_of(a, ph);
-            if (tr) tr[3] = gtime();
+            if (tr) {
+                tr[3] = gtime();
+                tr[14] = clock64();
+            }
         }
         return true;
     };
