@@ -651,20 +651,13 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
     float4 *vec4 = reinterpret_cast<float4 *>(sm.u.vec);
     float4 *x4 = reinterpret_cast<float4 *>(sm.x);
     bool ok = true;
+    if (tr && tid == 0) tr[10] = clock64();
     if (kind == T_QKV || kind == T_GATEUP || kind == T_LMHEAD) {
         const __nv_bfloat16 *nwp = kind == T_QKV ? a.layers[l].input_norm
                                    : kind == T_GATEUP ? a.layers[l].post_norm
                                                       : a.final_norm;
         constexpr int NH = vec_iters<kBlockH>();  // float4 slots of x per thread
         float4 nw[NH];
-#pragma unroll
-        for (int i = 0; i < NH; ++i) {
-            const int idx = tid + kConsumerThreads * i;
-            if (idx < kBlockH / 4) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(nwp) + idx);
-                nw[i] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
-            }
-        }
         float4 pv[D][NH];
         if (!(kind == T_QKV && l == 0)) {  // at layer 0 x is the embedding, already staged
             const int b = kind == T_GATEUP ? XB_PO : XB_PD;
@@ -678,7 +671,18 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
             }
             ok = poll_vec<D, kBlockH>(gg, bb, tg, pv, a.flags);
         }
-        if (tr && tid == 0) tr[1] = gtime();
+        if (tr && tid == 0) {
+            tr[1] = gtime();
+            tr[15] = clock64();
+        }
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+            const int idx = tid + kConsumerThreads * i;
+            if (idx < kBlockH / 4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(nwp) + idx);
+                nw[i] = make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+            }
+        }
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < NH; ++i) {
@@ -713,7 +717,10 @@ __device__ __forceinline__ bool stage_input(int kind, int l, int K, const Decode
     const int gg[1] = {sm.g};
     float4 v[1][NI];
     ok = poll_vec_n<1, NI>(gg, b, K / 4, tg, v, a.flags);
-    if (tr && tid == 0) tr[1] = gtime();
+    if (tr && tid == 0) {
+        tr[1] = gtime();
+        tr[15] = clock64();
+    }
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
         const int idx = tid + kConsumerThreads * i;
