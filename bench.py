@@ -435,6 +435,58 @@ def decode_sub(qw, wl, K: int, W: int, gpu: int) -> dict:
             "clocks": r["clocks"]}
 
 
+def measure_batch(qw, wl, B: int, K: int, W: int, gpu: int) -> dict:
+    """Batched decode (qw_batch_*): B sequences of the workload's shape, each with its own
+    seeded prompt of the workload's length, prefilled, then W untimed and K timed steps of all B
+    (CUDA events on the model's stream, a synchronize on both sides)."""
+    import torch
+
+    host = qi.make_weights(wl)
+    dev = qw.weights_to_device(host, int8=wl.weight_format == "int8_g32")
+    del host
+    n_ctx = wl.prompt_len + W + K + 1
+    model = qw.Model(wl, dev, max_ctx=n_ctx)
+    batch = qw.Batch(model, B, n_ctx)
+    g = np.random.default_rng(1000 + B)
+    for s in range(B):
+        batch.prefill(s, g.integers(0, wl.vocab, size=wl.prompt_len), want_token=False)
+    for _ in range(W):
+        batch.step(B, want_tokens=False)
+    model.sync()
+    batch.sync()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(gpu)
+    clocks.start()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    first = batch.length(0)
+    t0.record(stream)
+    for _ in range(K):
+        batch.step(B, want_tokens=False)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    batch.sync()
+    ms = t0.elapsed_time(t1)
+    positions = range(first, first + K)
+    step_bytes = [weight_bytes(wl) + B * (kv_bytes_per_pos(wl) * (p + 1) + 4 * wl.vocab) for p in positions]
+    peak, peak_kind = measured_peaks()
+    achieved = sum(step_bytes) / (ms / 1000.0) / 1e9
+    batch.close()
+    model.close()
+    del dev
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "batch": B, "value": B * K / (ms / 1000.0), "unit": "tokens/s (all sequences)",
+            "per_sequence": K / (ms / 1000.0), "steps": K, "warmup": W, "ms_per_step": ms / K,
+            "positions_timed": [positions[0], positions[-1]],
+            "compute": "fp16 tensor-core operands for the projections and MLP (M = batch), f32 accumulation; "
+                       "per-sequence split attention and the lm_head on CUDA cores",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "bytes_per_step_at_first_pos": step_bytes[0]},
+            "clocks": clk}
+
+
 def run_ours(args, wl):
     import torch
 
@@ -478,6 +530,9 @@ def run_ours(args, wl):
             sub = qi.WORKLOADS[name]
             if sub.name != wl.name:
                 line[key] = decode_sub(qw, sub, min(k_sub, sub.decode_steps - W), W, local)
+    if not args.no_extra and ws == 1:
+        for B in (8,):
+            line[f"decode_batch{B}"] = measure_batch(qw, qi.WORKLOADS["qwen3_0p6b_decode"], B, 64, W, local)
     if not args.no_prefill:
         line["prefill"] = measure_prefill(qw, qi.WORKLOADS[args.prefill_workload], args.prefill_reps,
                                           max(3, min(W, 5)), local)

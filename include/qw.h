@@ -204,6 +204,58 @@ int qw_sync(qw_model *m);
 /* Release the handle (the caller's device buffers are untouched). NULL is allowed. */
 void qw_model_destroy(qw_model *m);
 
+/* ---------------------------------------------------------- batched decode */
+
+/*
+ * A batch: up to 8 independent sequences of one model, each with its own K/V cache
+ * and length, decoded together one token per sequence per step ("Portable WebAssembly
+ * Runtime Architecture for TinyRustLM", sections "Threads, Scheduling" and "Prefill
+ * versus decode"; each sequence computes exactly the decode step of the single-sequence
+ * calls).  The B rows of a step run through the batched prefill's tensor-core GEMMs
+ * (fp16 operands, f32 accumulation, M = B), per-sequence split attention over each
+ * cache, and one pass of the tied lm_head for all rows; the cache uses the model's
+ * format.  Requires the batched prefill (qw_prefill's tensor-core path) to be available
+ * and query heads = 2 x KV heads; max_ctx <= the model's max_ctx.
+ *
+ * Workspace: caller-owned device memory of qw_batch_workspace_bytes (256-byte aligned),
+ * holding every sequence's cache ([n_layers][n_kv_heads][max_ctx][head_dim] K and V
+ * blocks), logits [max_batch][vocab] and step scratch.  Calls are stream-ordered on the
+ * model's stream and share the model's prefill scratch: do not run batch calls and the
+ * model's own calls concurrently from several threads.  A batch becomes invalid when
+ * its model is destroyed.
+ */
+typedef struct qw_batch qw_batch;
+enum { QW_BATCH_MAX = 8 };
+
+/* Bytes of device workspace for a batch; 0 for an invalid model or sizes. */
+size_t qw_batch_workspace_bytes(const qw_model *m, int32_t max_batch, int32_t max_ctx);
+int qw_batch_create(qw_model *m, int32_t max_batch, int32_t max_ctx, void *workspace_dev, size_t workspace_bytes,
+                    qw_batch **out);
+void qw_batch_destroy(qw_batch *b);
+/* Length of sequence seq <- 0 (seq = -1: every sequence, and a recorded device error is
+ * cleared). */
+int qw_batch_reset(qw_batch *b, int32_t seq);
+int qw_batch_length(const qw_batch *b, int32_t seq, int32_t *out);
+/* Append n prompt tokens to sequence seq through the batched prefill; its greedy pick
+ * becomes the sequence's device-resident last token (and goes to *next_token_host if
+ * given, which synchronises). */
+int qw_batch_prefill(qw_batch *b, int32_t seq, const int32_t *tokens_host, int32_t n, int32_t *next_token_host);
+/* One decode step of sequences 0 .. n_seq-1: tokens_host[s] is sequence s's input token,
+ * or -1 (or tokens_host NULL for all) for its device-resident last pick.  Each sequence
+ * appends one K/V row at its own length.  next_tokens_host [n_seq] (optional) receives
+ * the greedy picks and synchronises; without it the call returns after launching.
+ * QW_CONTEXT_EXCEEDED if any sequence is full; a non-finite logit sets
+ * QW_NUMERICAL_FAILURE, reported by the next synchronising call, after which the batch
+ * refuses work until qw_batch_reset(b, -1). */
+int qw_batch_step(qw_batch *b, int32_t n_seq, const int32_t *tokens_host, int32_t *next_tokens_host);
+/* f32 logits [n_seq][vocab] of the last step (device), n = n_seq * vocab. */
+int qw_batch_logits(qw_batch *b, float *dst_dev, int64_t n);
+/* f32 [n_layers + 1][n_seq][hidden] residual stream of the last step (the model's
+ * QW_DEBUG_HIDDEN flag must have been set for that step). */
+int qw_batch_debug_hidden(qw_batch *b, float *dst_dev, int64_t n);
+/* Wait for the batch's work; returns a recorded device error. */
+int qw_batch_sync(qw_batch *b);
+
 /* ---------------------------------------------------------------- testing */
 
 /*

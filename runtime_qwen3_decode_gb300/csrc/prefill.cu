@@ -35,6 +35,7 @@
 #include <cstdio>
 #include <vector>
 
+#include "qw_batch.h"
 #include "qw_prefill.h"
 #include "tc.cuh"
 
@@ -60,8 +61,12 @@ struct QkvOut {
     int q_rows;
     void *kc, *vc;                         // this layer's cache planes [Hkv][max_ctx][128]
     int kv_f32, max_ctx;
-    __half *k16, *v16t;                    // fp16 shadows [Hkv][kv_rows][128] and [Hkv][128][kv_rows]
+    __half *k16, *v16t;                    // fp16 shadows [Hkv][kv_rows][128] and [Hkv][128][kv_rows] (or null)
     int kv_rows;
+    // batched decode: row t is the new position row_pos[t] of sequence t, whose cache planes sit
+    // t * seq_elems elements after kc / vc; null for a prompt (row t at position pos0 + t)
+    const int *row_pos;
+    size_t seq_elems;
 };
 
 struct GemmParams {
@@ -166,7 +171,7 @@ __device__ __forceinline__ float4 round_bf16(float4 x) {
 template <typename KT>
 __device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32], int slot, int t, int r0, int M,
                                              float *stg) {
-    const int P = o.pos0 + t;
+    const int P = o.row_pos ? (t < M ? o.row_pos[t] : 0) : o.pos0 + t;
     if (slot < o.Hq + o.Hkv) {
         const __nv_bfloat16 *w = slot < o.Hq ? o.q_norm : o.k_norm;
         float ss = 0.f;
@@ -198,20 +203,22 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32],
                 *reinterpret_cast<uint2 *>(o.q16 + ((size_t)slot * o.q_rows + tr) * kHeadDim + d) = pack_half4(x);
                 return;
             }
-            const size_t prow = (size_t)(o.pos0 + tr) * kHeadDim + d;
+            const size_t prow = (o.row_pos ? (size_t)tr * o.seq_elems + (size_t)o.row_pos[tr] * kHeadDim
+                                           : (size_t)(o.pos0 + tr) * kHeadDim) +
+                                d;
             if constexpr (sizeof(KT) == 4) {
                 *reinterpret_cast<float4 *>(cache + prow) = x;
             } else {
                 *reinterpret_cast<uint2 *>(cache + prow) = pack_bf164(x);
                 x = round_bf16(x);  // the shadows hold the cached value
             }
-            if (is_k)
+            if (is_k && o.k16)
                 *reinterpret_cast<uint2 *>(o.k16 + ((size_t)kvh * o.kv_rows + o.pos0 + tr) * kHeadDim + d) =
                     pack_half4(x);
         });
     }
     // V^T shadow: for each dim the warp's 32 rows are 32 consecutive positions (64 B)
-    if (!is_q && !is_k && t < M) {
+    if (!is_q && !is_k && t < M && o.v16t) {
         __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P;
 #pragma unroll
         for (int i = 0; i < kHeadDim; ++i) {
@@ -1222,6 +1229,7 @@ cudaError_t prefill_prepare() {
     if ((e = set_gemm_attr<256, EPI_SWIGLU>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_ADD>()) != cudaSuccess) return e;
     if ((e = set_gemm_attr<128, EPI_STORE>()) != cudaSuccess) return e;
+    if ((e = batch_prepare()) != cudaSuccess) return e;
     return cudaFuncSetAttribute(fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FaSmem::kDyn);
 }
 
@@ -1424,6 +1432,110 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
         if (cudaGetLastError() != cudaSuccess) return 1;
     }
     return 0;
+}
+
+// ------------------------------------------------------------------ batched decode
+
+int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &bs, cudaStream_t stream) {
+    PrefillImpl *im = st->impl;
+    if (!im || !st->ready || bs.B < 1 || bs.B > st->rows_max || bs.B > kBatchMax) return 1;
+    const qw_config &c = im->cfg;
+    const PrefillLayout &L = im->lay;
+    uint8_t *buf = st->buf;
+    const int H = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, QD = Hq * kHeadDim, KD = Hkv * kHeadDim,
+              I = c.intermediate, B = bs.B;
+    if (Hq != kBatchG * Hkv) return 1;
+    float *x = reinterpret_cast<float *>(buf + L.x);
+    __half *h = reinterpret_cast<__half *>(buf + L.h);
+    __half *q16 = reinterpret_cast<__half *>(buf + L.q16);
+    __half *o16 = reinterpret_cast<__half *>(buf + L.o16);
+    __half *act = reinterpret_cast<__half *>(buf + L.act);
+    const size_t esz = a.kv_f32 ? 4 : 2;
+    const size_t plane = (size_t)Hkv * bs.max_ctx * kHeadDim;  // elements of one layer's K (or V) plane
+    const DevLayer *hl = im->host_layers.data();
+    const int S = batch_splits(bs.max_n);
+    CUtensorMap mh, mo, ma;
+    if (!make_map(&mh, h, B, H, BM) || !make_map(&mo, o16, B, QD, BM) || !make_map(&ma, act, B, I, BM)) return 1;
+    if (launch_batch_tokens(bs.tokens_in, bs.picks, B, bs.tokens, stream) != cudaSuccess) return 1;
+    launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream);
+    if (bs.hidden) cudaMemcpyAsync(bs.hidden, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, stream);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
+        uint8_t *kc = reinterpret_cast<uint8_t *>(bs.kc) + (size_t)l * plane * esz;
+        uint8_t *vc = reinterpret_cast<uint8_t *>(bs.vc) + (size_t)l * plane * esz;
+        GemmParams gp{};
+        gp.flags = a.flags;
+        gp.M = B;
+        // q | k | v: QK-Norm, RoPE at each sequence's position, K/V rows into each sequence's cache
+        gp.N = QD + 2 * KD;
+        gp.K = H;
+        QkvOut &qo = gp.qkv;
+        qo.q_norm = hl[l].q_norm;
+        qo.k_norm = hl[l].k_norm;
+        qo.rope = a.rope;
+        qo.Hq = Hq;
+        qo.Hkv = Hkv;
+        qo.eps = a.eps;
+        qo.q16 = q16;
+        qo.q_rows = st->rows_max;
+        qo.kc = kc;
+        qo.vc = vc;
+        qo.kv_f32 = a.kv_f32;
+        qo.max_ctx = bs.max_ctx;
+        qo.row_pos = bs.row_pos;
+        qo.seq_elems = bs.seq_elems;
+        if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
+        BatchAttn ap{};
+        ap.q16 = q16;
+        ap.q_rows = st->rows_max;
+        ap.kc = kc;
+        ap.vc = vc;
+        ap.seq_elems = bs.seq_elems;
+        ap.max_ctx = bs.max_ctx;
+        ap.row_pos = bs.row_pos;
+        ap.S = S;
+        ap.Hq = Hq;
+        ap.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
+        ap.part = bs.part;
+        if (launch_batch_attn(ap, Hkv, B, a.kv_f32, stream) != cudaSuccess) return 1;
+        if (launch_batch_merge(bs.part, S, Hq, B, o16, QD, stream) != cudaSuccess) return 1;
+        // x += o Wo^T
+        gp.N = H;
+        gp.K = QD;
+        gp.out = x;
+        gp.ldo = H;
+        if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
+        launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream);
+        // a = silu(h Wg^T) * (h Wu^T)
+        gp.N = 2 * I;
+        gp.K = H;
+        gp.act = act;
+        gp.ldh = I;
+        if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream) != cudaSuccess) return 1;
+        // x += a Wd^T
+        gp.N = H;
+        gp.K = I;
+        gp.out = x;
+        gp.ldo = H;
+        if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream) != cudaSuccess) return 1;
+        if (bs.hidden)
+            cudaMemcpyAsync(bs.hidden + (size_t)(l + 1) * B * H, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
+                            stream);
+        if (l + 1 < c.n_layers) launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream);
+    }
+    BatchHead hp{};
+    hp.x = x;
+    hp.final_norm = a.final_norm;
+    hp.E = a.lm_head;
+    hp.B = B;
+    hp.V = a.V;
+    hp.eps = a.eps;
+    hp.logits = bs.logits;
+    hp.keys = bs.keys;
+    hp.picks = bs.picks;
+    hp.flags = a.flags;
+    if (launch_batch_head(hp, H, st->nsm, stream) != cudaSuccess) return 1;
+    return cudaGetLastError() != cudaSuccess;
 }
 
 // ------------------------------------------------------------------ GEMM test entry

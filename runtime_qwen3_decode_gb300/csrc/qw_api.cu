@@ -15,6 +15,7 @@
 
 #include "qw.h"
 #include "qw_internal.h"
+#include "qw_batch.h"
 #include "qw_prefill.h"
 #include "qw_sample.h"
 
@@ -672,6 +673,292 @@ int qw_debug_gemm_f16(const void *a_dev, const void *b_dev, float *c_dev, int32_
     if (!a_dev || !b_dev || !c_dev) return QW_INVALID_ARGUMENT;
     if (!aligned(a_dev, 16) || !aligned(b_dev, 16) || !aligned(c_dev, 16)) return QW_ALIGNMENT;
     return qw::prefill_debug_gemm(a_dev, b_dev, c_dev, M, N, K, bn, (cudaStream_t)cuda_stream);
+}
+
+// ------------------------------------------------------------------ batched decode
+
+}  // extern "C"
+
+struct qw_batch {
+    qw_model *m = nullptr;
+    int max_batch = 0, max_ctx = 0;
+    size_t seq_elems = 0;                // elements of one sequence's K (or V) cache block
+    uint8_t *kc = nullptr, *vc = nullptr;
+    int32_t *tok_in = nullptr, *tok = nullptr, *picks = nullptr;
+    int *row_pos = nullptr;
+    unsigned long long *keys = nullptr;
+    qw::StepFlags *flags = nullptr;
+    float *part = nullptr, *logits = nullptr, *hidden = nullptr;
+    std::vector<int32_t> len;
+    std::vector<int> has_last;
+    int last_n = 0;                      // sequences of the last step (rows of logits / hidden)
+    int failed = 0;
+    // A step's launches depend on the sequence count, the attention split count and the debug
+    // dump only; each combination is captured once (on a private stream) into a CUDA graph and
+    // replayed on the model's stream.
+    struct Graph {
+        int B, S, hidden;
+        cudaGraphExec_t exec;
+    };
+    std::vector<Graph> graphs;
+    cudaStream_t cap = nullptr;
+};
+
+namespace {
+
+std::unordered_set<const void *> g_live_batch;
+
+bool live_batch(const qw_batch *b) {
+    std::lock_guard<std::mutex> g(g_live_mu);
+    return b && g_live_batch.count(b) && g_live.count(b->m);
+}
+
+struct BatchLayout {
+    size_t kc, vc, small, flags, part, logits, hidden, total;
+};
+
+// Regions of a batch workspace (256-byte aligned): the K and V cache blocks of every sequence,
+// token / position / pick / key arrays, flags, attention partials, logits, the debug dump.
+bool batch_layout(const qw_config &c, int max_batch, int max_ctx, BatchLayout *L) {
+    const size_t esz = c.kv_format == QW_KV_F32 ? 4 : 2;
+    const size_t block = (size_t)c.n_layers * c.n_kv_heads * max_ctx * c.head_dim * esz;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    L->kc = take(block * max_batch);
+    L->vc = take(block * max_batch);
+    L->small = take(5 * qw::kBatchMax * 8);
+    L->flags = take(sizeof(qw::StepFlags));
+    L->part = take((size_t)max_batch * c.n_heads * qw::kBatchMaxSplits * qw::kBatchPartStride * 4);
+    L->logits = take((size_t)max_batch * c.vocab * 4);
+    L->hidden = take((size_t)(c.n_layers + 1) * max_batch * c.hidden * 4);
+    L->total = off;
+    return true;
+}
+
+int batch_read(qw_batch *b, int32_t *picks_host, int n) {
+    qw::StepFlags f;
+    int rc = cuda_status(cudaMemcpyAsync(&f, b->flags, sizeof(f), cudaMemcpyDeviceToHost, b->m->stream));
+    if (!rc && picks_host)
+        rc = cuda_status(cudaMemcpyAsync(picks_host, b->picks, (size_t)n * 4, cudaMemcpyDeviceToHost, b->m->stream));
+    if (!rc) rc = cuda_status(cudaStreamSynchronize(b->m->stream));
+    if (rc) return rc;
+    if (f.err) {
+        b->failed = (int)f.err;
+        return (int)f.err;
+    }
+    return QW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qw_batch_workspace_bytes(const qw_model *m, int32_t max_batch, int32_t max_ctx) {
+    if (!live(m) || max_batch < 1 || max_batch > qw::kBatchMax || max_ctx < 1 || max_ctx > m->cfg.max_ctx) return 0;
+    BatchLayout L;
+    batch_layout(m->cfg, max_batch, max_ctx, &L);
+    return L.total;
+}
+
+int qw_batch_create(qw_model *m, int32_t max_batch, int32_t max_ctx, void *workspace_dev, size_t workspace_bytes,
+                    qw_batch **out) {
+    if (!out) return QW_INVALID_ARGUMENT;
+    *out = nullptr;
+    if (!live(m)) return QW_INVALID_HANDLE;
+    if (max_batch < 1 || max_batch > qw::kBatchMax || max_ctx < 1 || max_ctx > m->cfg.max_ctx)
+        return QW_INVALID_ARGUMENT;
+    if (!qw::prefill_supported(m->pf) || max_batch > m->pf.rows_max || m->cfg.n_heads != qw::kBatchG * m->cfg.n_kv_heads)
+        return QW_UNSUPPORTED_SHAPE;
+    if (!aligned(workspace_dev, 256)) return QW_ALIGNMENT;
+    BatchLayout L;
+    batch_layout(m->cfg, max_batch, max_ctx, &L);
+    if (workspace_bytes < L.total) return QW_OUT_OF_MEMORY;
+    qw_batch *b = new (std::nothrow) qw_batch();
+    if (!b) return QW_OUT_OF_MEMORY;
+    uint8_t *ws = (uint8_t *)workspace_dev;
+    b->m = m;
+    b->max_batch = max_batch;
+    b->max_ctx = max_ctx;
+    b->seq_elems = (size_t)m->cfg.n_layers * m->cfg.n_kv_heads * max_ctx * m->cfg.head_dim;
+    b->kc = ws + L.kc;
+    b->vc = ws + L.vc;
+    b->tok_in = (int32_t *)(ws + L.small);
+    b->tok = b->tok_in + qw::kBatchMax;
+    b->picks = b->tok + qw::kBatchMax;
+    b->row_pos = (int *)(b->picks + qw::kBatchMax);
+    b->keys = (unsigned long long *)(ws + L.small + 4 * qw::kBatchMax * 4 + 64);
+    b->flags = (qw::StepFlags *)(ws + L.flags);
+    b->part = (float *)(ws + L.part);
+    b->logits = (float *)(ws + L.logits);
+    b->hidden = (float *)(ws + L.hidden);
+    b->len.assign(max_batch, 0);
+    b->has_last.assign(max_batch, 0);
+    int rc = cuda_status(cudaMemsetAsync(ws + L.small, 0, L.part - L.small, m->stream));
+    if (!rc) rc = cuda_status(cudaStreamSynchronize(m->stream));
+    if (!rc) rc = cuda_status(cudaStreamCreateWithFlags(&b->cap, cudaStreamNonBlocking));
+    if (rc) {
+        delete b;
+        return rc;
+    }
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        g_live_batch.insert(b);
+    }
+    *out = b;
+    return QW_OK;
+}
+
+void qw_batch_destroy(qw_batch *b) {
+    bool model_live;
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        if (!g_live_batch.erase(b)) return;
+        model_live = g_live.count(b->m) != 0;
+    }
+    if (model_live) cudaStreamSynchronize(b->m->stream);
+    for (auto &g : b->graphs) cudaGraphExecDestroy(g.exec);
+    if (b->cap) cudaStreamDestroy(b->cap);
+    delete b;
+}
+
+int qw_batch_reset(qw_batch *b, int32_t seq) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    if (seq < -1 || seq >= b->max_batch) return QW_INVALID_ARGUMENT;
+    for (int s = 0; s < b->max_batch; ++s)
+        if (seq == -1 || s == seq) {
+            b->len[s] = 0;
+            b->has_last[s] = 0;
+        }
+    if (seq == -1) {
+        b->failed = 0;
+        return cuda_status(cudaMemsetAsync(b->flags, 0, sizeof(qw::StepFlags), b->m->stream));
+    }
+    return QW_OK;
+}
+
+int qw_batch_length(const qw_batch *b, int32_t seq, int32_t *out) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    if (!out || seq < 0 || seq >= b->max_batch) return QW_INVALID_ARGUMENT;
+    *out = b->len[seq];
+    return QW_OK;
+}
+
+int qw_batch_prefill(qw_batch *b, int32_t seq, const int32_t *tokens_host, int32_t n, int32_t *next_token_host) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    if (b->failed) return b->failed;
+    qw_model *m = b->m;
+    if (seq < 0 || seq >= b->max_batch || n < 1 || !tokens_host) return QW_INVALID_ARGUMENT;
+    if ((int64_t)b->len[seq] + n > b->max_ctx) return QW_CONTEXT_EXCEEDED;
+    for (int32_t i = 0; i < n; ++i)
+        if (tokens_host[i] < 0 || tokens_host[i] >= m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    qw::DecodeArgs a = m->args;  // the model's weights and RoPE table; this sequence's cache
+    const size_t esz = m->cfg.kv_format == QW_KV_F32 ? 4 : 2;
+    a.kc = b->kc + (size_t)seq * b->seq_elems * esz;
+    a.vc = b->vc + (size_t)seq * b->seq_elems * esz;
+    a.max_ctx = b->max_ctx;
+    a.logits = b->logits + (size_t)seq * m->cfg.vocab;
+    a.flags = b->flags;
+    if (qw::prefill_run(&m->pf, a, b->len[seq], tokens_host, n, 0, m->stream)) return QW_CUDA_ERROR;
+    b->len[seq] += n;
+    b->has_last[seq] = 1;
+    int rc = cuda_status(cudaMemcpyAsync(b->picks + seq, &b->flags->next_tok, 4, cudaMemcpyDeviceToDevice, m->stream));
+    if (rc) return rc;
+    if (next_token_host) {
+        rc = batch_read(b, nullptr, 0);
+        if (rc) return rc;
+        return cuda_status(cudaMemcpy(next_token_host, b->picks + seq, 4, cudaMemcpyDeviceToHost));
+    }
+    return QW_OK;
+}
+
+int qw_batch_step(qw_batch *b, int32_t n_seq, const int32_t *tokens_host, int32_t *next_tokens_host) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    if (b->failed) return b->failed;
+    qw_model *m = b->m;
+    if (n_seq < 1 || n_seq > b->max_batch) return QW_INVALID_ARGUMENT;
+    int32_t tok[qw::kBatchMax];
+    int pos[qw::kBatchMax];
+    int max_n = 0;
+    for (int s = 0; s < n_seq; ++s) {
+        tok[s] = tokens_host ? tokens_host[s] : -1;
+        if (tok[s] < -1 || tok[s] >= m->cfg.vocab) return QW_INVALID_ARGUMENT;
+        if (tok[s] == -1 && !b->has_last[s]) return QW_INVALID_ARGUMENT;
+        if (b->len[s] + 1 > b->max_ctx) return QW_CONTEXT_EXCEEDED;
+        pos[s] = b->len[s];
+        max_n = pos[s] + 1 > max_n ? pos[s] + 1 : max_n;
+    }
+    int rc = cuda_status(cudaMemcpyAsync(b->tok_in, tok, (size_t)n_seq * 4, cudaMemcpyHostToDevice, m->stream));
+    if (!rc) rc = cuda_status(cudaMemcpyAsync(b->row_pos, pos, (size_t)n_seq * 4, cudaMemcpyHostToDevice, m->stream));
+    if (rc) return rc;
+    qw::BatchStep bs{};
+    bs.B = n_seq;
+    bs.tokens_in = b->tok_in;
+    bs.tokens = b->tok;
+    bs.row_pos = b->row_pos;
+    bs.max_n = max_n;
+    bs.kc = b->kc;
+    bs.vc = b->vc;
+    bs.seq_elems = b->seq_elems;
+    bs.max_ctx = b->max_ctx;
+    bs.part = b->part;
+    bs.logits = b->logits;
+    bs.keys = b->keys;
+    bs.picks = b->picks;
+    bs.hidden = (m->debug & QW_DEBUG_HIDDEN) ? b->hidden : nullptr;
+    qw::DecodeArgs a = m->args;
+    a.flags = b->flags;
+    const int S = qw::batch_splits(max_n), hid = bs.hidden != nullptr;
+    cudaGraphExec_t exec = nullptr;
+    for (auto &g : b->graphs)
+        if (g.B == n_seq && g.S == S && g.hidden == hid) exec = g.exec;
+    if (!exec) {  // capture this combination's launches once
+        if (cuda_status(cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeThreadLocal))) return QW_CUDA_ERROR;
+        const int frc = qw::prefill_batch_step(&m->pf, a, bs, b->cap);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t ce = cudaStreamEndCapture(b->cap, &graph);
+        if (frc || ce != cudaSuccess || !graph) {
+            if (graph) cudaGraphDestroy(graph);
+            cudaGetLastError();
+            return QW_CUDA_ERROR;
+        }
+        const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (ie != cudaSuccess) return cuda_status(ie);
+        b->graphs.push_back({n_seq, S, hid, exec});
+    }
+    rc = cuda_status(cudaGraphLaunch(exec, m->stream));
+    if (rc) return rc;
+    for (int s = 0; s < n_seq; ++s) {
+        b->len[s] += 1;
+        b->has_last[s] = 1;
+    }
+    b->last_n = n_seq;
+    if (next_tokens_host) return batch_read(b, next_tokens_host, n_seq);
+    return QW_OK;
+}
+
+int qw_batch_logits(qw_batch *b, float *dst_dev, int64_t n) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    if (!dst_dev || b->last_n == 0 || n != (int64_t)b->last_n * b->m->cfg.vocab) return QW_INVALID_ARGUMENT;
+    return cuda_status(
+        cudaMemcpyAsync(dst_dev, b->logits, (size_t)n * 4, cudaMemcpyDeviceToDevice, b->m->stream));
+}
+
+int qw_batch_debug_hidden(qw_batch *b, float *dst_dev, int64_t n) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    const qw_config &c = b->m->cfg;
+    if (!dst_dev || b->last_n == 0 || n != (int64_t)(c.n_layers + 1) * b->last_n * c.hidden) return QW_INVALID_ARGUMENT;
+    return cuda_status(
+        cudaMemcpyAsync(dst_dev, b->hidden, (size_t)n * 4, cudaMemcpyDeviceToDevice, b->m->stream));
+}
+
+int qw_batch_sync(qw_batch *b) {
+    if (!live_batch(b)) return QW_INVALID_HANDLE;
+    return batch_read(b, nullptr, 0);
 }
 
 }  // extern "C"

@@ -1,0 +1,52 @@
+// qw_batch.h - batched decode: B sequences, one new token each per step.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qw_internal.h"
+
+namespace qw {
+
+constexpr int kBatchMax = 8;            // sequences per batched step
+constexpr int kBatchG = 2;              // query heads per KV head (the Qwen3-0.6B block)
+constexpr int kBatchPartStride = 132;   // floats per attention partial: acc[128], max, sum, pad
+constexpr int kBatchHeadThreads = 256;
+constexpr int kBatchSplitRows = 128;    // cached positions per attention split (at most)
+constexpr int kBatchMaxSplits = 64;
+
+struct BatchAttn {
+    const __half *q16;    // [Hq][q_rows][128]: row b = sequence b's rotated query heads
+    int q_rows;
+    const void *kc, *vc;  // this layer's planes of sequence 0: [Hkv][max_ctx][128] (f32 or bf16)
+    size_t seq_elems;     // elements from one sequence's cache to the next one's
+    int max_ctx;
+    const int *row_pos;   // [B] this step's position of each sequence (its row is cached already)
+    int S, Hq;            // splits per (sequence, KV head); query heads
+    float scale_log2;     // log2(e) / sqrt(head_dim)
+    float *part;          // [B][Hq][S][kBatchPartStride]
+};
+
+struct BatchHead {
+    const float *x;                 // [B][H] residual stream after the last layer
+    const __nv_bfloat16 *final_norm, *E;
+    int B, V;
+    float eps;
+    float *logits;                  // [B][V]
+    unsigned long long *keys;       // [B] packed argmax keys, zero on entry (left zero)
+    int32_t *picks;                 // [B] greedy picks out
+    StepFlags *flags;
+};
+
+cudaError_t batch_prepare();
+cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st);
+cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st);
+cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *o16, int ldo, cudaStream_t st);
+cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st);
+
+// Splits per (sequence, KV head) for a step whose longest sequence caches n positions.
+inline int batch_splits(int n) {
+    int s = (n + kBatchSplitRows - 1) / kBatchSplitRows;
+    return s < 1 ? 1 : s > kBatchMaxSplits ? kBatchMaxSplits : s;
+}
+
+}  // namespace qw

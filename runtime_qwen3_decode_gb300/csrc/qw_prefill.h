@@ -31,6 +31,28 @@ inline bool prefill_supported(const PrefillState &st) { return st.ready != 0; }
 // (flags->next_tok); debug bit 1 dumps the last row's hidden state after every layer.
 int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *tokens_host, int n, int debug,
                 cudaStream_t stream);
+// One batched decode step: B sequences, one new token each (their tokens resolved on the device:
+// -1 takes the sequence's previous pick).  Sequence b's cache is the block of seq_elems elements
+// starting seq_elems * b after kc / vc ([L][Hkv][max_ctx][128]); its new row goes to position
+// row_pos[b].  The B rows run through the tensor-core GEMMs of the prefill (M = B) and the
+// batched attention and head kernels of batch.cu; logits [B][V] and picks [B] come out.
+struct BatchStep {
+    int B;
+    const int32_t *tokens_in;  // device [B]: token or -1
+    int32_t *tokens;           // device [B] scratch: the resolved tokens
+    const int *row_pos;        // device [B]
+    int max_n;                 // the longest sequence's cached positions after this step's row
+    void *kc, *vc;
+    size_t seq_elems;
+    int max_ctx;
+    float *part;               // attention partials [B][Hq][splits][132]
+    float *logits;             // [B][V]
+    unsigned long long *keys;  // [B], zero
+    int32_t *picks;            // [B] in (previous picks) and out
+    float *hidden;             // optional [L + 1][B][H] residual stream dump
+};
+int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &bs, cudaStream_t stream);
+
 // C = A B^T with fp16 A [M,K], B [N,K] and f32 C [M,N] through the tensor-core GEMM (tests).
 int prefill_debug_gemm(const void *a, const void *b, float *c, int M, int N, int K, int bn, cudaStream_t stream);
 

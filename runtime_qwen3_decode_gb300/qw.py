@@ -53,7 +53,10 @@ EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_ste
            "qw_kv_reset", "qw_kv_length", "qw_sync", "qw_model_destroy", "qw_kv_import", "qw_kv_export",
            "qw_set_debug", "qw_debug_hidden", "qw_status_string", "qw_abi_version", "qw_debug_trace", "qw_query",
            "qw_decode_step_noalloc", "qw_debug_gemm_f16", "qw_sample_scratch_bytes", "qw_sample_logits",
-           "qw_sampler_seed", "qw_sampler_state", "qw_sample")
+           "qw_sampler_seed", "qw_sampler_state", "qw_sample", "qw_batch_workspace_bytes", "qw_batch_create",
+           "qw_batch_destroy", "qw_batch_reset", "qw_batch_length", "qw_batch_prefill", "qw_batch_step",
+           "qw_batch_logits", "qw_batch_debug_hidden", "qw_batch_sync")
+BATCH_MAX = 8
 
 
 class QwError(RuntimeError):
@@ -129,6 +132,18 @@ def _lib():
             L.qw_sampler_seed.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64]
             L.qw_sampler_state.argtypes = [vp, vp]
             L.qw_sample.argtypes = [vp, ctypes.POINTER(Sampling), vp, i32, vp]
+            L.qw_batch_workspace_bytes.argtypes = [vp, i32, i32]
+            L.qw_batch_workspace_bytes.restype = ctypes.c_size_t
+            L.qw_batch_create.argtypes = [vp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]
+            L.qw_batch_destroy.argtypes = [vp]
+            L.qw_batch_destroy.restype = None
+            L.qw_batch_reset.argtypes = [vp, i32]
+            L.qw_batch_length.argtypes = [vp, i32, i32p]
+            L.qw_batch_prefill.argtypes = [vp, i32, i32p, i32, i32p]
+            L.qw_batch_step.argtypes = [vp, i32, i32p, i32p]
+            L.qw_batch_logits.argtypes = [vp, vp, i64]
+            L.qw_batch_debug_hidden.argtypes = [vp, vp, i64]
+            L.qw_batch_sync.argtypes = [vp]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -402,3 +417,77 @@ class Model:
         out = torch.empty((c.n_layers + 1, c.hidden), dtype=torch.float32, device="cuda")
         _check(_lib().qw_debug_hidden(self._h, out.data_ptr(), out.numel()), "qw_debug_hidden")
         return out
+
+
+class Batch:
+    """Up to BATCH_MAX sequences of one Model decoded together (qw_batch_*), each with its own
+    K/V cache and length; workspace from torch on the model's device."""
+
+    def __init__(self, model: "Model", max_batch: int, max_ctx: int):
+        import torch
+
+        self.model = model
+        self.max_batch = max_batch
+        self.max_ctx = max_ctx
+        n = _lib().qw_batch_workspace_bytes(model._h, max_batch, max_ctx)
+        if n == 0:
+            raise QwError(INVALID_ARGUMENT, "qw_batch_workspace_bytes")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device="cuda")
+        h = ctypes.c_void_p()
+        _check(_lib().qw_batch_create(model._h, max_batch, max_ctx, self.workspace.data_ptr(), n, ctypes.byref(h)),
+               "qw_batch_create")
+        self._h = h
+        self.last_n = 0
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().qw_batch_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, seq: int = -1):
+        _check(_lib().qw_batch_reset(self._h, seq), "qw_batch_reset")
+
+    def length(self, seq: int) -> int:
+        out = ctypes.c_int32()
+        _check(_lib().qw_batch_length(self._h, seq, ctypes.byref(out)), "qw_batch_length")
+        return out.value
+
+    def prefill(self, seq: int, tokens, want_token: bool = True):
+        t = (ctypes.c_int32 * len(tokens))(*[int(x) for x in tokens])
+        out = ctypes.c_int32(-1)
+        _check(_lib().qw_batch_prefill(self._h, seq, t, len(tokens), ctypes.byref(out) if want_token else None),
+               "qw_batch_prefill")
+        return out.value if want_token else None
+
+    def step(self, n_seq: int, tokens=None, want_tokens: bool = True):
+        """One step of sequences 0..n_seq-1; tokens None (or -1 entries) = each one's last pick."""
+        t = None if tokens is None else (ctypes.c_int32 * n_seq)(*[int(x) for x in tokens])
+        out = (ctypes.c_int32 * n_seq)()
+        _check(_lib().qw_batch_step(self._h, n_seq, t, out if want_tokens else None), "qw_batch_step")
+        self.last_n = n_seq
+        return list(out) if want_tokens else None
+
+    def logits(self):
+        import torch
+
+        V = self.model.cfg.vocab
+        out = torch.empty((self.last_n, V), dtype=torch.float32, device="cuda")
+        _check(_lib().qw_batch_logits(self._h, out.data_ptr(), out.numel()), "qw_batch_logits")
+        return out
+
+    def debug_hidden(self):
+        import torch
+
+        c = self.model.cfg
+        out = torch.empty((c.n_layers + 1, self.last_n, c.hidden), dtype=torch.float32, device="cuda")
+        _check(_lib().qw_batch_debug_hidden(self._h, out.data_ptr(), out.numel()), "qw_batch_debug_hidden")
+        return out
+
+    def sync(self):
+        _check(_lib().qw_batch_sync(self._h), "qw_batch_sync")
