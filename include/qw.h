@@ -256,6 +256,76 @@ int qw_batch_debug_hidden(qw_batch *b, float *dst_dev, int64_t n);
 /* Wait for the batch's work; returns a recorded device error. */
 int qw_batch_sync(qw_batch *b);
 
+/* -------------------------------------------------------- checkpoint files */
+
+/*
+ * Safetensors / SLM2 checkpoints ("Scalar-Native Qwen3 Reference Runtime As The
+ * Numerical Authority", section 3 "File Layout and Safe Metadata Parsing"; "M1 - Load
+ * the weights", sections "The loading stack" and "The safetensors format"):
+ * [u64 little-endian N][N bytes of UTF-8 JSON][blob].  The JSON maps each tensor name
+ * to {"dtype", "shape", "data_offsets": [begin, end]} (offsets into the blob), plus an
+ * optional "__metadata__" object of strings.  dtypes: "BF16", "F16", "F32", "I8" and
+ * "Q8_0" (SLM2's 34-byte blocks: an fp16 scale, then 32 int8 codes).
+ *
+ * qw_checkpoint_open parses and validates the header of a file held in host memory
+ * (mapped or read by the caller; borrowed until qw_checkpoint_close).  bytes_len may
+ * cover only the prefix and header (then the checks run but nothing is uploaded);
+ * file_size is the whole file's size.  Every entry must satisfy, else
+ * QW_INVALID_ARGUMENT with the reason in qw_checkpoint_last_error(): end <= blob size;
+ * spans sorted by begin do not overlap; 8 + N + begin is a multiple of 8;
+ * end - begin == the bytes of shape x dtype; a Q8_0 tensor holds whole 32-element
+ * blocks; no duplicate names, unknown keys or dtypes, rank <= 4, nothing after the
+ * header object.
+ */
+typedef struct qw_checkpoint qw_checkpoint;
+enum qw_dtype { QW_DT_BF16 = 0, QW_DT_F16 = 1, QW_DT_F32 = 2, QW_DT_I8 = 3, QW_DT_Q8_0 = 4 };
+
+int qw_checkpoint_open(const void *bytes, uint64_t bytes_len, uint64_t file_size, qw_checkpoint **out);
+void qw_checkpoint_close(qw_checkpoint *c);
+/* Reason of the last failed qw_checkpoint_* call of this thread ("" after a success). */
+const char *qw_checkpoint_last_error(void);
+/* Tensors in the file (-1 for an invalid handle); entry i (sorted by begin): name
+ * (NUL-terminated, name_cap bytes available), dtype, rank, dims [4] (0-padded), blob
+ * offsets.  Any output pointer may be NULL. */
+int32_t qw_checkpoint_count(const qw_checkpoint *c);
+int qw_checkpoint_tensor(const qw_checkpoint *c, int32_t i, char *name, int32_t name_cap, int32_t *dtype,
+                         int32_t *rank, int64_t *dims, uint64_t *begin, uint64_t *end);
+
+/*
+ * Cross-check against the tensor set cfg implies ("M1 - Load the weights", section
+ * "Deriving what should be there"): model.embed_tokens.weight [V,H],
+ * model.norm.weight [H], an optional lm_head.weight [V,H] (a tied head may be absent or
+ * shipped as a copy), and per layer input_layernorm [H], self_attn.{q,k,v}_proj
+ * [n_heads*d or n_kv_heads*d, H], self_attn.{q,k}_norm [d], self_attn.o_proj
+ * [H, n_heads*d], post_attention_layernorm [H], mlp.{gate,up}_proj [I,H],
+ * mlp.down_proj [H,I].  Loadable dtypes: BF16 or F32 norm vectors, BF16 embedding and
+ * head, and BF16 (QW_W_BF16) or Q8_0 (QW_W_INT8_G32) matrices.  Parameter counts:
+ * stored = every tensor of the file; logical = a shipped head copy not counted.
+ * Returns QW_OK when clean, QW_UNSUPPORTED_SHAPE when a tensor is missing, mis-shaped,
+ * unexpected or of an unloadable dtype (the first such problem in first_problem).
+ */
+typedef struct {
+    int32_t n_tensors, n_expected, n_found, n_missing, n_misshaped, n_unexpected, n_bad_dtype;
+    int32_t lm_head_copy;
+    int64_t stored_params, logical_params, embedding_params;
+    char first_problem[256];
+} qw_checkpoint_report;
+int qw_checkpoint_check(const qw_checkpoint *c, const qw_config *cfg, qw_checkpoint_report *report);
+
+/*
+ * Device bytes qw_checkpoint_upload needs (0 on error).  The upload copies every tensor
+ * of a clean checkpoint (with its blob in memory) into dst_dev (256-byte aligned): the
+ * embedding, the final norm, a head only if it differs from the embedding (a byte-equal
+ * copy is tied), and per layer the four norm vectors (F32 ones must be exactly
+ * representable in bf16, else QW_UNSUPPORTED_QUANTIZATION) and the seven matrices
+ * (BF16 as stored; Q8_0 split into int8 codes [out, in] and fp16 scales [out, in/32],
+ * the same values).  It fills layers (a host array of n_layers entries) and *table for
+ * qw_model_create, and synchronises cuda_stream before returning.
+ */
+size_t qw_checkpoint_upload_bytes(const qw_checkpoint *c, const qw_config *cfg);
+int qw_checkpoint_upload(const qw_checkpoint *c, const qw_config *cfg, void *dst_dev, size_t dst_bytes,
+                         qw_layer_weights *layers, qw_weights *table, void *cuda_stream);
+
 /* ---------------------------------------------------------------- testing */
 
 /*

@@ -55,8 +55,19 @@ EXPORTS = ("qw_workspace_bytes", "qw_model_create", "qw_prefill", "qw_decode_ste
            "qw_decode_step_noalloc", "qw_debug_gemm_f16", "qw_sample_scratch_bytes", "qw_sample_logits",
            "qw_sampler_seed", "qw_sampler_state", "qw_sample", "qw_batch_workspace_bytes", "qw_batch_create",
            "qw_batch_destroy", "qw_batch_reset", "qw_batch_length", "qw_batch_prefill", "qw_batch_step",
-           "qw_batch_logits", "qw_batch_debug_hidden", "qw_batch_sync")
+           "qw_batch_logits", "qw_batch_debug_hidden", "qw_batch_sync", "qw_checkpoint_open",
+           "qw_checkpoint_close", "qw_checkpoint_last_error", "qw_checkpoint_count", "qw_checkpoint_tensor",
+           "qw_checkpoint_check", "qw_checkpoint_upload_bytes", "qw_checkpoint_upload")
+DT_BF16, DT_F16, DT_F32, DT_I8, DT_Q8_0 = 0, 1, 2, 3, 4
 BATCH_MAX = 8
+
+
+class CheckpointReport(ctypes.Structure):
+    _fields_ = [("n_tensors", ctypes.c_int32), ("n_expected", ctypes.c_int32), ("n_found", ctypes.c_int32),
+                ("n_missing", ctypes.c_int32), ("n_misshaped", ctypes.c_int32), ("n_unexpected", ctypes.c_int32),
+                ("n_bad_dtype", ctypes.c_int32), ("lm_head_copy", ctypes.c_int32), ("stored_params", ctypes.c_int64),
+                ("logical_params", ctypes.c_int64), ("embedding_params", ctypes.c_int64),
+                ("first_problem", ctypes.c_char * 256)]
 
 
 class QwError(RuntimeError):
@@ -144,6 +155,22 @@ def _lib():
             L.qw_batch_logits.argtypes = [vp, vp, i64]
             L.qw_batch_debug_hidden.argtypes = [vp, vp, i64]
             L.qw_batch_sync.argtypes = [vp]
+            u64 = ctypes.c_uint64
+            L.qw_checkpoint_open.argtypes = [vp, u64, u64, ctypes.POINTER(ctypes.c_void_p)]
+            L.qw_checkpoint_close.argtypes = [vp]
+            L.qw_checkpoint_close.restype = None
+            L.qw_checkpoint_last_error.argtypes = []
+            L.qw_checkpoint_last_error.restype = ctypes.c_char_p
+            L.qw_checkpoint_count.argtypes = [vp]
+            L.qw_checkpoint_count.restype = i32
+            L.qw_checkpoint_tensor.argtypes = [vp, i32, ctypes.c_char_p, i32, i32p, i32p,
+                                               ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(u64),
+                                               ctypes.POINTER(u64)]
+            L.qw_checkpoint_check.argtypes = [vp, ctypes.POINTER(Config), ctypes.POINTER(CheckpointReport)]
+            L.qw_checkpoint_upload_bytes.argtypes = [vp, ctypes.POINTER(Config)]
+            L.qw_checkpoint_upload_bytes.restype = ctypes.c_size_t
+            L.qw_checkpoint_upload.argtypes = [vp, ctypes.POINTER(Config), vp, ctypes.c_size_t,
+                                               ctypes.POINTER(LayerWeights), ctypes.POINTER(Weights), vp]
             L.qw_status_string.argtypes = [ctypes.c_int]
             L.qw_status_string.restype = ctypes.c_char_p
             L.qw_abi_version.argtypes = []
@@ -279,7 +306,9 @@ def sample_logits(logits, params: Sampling, rng, token_out, history=None, scratc
 class Model:
     """One decoder instance on the current CUDA device and stream."""
 
-    def __init__(self, dims, dev_weights: dict, max_ctx: int | None = None, stream=None):
+    def __init__(self, dims, dev_weights: dict | None, max_ctx: int | None = None, stream=None, table=None):
+        """dev_weights: device tensors from weights_to_device; or table = (keep-alive object,
+        Weights, layer array) as Checkpoint.upload returns it."""
         import torch
 
         self.dims = dims
@@ -288,9 +317,16 @@ class Model:
         nbytes = workspace_bytes(self.cfg)
         if nbytes == 0:
             raise QwError(UNSUPPORTED_SHAPE, "workspace_bytes")
-        self._w = dev_weights
+        self._w = dev_weights if table is None else table
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         self.stream = stream if stream is not None else torch.cuda.current_stream()
+        if table is not None:
+            self._layers = table[2]
+            h = ctypes.c_void_p()
+            _check(_lib().qw_model_create(ctypes.byref(self.cfg), ctypes.byref(table[1]), self.workspace.data_ptr(),
+                                          nbytes, self.stream.cuda_stream, ctypes.byref(h)), "qw_model_create")
+            self._h = h
+            return
         layers = (LayerWeights * self.cfg.n_layers)()
         for l, lw in enumerate(dev_weights["layers"]):
             L = layers[l]
@@ -491,3 +527,64 @@ class Batch:
 
     def sync(self):
         _check(_lib().qw_batch_sync(self._h), "qw_batch_sync")
+
+
+class Checkpoint:
+    """A safetensors / SLM2 checkpoint held in host memory (qw_checkpoint_*): `data` is the file's
+    bytes (or only its prefix and header, with file_size the whole file's size)."""
+
+    def __init__(self, data, file_size: int | None = None):
+        self._buf = bytes(data) if not isinstance(data, (bytes, bytearray)) else data
+        self._c = ctypes.create_string_buffer(bytes(self._buf), len(self._buf))
+        size = len(self._buf) if file_size is None else file_size
+        h = ctypes.c_void_p()
+        rc = _lib().qw_checkpoint_open(ctypes.cast(self._c, ctypes.c_void_p), len(self._buf), size, ctypes.byref(h))
+        if rc != OK:
+            raise QwError(rc, "qw_checkpoint_open: " + _lib().qw_checkpoint_last_error().decode())
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().qw_checkpoint_close(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def tensors(self):
+        """[(name, dtype, shape, begin, end)] sorted by begin."""
+        out = []
+        for i in range(_lib().qw_checkpoint_count(self._h)):
+            name = ctypes.create_string_buffer(512)
+            dt, rk = ctypes.c_int32(), ctypes.c_int32()
+            dims = (ctypes.c_int64 * 4)()
+            b, e = ctypes.c_uint64(), ctypes.c_uint64()
+            _check(_lib().qw_checkpoint_tensor(self._h, i, name, 512, ctypes.byref(dt), ctypes.byref(rk), dims,
+                                               ctypes.byref(b), ctypes.byref(e)), "qw_checkpoint_tensor")
+            out.append((name.value.decode(), dt.value, tuple(dims[:rk.value]), b.value, e.value))
+        return out
+
+    def check(self, cfg: Config):
+        """(status, CheckpointReport): status OK when the file matches cfg's tensor set."""
+        rep = CheckpointReport()
+        rc = _lib().qw_checkpoint_check(self._h, ctypes.byref(cfg), ctypes.byref(rep))
+        return rc, rep
+
+    def upload(self, cfg: Config):
+        """Device copy of the weights in the layout qw_model_create takes: (workspace tensor, Weights, layers)."""
+        import torch
+
+        n = _lib().qw_checkpoint_upload_bytes(self._h, ctypes.byref(cfg))
+        if n == 0:
+            raise QwError(INVALID_ARGUMENT, "qw_checkpoint_upload_bytes")
+        buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+        layers = (LayerWeights * cfg.n_layers)()
+        table = Weights()
+        rc = _lib().qw_checkpoint_upload(self._h, ctypes.byref(cfg), buf.data_ptr(), n, layers, ctypes.byref(table),
+                                         torch.cuda.current_stream().cuda_stream)
+        if rc != OK:
+            raise QwError(rc, "qw_checkpoint_upload: " + _lib().qw_checkpoint_last_error().decode())
+        return buf, table, layers
