@@ -30,6 +30,7 @@ NUMERICAL_FAILURE = 18
 
 W_BF16 = 0
 W_INT8_G32 = 1
+W_Q8Q8 = 2
 MATRICES = ("q", "k", "v", "o", "gate", "up", "down")
 
 
@@ -81,6 +82,11 @@ def lib():
             L.ora_silu.argtypes = [ctypes.c_float]
             L.ora_silu.restype = ctypes.c_float
             L.ora_matvec.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, f32p, f32p, ctypes.c_int]
+            L.ora_f32_to_f16.argtypes = [ctypes.c_float]
+            L.ora_f32_to_f16.restype = ctypes.c_uint16
+            L.ora_quantize_q8_block.argtypes = [f32p, vp, vp]
+            L.ora_q8_block_dot.argtypes = [vp, vp]
+            L.ora_q8_block_dot.restype = ctypes.c_int32
             L.ora_rmsnorm.argtypes = [f32p, vp, ctypes.c_int, ctypes.c_float, f32p]
             L.ora_rope_angles.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, f32p, f32p]
             L.ora_rope_apply.argtypes = [f32p, ctypes.c_int, f32p, f32p]
@@ -164,8 +170,9 @@ def attention_head(q, K, V) -> np.ndarray:
     return o
 
 
-def matvec(w, x, scales=None) -> np.ndarray:
-    """y = W x with W bf16 bits [rows, cols] (uint16) or int8 codes [rows, cols] + fp16 scales."""
+def matvec(w, x, scales=None, q8_act: bool = False) -> np.ndarray:
+    """y = W x with W bf16 bits [rows, cols] (uint16) or int8 codes [rows, cols] + fp16 scales;
+    q8_act: the input quantized per 32-element block first (the Q8 x Q8 format)."""
     x = _f32(x)
     rows, cols = w.shape
     y = np.empty(rows, np.float32)
@@ -175,10 +182,34 @@ def matvec(w, x, scales=None) -> np.ndarray:
     else:
         w = np.ascontiguousarray(w, dtype=np.int8)
         s = np.ascontiguousarray(scales, dtype=np.uint16)
-        rc = lib().ora_matvec(W_INT8_G32, w.ctypes.data, s.ctypes.data, rows, cols, _fp(x), _fp(y), 1)
+        rc = lib().ora_matvec(W_Q8Q8 if q8_act else W_INT8_G32, w.ctypes.data, s.ctypes.data, rows, cols, _fp(x),
+                              _fp(y), 1)
     if rc:
         raise OracleError(rc, "matvec")
     return y
+
+
+def f32_to_f16(v: float) -> int:
+    """binary32 -> binary16 bits, round to nearest even."""
+    return int(lib().ora_f32_to_f16(ctypes.c_float(v)))
+
+
+def quantize_q8_block(a):
+    """(int8 codes [32], fp16 scale bits) of one 32-element activation block (Q8 x Q8 format)."""
+    a = _f32(a)
+    if a.size != 32:
+        raise ValueError("a block has 32 elements")
+    q = np.empty(32, np.int8)
+    s = np.zeros(1, np.uint16)
+    lib().ora_quantize_q8_block(_fp(a), q.ctypes.data, s.ctypes.data)
+    return q, int(s[0])
+
+
+def q8_block_dot(w, a) -> int:
+    """i32 sum of the 32 products of two int8 blocks."""
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    return int(lib().ora_q8_block_dot(w.ctypes.data, a.ctypes.data))
 
 
 def argmax(logits) -> int:
@@ -228,6 +259,10 @@ class OracleModel:
         self.wl = wl
         self._w = weights  # keep the arrays alive
         fmt = W_INT8_G32 if wl.weight_format == "int8_g32" else W_BF16
+        if getattr(wl, "act_format", "f32") == "q8":
+            if fmt != W_INT8_G32:
+                raise ValueError("int8 activations need int8 g32 weights")
+            fmt = W_Q8Q8
         cfg = _Config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate, wl.vocab,
                       wl.rms_eps, wl.rope_theta, max_ctx or wl.max_ctx, fmt,
                       nthreads or max(1, os.cpu_count() or 1))
@@ -240,7 +275,7 @@ class OracleModel:
             L.k_norm = lw["k_norm"].ctypes.data
             L.post_norm = lw["post_norm"].ctypes.data
             for j, m in enumerate(MATRICES):
-                if fmt == W_INT8_G32:
+                if fmt != W_BF16:
                     L.w[j] = lw[m + "_q8"].ctypes.data
                     L.s[j] = lw[m + "_s"].ctypes.data
                 else:

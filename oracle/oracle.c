@@ -33,6 +33,15 @@
  *   attention    s_j = (q . k_j) * (1/sqrt(d)); m = max s; e_j = expf(s_j - m);
  *                z = sum e_j (j order); o = sum_j (e_j / z) v_j (j order)
  *   SiLU         silu(g) = g * (1 / (1 + expf(-g)));  a = silu(g) * u
+ *   Q8 x Q8      (weight format 2, "Real-Browser WASM Qwen3 Execution", section 5
+ *                "Q8_0 Mixed-Precision Matrix Multiplication": the f32 input of every
+ *                projection is quantized per 32-element block before the dot product):
+ *                d = amax / 127; q_i = clamp(round-half-away(a_i / d), -127, 127)
+ *                (all 0 when amax = 0); the block scale kept as fp16(d) (round to
+ *                nearest even).  Per row, per block b in order: isum = sum of the 32
+ *                products q_w q_a in i32 (|isum| <= 32 * 127 * 127 < 2^31, the
+ *                "Integer-overflow rule" of "Portable WebAssembly Runtime
+ *                Architecture"), acc += f32(isum) * (f32(s_w) * f32(s_a)).
  */
 #include <math.h>
 #include <pthread.h>
@@ -50,7 +59,7 @@ enum {
     ORA_NUMERICAL_FAILURE = 18,
 };
 
-enum { ORA_W_BF16 = 0, ORA_W_INT8_G32 = 1 };
+enum { ORA_W_BF16 = 0, ORA_W_INT8_G32 = 1, ORA_W_Q8Q8 = 2 };
 
 typedef struct {
     int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab;
@@ -66,12 +75,12 @@ enum { M_Q = 0, M_K, M_V, M_O, M_GATE, M_UP, M_DOWN, M_COUNT };
 
 typedef struct {
     const uint16_t *input_norm, *q_norm, *k_norm, *post_norm; /* bf16 */
-    const void *w[M_COUNT];       /* bf16 [out,in], or int8 [out,in] for ORA_W_INT8_G32 */
-    const uint16_t *s[M_COUNT];   /* fp16 [out, in/32] scales (int8 format only) */
+    const void *w[M_COUNT];       /* bf16 [out,in], or int8 [out,in] (ORA_W_INT8_G32, ORA_W_Q8Q8) */
+    const uint16_t *s[M_COUNT];   /* fp16 [out, in/32] scales (int8 formats only) */
 } ora_layer;
 
 typedef struct {
-    int fmt;             /* ORA_W_BF16 or ORA_W_INT8_G32 */
+    int fmt;             /* ORA_W_BF16, ORA_W_INT8_G32 or ORA_W_Q8Q8 */
     int rows, cols;
     const void *w;
     const uint16_t *s;
@@ -110,6 +119,55 @@ float ora_f16_to_f32(uint16_t h) {
         v = ldexpf((float)(1024u + m), (int)e - 25); /* (1 + m/1024) * 2^(e-15) */
     }
     return sign ? -v : v;
+}
+
+/* IEEE 754 binary32 -> binary16, round to nearest even (overflow to infinity, gradual
+ * underflow to subnormals). */
+uint16_t ora_f32_to_f16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    const uint32_t e = (u >> 23) & 0xffu, m = u & 0x7fffffu;
+    if (e == 0xffu) return (uint16_t)(sign | 0x7c00u | (m ? 0x200u : 0u));
+    const float a = fabsf(f);
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7c00u);  /* rounds past the largest finite half */
+    if (a < ldexpf(1.0f, -14)) {                          /* subnormal half: a multiple of 2^-24 */
+        const float t = a * ldexpf(1.0f, 24);               /* exact: a power-of-two scaling */
+        float r = rintf(t);                                 /* the default mode: nearest even */
+        return (uint16_t)(sign | (uint16_t)r);              /* r = 1024 becomes the smallest normal */
+    }
+    /* normal: keep 10 mantissa bits, round the 13 dropped ones to nearest even */
+    uint32_t he = e - 127 + 15, hm = m >> 13, rest = m & 0x1fffu;
+    if (rest > 0x1000u || (rest == 0x1000u && (hm & 1u))) {
+        hm += 1;
+        if (hm == 0x400u) {
+            hm = 0;
+            he += 1;
+        }
+    }
+    if (he >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (he << 10) | hm);
+}
+
+/* One 32-element activation block to int8 codes and its fp16 scale (the Q8 x Q8 reading above). */
+void ora_quantize_q8_block(const float *a, int8_t *q, uint16_t *scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) amax = fabsf(a[i]) > amax ? fabsf(a[i]) : amax;
+    const float d = amax / 127.0f;
+    for (int i = 0; i < 32; ++i) {
+        float v = d > 0.0f ? roundf(a[i] / d) : 0.0f;  /* roundf: halves away from zero */
+        if (v > 127.0f) v = 127.0f;
+        if (v < -127.0f) v = -127.0f;
+        q[i] = (int8_t)v;
+    }
+    *scale = ora_f32_to_f16(d);
+}
+
+/* Integer dot product of one block: sum of 32 int8 x int8 products in i32. */
+int32_t ora_q8_block_dot(const int8_t *w, const int8_t *a) {
+    int32_t s = 0;
+    for (int i = 0; i < 32; ++i) s += (int32_t)w[i] * (int32_t)a[i];
+    return s;
 }
 
 float ora_silu(float g) {
@@ -162,10 +220,18 @@ static void parallel_rows(int nthreads, int64_t n, row_fn fn, void *ctx) {
 
 /* ------------------------------------------------------------ dot rows */
 
-/* y = W[row,:] . x, accumulated sequentially over k (int8: act * (q * scale)). */
-static float mat_row_dot(const ora_mat *m, int64_t row, const float *x) {
+/* y = W[row,:] . x, accumulated sequentially over k (int8: act * (q * scale)); Q8 x Q8: block by
+ * block over the quantized input (xq codes, xs fp16 scales). */
+static float mat_row_dot(const ora_mat *m, int64_t row, const float *x, const int8_t *xq, const uint16_t *xs) {
     float acc = 0.0f;
-    if (m->fmt == ORA_W_BF16) {
+    if (m->fmt == ORA_W_Q8Q8) {
+        const int8_t *q = (const int8_t *)m->w + row * m->cols;
+        const uint16_t *s = m->s + row * (m->cols / 32);
+        for (int b = 0; b < m->cols / 32; ++b) {
+            const int32_t isum = ora_q8_block_dot(q + b * 32, xq + b * 32);
+            acc += (float)isum * (ora_f16_to_f32(s[b]) * ora_f16_to_f32(xs[b]));
+        }
+    } else if (m->fmt == ORA_W_BF16) {
         const uint16_t *w = (const uint16_t *)m->w + row * m->cols;
         for (int k = 0; k < m->cols; ++k) acc += x[k] * ora_bf16_to_f32(w[k]);
     } else {
@@ -187,25 +253,38 @@ typedef struct {
     const float *x;
     float *y;
     const float *residual; /* NULL or residual added as y = residual + dot */
+    const int8_t *xq;      /* Q8 x Q8: the quantized input */
+    const uint16_t *xs;
 } matvec_ctx;
 
 static void matvec_rows(void *p, int64_t b, int64_t e) {
     matvec_ctx *c = (matvec_ctx *)p;
     for (int64_t r = b; r < e; ++r) {
-        float d = mat_row_dot(c->m, r, c->x);
+        float d = mat_row_dot(c->m, r, c->x, c->xq, c->xs);
         c->y[r] = c->residual ? c->residual[r] + d : d;
     }
 }
 
 static void matvec(int nthreads, const ora_mat *m, const float *x, float *y, const float *residual) {
-    matvec_ctx c = {m, x, y, residual};
+    matvec_ctx c = {m, x, y, residual, NULL, NULL};
+    int8_t *xq = NULL;
+    uint16_t *xs = NULL;
+    if (m->fmt == ORA_W_Q8Q8) {  /* the input is quantized once, then every row reads it */
+        xq = (int8_t *)malloc((size_t)m->cols);
+        xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(m->cols / 32));
+        for (int b = 0; b < m->cols / 32; ++b) ora_quantize_q8_block(x + b * 32, xq + b * 32, xs + b);
+        c.xq = xq;
+        c.xs = xs;
+    }
     parallel_rows(nthreads, m->rows, matvec_rows, &c);
+    free(xq);
+    free(xs);
 }
 
 /* Exposed for tests: y[r] = W[r,:] . x for one bf16 or int8 matrix. */
 int ora_matvec(int fmt, const void *w, const uint16_t *s, int rows, int cols, const float *x, float *y,
                int nthreads) {
-    if (fmt == ORA_W_INT8_G32 && cols % 32) return ORA_UNSUPPORTED_QUANTIZATION;
+    if (fmt != ORA_W_BF16 && cols % 32) return ORA_UNSUPPORTED_QUANTIZATION;
     ora_mat m = {fmt, rows, cols, w, s};
     matvec(nthreads, &m, x, y, NULL);
     return ORA_OK;
@@ -328,10 +407,11 @@ static int check_config(const ora_config *c) {
         c->intermediate < 1 || c->vocab < 1 || c->max_ctx < 1)
         return ORA_INVALID_ARGUMENT;
     if (c->n_heads % c->n_kv_heads || c->head_dim % 2) return ORA_UNSUPPORTED_SHAPE;
-    if (c->weight_format == ORA_W_INT8_G32 &&
+    if (c->weight_format != ORA_W_BF16 &&
         (c->hidden % 32 || c->intermediate % 32 || (c->n_heads * c->head_dim) % 32))
         return ORA_UNSUPPORTED_QUANTIZATION;
-    if (c->weight_format != ORA_W_BF16 && c->weight_format != ORA_W_INT8_G32) return ORA_UNSUPPORTED_QUANTIZATION;
+    if (c->weight_format != ORA_W_BF16 && c->weight_format != ORA_W_INT8_G32 && c->weight_format != ORA_W_Q8Q8)
+        return ORA_UNSUPPORTED_QUANTIZATION;
     return ORA_OK;
 }
 

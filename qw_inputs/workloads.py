@@ -25,6 +25,7 @@ class Workload:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     weight_format: str = "bf16"      # "bf16" | "int8_g32"
+    act_format: str = "f32"          # "f32" | "q8": projection inputs quantized per 32-block (int8 weights)
     kv_format: str = "f32"           # K/V cache element type: "f32" (the reference's) | "bf16"
     prompt_len: int = 0              # prefill tokens
     kv_prefill: int = 0              # positions imported into the K/V cache instead of a prompt
