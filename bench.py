@@ -530,6 +530,10 @@ def run_ours(args, wl):
             sub = qi.WORKLOADS[name]
             if sub.name != wl.name:
                 line[key] = decode_sub(qw, sub, min(k_sub, sub.decode_steps - W), W, local)
+        # the int8 workload with int8 activations too (Q8 x Q8; its prompt runs through the decode path)
+        q8 = qi.WORKLOADS["qwen3_0p6b_int8"].with_(act_format="q8")
+        line["decode_q8q8"] = decode_sub(qw, q8, 248, W, local)
+        line["decode_q8q8"]["activations"] = "int8, per 32-element block, quantized in the kernel"
     if not args.no_extra and ws == 1:
         for B in (8,):
             line[f"decode_batch{B}"] = measure_batch(qw, qi.WORKLOADS["qwen3_0p6b_decode"], B, 64, W, local)

@@ -66,8 +66,15 @@ enum qw_status {
 /* Weight storage of the seven projection matrices (q, k, v, o, gate, up, down). */
 enum qw_weight_format {
     QW_W_BF16 = 0,      /* bf16 [out, in] row-major */
-    QW_W_INT8_G32 = 1   /* int8 codes [out, in] + fp16 scales [out, in/32]; w = f32(q) * f32(s)
+    QW_W_INT8_G32 = 1,  /* int8 codes [out, in] + fp16 scales [out, in/32]; w = f32(q) * f32(s)
                            ("Scalar-Native ...", section 3 "Mixed-Q8 Quantization Definition") */
+    QW_W_Q8Q8 = 2       /* weights as QW_W_INT8_G32; every projection's input is quantized per
+                           32-element block at run time (d = amax/127, codes round-half-away(a/d)
+                           clamped to +-127, scale fp16(d)) and each block contributes
+                           f32(i32 dot of the codes) * f32(s_w) * f32(s_a) ("Real-Browser WASM Qwen3
+                           Execution", section 5 "Q8_0 Mixed-Precision Matrix Multiplication").
+                           Prompts run through the decode path one token at a time; batches
+                           (qw_batch_*) are not available for this format. */
 };
 
 /*

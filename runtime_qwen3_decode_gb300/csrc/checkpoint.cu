@@ -278,7 +278,7 @@ size_t upload_bytes(const qw_config &c, bool head_copy) {
     size_t per = 2 * up256(H * 2) + 2 * up256(d * 2);
     for (const auto &m : mats) {
         const size_t e = m[0] * m[1];
-        per += c.weight_format == QW_W_INT8_G32 ? up256(e) + up256(e / 32 * 2) : up256(e * 2);
+        per += c.weight_format != QW_W_BF16 ? up256(e) + up256(e / 32 * 2) : up256(e * 2);
     }
     return n + per * c.n_layers;
 }
@@ -451,7 +451,7 @@ int qw_checkpoint_check(const qw_checkpoint *c, const qw_config *cfg, qw_checkpo
         }
         const bool vec = e.kind == 1, mat = e.kind == 2;
         const bool dt_ok = vec ? (t.dtype == QW_DT_BF16 || t.dtype == QW_DT_F32)
-                           : mat ? (cfg->weight_format == QW_W_INT8_G32 ? t.dtype == QW_DT_Q8_0 : t.dtype == QW_DT_BF16)
+                           : mat ? (cfg->weight_format != QW_W_BF16 ? t.dtype == QW_DT_Q8_0 : t.dtype == QW_DT_BF16)
                                  : t.dtype == QW_DT_BF16;
         if (!dt_ok) {
             r->n_bad_dtype += 1;

@@ -51,7 +51,7 @@ cudaError_t decode_prepare(int *blocks_per_sm) {
     const int bytes = (int)decode_smem_bytes();
     *blocks_per_sm = 1 << 30;
     for (int D = 1; D <= 2; ++D)
-    for (int fmt = 0; fmt < 2; ++fmt)
+    for (int fmt = 0; fmt < 3; ++fmt)
         for (int kv = 0; kv < 2; ++kv) {
             const void *fn = decode_fn(D, fmt, kv);
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

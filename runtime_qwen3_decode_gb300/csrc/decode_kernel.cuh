@@ -307,7 +307,7 @@ __device__ __forceinline__ Phase describe(const DecodeArgs &a, int ph, int g, in
         case T_DOWN: R = a.H; p.K = a.I / D; break;
         default: R = a.V; p.K = a.H; break;
     }
-    p.i8 = (p.type != T_LMHEAD) && a.fmt == 1;
+    p.i8 = (p.type != T_LMHEAD) && a.fmt != 0;  // int8 storage for both int8 formats
     const int bpr = (p.pair ? 2 : 1) * (p.i8 ? p.K + p.K / 16 : 2 * p.K);
     int fit = kSlotBytes / bpr;
     if (fit > 64) fit = 64;
@@ -629,6 +629,43 @@ __device__ __forceinline__ void piece_fma(const WPiece<I8> &wp, const float2 (&a
     for (int k = 0; k < 4; ++k) acc = __ffma2_rn(w[k], act[k], acc);
 }
 
+// Q8 x Q8 (weight format 2): the lane's 8 activation columns of one slice times mul, quantized
+// as part of their 32-column block (lanes 4j .. 4j + 3 of a slice share one): d = amax / 127,
+// codes round-half-away(a / d) clamped to +-127 (0 when amax is 0), the scale rounded to fp16;
+// lo / hi hold the codes of columns 0..3 / 4..7 as bytes, matching a weight piece's layout.
+struct QAct {
+    uint32_t lo, hi;
+    float d;
+};
+__device__ __forceinline__ QAct quant8(const float2 (&a)[4], float mul) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = a[k].x * mul;
+        v[2 * k + 1] = a[k].y * mul;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const float d = m / 127.0f;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float t = d > 0.f ? roundf(v[i] / d) : 0.f;  // halves away from zero
+        t = fminf(fmaxf(t, -127.f), 127.f);
+        w[i >> 2] |= ((uint32_t)(int)t & 0xffu) << (8 * (i & 3));
+    }
+    return QAct{w[0], w[1], __half2float(__float2half_rn(d))};
+}
+
+// acc += (integer dot of a weight piece with the lane's activation codes) * (s_w * s_a)
+__device__ __forceinline__ void piece_dot_q8(const WPiece<true> &wp, const QAct &qa, float &acc) {
+    const int isum = __dp4a((int)wp.v.x, (int)qa.lo, __dp4a((int)wp.v.y, (int)qa.hi, 0));
+    acc = fmaf((float)isum, __half2float(wp.s) * qa.d, acc);
+}
+
 __device__ __forceinline__ float warp_sum2(float2 v) {
     float s = v.x + v.y;
 #pragma unroll
@@ -785,9 +822,10 @@ __host__ __device__ constexpr int pow2_at_least(int n = 1) { return n >= N ? n :
 // reads the activation, runs the paired FMAs of all its rows and one transposed warp reduction
 // for all of them, and stores the results through precomputed addresses.  Rows beyond PR per
 // warp (only with fewer SMs than the block is laid out for) follow one at a time.
-template <int NP, bool I8, bool PAIR, int PR>
+template <int NP, int WF, bool PAIR, int PR>
 __device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0, unsigned out_tag, float scale,
                                           unsigned long long *tr) {
+    constexpr bool I8 = WF != 0, Q8A = WF == 2;
     constexpr int NR = PAIR ? 2 : 1;
     constexpr int NV = PR * NR;               // values a lane accumulates
     constexpr int RP = pow2_at_least<NV>();   // padded to a power of two for the reduction
@@ -825,6 +863,12 @@ __device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0
     float2 act[NP][4];
 #pragma unroll
     for (int s = 0; s < NP; ++s) load_slice(sm.u.vec, s, lane, act[s]);
+    QAct qa[Q8A ? NP : 1];
+    if constexpr (Q8A) {  // the normalised input quantized per block; the scale is inside the codes' d
+#pragma unroll
+        for (int s = 0; s < NP; ++s) qa[s] = quant8(act[s], scale);
+    }
+    const float oscale = Q8A ? 1.0f : scale;
     if (tr && ctid() == 0) tr[8] = clock64();
     {
         float v[RP];  // value q NR + r = this lane's part of row (q, r)
@@ -832,14 +876,21 @@ __device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0
         for (int q = 0; q < PR; ++q)
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                if constexpr (Q8A) {
+                    float acc = 0.f;
 #pragma unroll
-                for (int s = 0; s < NP; ++s) piece_fma<I8>(pre[q][r][s], act[s], acc[s & 1]);
-                v[q * NR + r] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                    for (int s = 0; s < NP; ++s) piece_dot_q8(pre[q][r][s], qa[s], acc);
+                    v[q * NR + r] = acc;
+                } else {
+                    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int s = 0; s < NP; ++s) piece_fma<I8>(pre[q][r][s], act[s], acc[s & 1]);
+                    v[q * NR + r] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                }
             }
 #pragma unroll
         for (int i = NV; i < RP; ++i) v[i] = 0.f;
-        const float t = warp_sum_many<RP>(v, lane) * scale;
+        const float t = warp_sum_many<RP>(v, lane) * oscale;
         const int vi = lane / LW;  // the value this lane now holds
         if constexpr (PAIR) {
             const float up = __shfl_xor_sync(0xffffffffu, t, LW);  // value vi + 1: the pair's up row
@@ -865,9 +916,10 @@ __device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0
             for (int s = 0; s < NP; ++s) {
                 WPiece<I8> wp;
                 wp.load(rp[r], sc[r], 32 * s + lane);
-                piece_fma<I8>(wp, act[s], acc[s & 1]);
+                if constexpr (Q8A) piece_dot_q8(wp, qa[s], acc[0].x);
+                else piece_fma<I8>(wp, act[s], acc[s & 1]);
             }
-            o[r] = warp_sum((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) * scale;
+            o[r] = warp_sum((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) * oscale;
         }
         if (lane == 0) {
             float val = o[0];
@@ -884,8 +936,9 @@ __device__ __forceinline__ void gemv_rows(const Phase &p, int kind, unsigned it0
 // of the activation.
 // Each (row, slice) dot product goes to sm.part; then one thread per row adds the F slices in
 // order and writes the row's tagged result (silu(gate) * up for gate/up pairs).
-template <bool I8, bool PAIR>
+template <int WF, bool PAIR>
 __device__ __forceinline__ void gemv_ksplit(const Phase &p, int kind, unsigned it0, unsigned out_tag) {
+    constexpr bool I8 = WF != 0, Q8A = WF == 2;
     constexpr int NR = PAIR ? 2 : 1;
     Smem &sm = smem();
     const int warp = cwarp(), lane = clane(), tid = ctid(), g = sm.g;
@@ -894,6 +947,8 @@ __device__ __forceinline__ void gemv_ksplit(const Phase &p, int kind, unsigned i
     auto slice_rows = [&](int s, int j0, int step) {
         float2 act[4];
         load_slice(sm.u.vec, s, lane, act);
+        QAct qa{};
+        if constexpr (Q8A) qa = quant8(act, 1.0f);  // o_proj / down inputs carry no deferred scale
         for (int j = j0; j < R; j += step) {
             const int c = j / p.rpc, jj = j - c * p.rpc;
             const int n = min(p.rpc, R - c * p.rpc), ns = PAIR ? 2 * n : n;
@@ -904,7 +959,8 @@ __device__ __forceinline__ void gemv_ksplit(const Phase &p, int kind, unsigned i
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 float2 acc = make_float2(0.f, 0.f);
-                piece_fma<I8>(wp[r], act, acc);
+                if constexpr (Q8A) piece_dot_q8(wp[r], qa, acc.x);
+                else piece_fma<I8>(wp[r], act, acc);
                 const float v = warp_sum2(acc);
                 if (lane == 0) sm.part[(j * NR + r) * F + s] = v;
             }
@@ -989,7 +1045,7 @@ __device__ __forceinline__ int gemv_head(const Phase &p, unsigned it, float scal
 // is a runtime value, so one copy of each core serves every phase that shares its row shape.  A
 // layer phase takes its weight chunks from the ring before it waits for its input (they do not
 // depend on it), then stages the input, computes and releases the chunks.
-template <int D, bool I8>
+template <int D, int WF>
 __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     constexpr int KO = kBlockHq * kHeadDim / D, KD = kBlockI / D;
     constexpr int KMAX = KO > KD ? KO : KD;
@@ -1018,13 +1074,13 @@ __device__ __forceinline__ int gemv_phase(int ph, unsigned it) {
     if (ok) {
         if (tr && ctid() == 0) tr[2] = gtime();
         if (kind == T_GATEUP) {
-            gemv_rows<4, I8, true, kPreGateUp>(p, kind, it, out_tag, scale, tr);
+            gemv_rows<4, WF, true, kPreGateUp>(p, kind, it, out_tag, scale, tr);
         } else if (kind == T_QKV || (kind == T_OPROJ && KO == kBlockH)) {
-            gemv_rows<4, I8, false, kPreQkv>(p, kind, it, out_tag, scale, tr);
+            gemv_rows<4, WF, false, kPreQkv>(p, kind, it, out_tag, scale, tr);
         } else if (kind == T_DOWN && KD == 1536) {
-            gemv_rows<6, I8, false, kPreDown>(p, kind, it, out_tag, scale, tr);
+            gemv_rows<6, WF, false, kPreDown>(p, kind, it, out_tag, scale, tr);
         } else if constexpr (D == 1) {  // one group: o_proj and down rows of 2048 / 3072 columns, split over the warps
-            gemv_ksplit<I8, false>(p, kind, it, out_tag);
+            gemv_ksplit<WF, false>(p, kind, it, out_tag);
         }
     }
     if (!ok) return kFailed;
@@ -1381,7 +1437,7 @@ __device__ __forceinline__ int attn_phase(int ph, unsigned it) {
     return (int)(it | (dead ? kDeadBit : 0u));
 }
 
-template <int D, bool I8, typename KT>
+template <int D, int WF, typename KT>
 __device__ void consumer() {
     constexpr int G = kBlockG;
     Smem &sm = smem();
@@ -1433,7 +1489,7 @@ __device__ void consumer() {
     const int nph = kPhasesPerLayer * a.L + 1;
 #pragma unroll 1
     for (int ph = 0; ph < nph; ++ph) {
-        const int r = phase_type(a, ph) == T_ATTN ? attn_phase<G, KT>(ph, it) : gemv_phase<D, I8>(ph, it);
+        const int r = phase_type(a, ph) == T_ATTN ? attn_phase<G, KT>(ph, it) : gemv_phase<D, WF>(ph, it);
         if (!step(ph, r)) return;
     }
     if (tid == 0) {
@@ -1455,7 +1511,7 @@ __device__ void consumer() {
     }
 }
 
-template <int D, bool I8, typename KT>
+template <int D, int WF, typename KT>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
     Smem &sm = smem();
     const int tid = threadIdx.x;
@@ -1489,7 +1545,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         if (tid == kConsumerThreads) producer();
         return;
     }
-    consumer<D, I8, KT>();
+    consumer<D, WF, KT>();
 }
 
 }  // namespace

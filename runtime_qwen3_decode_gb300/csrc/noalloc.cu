@@ -72,7 +72,7 @@ extern "C" int qw_decode_step_noalloc(const qw_config *cfg, const qw_weights *w,
     if (pos >= cfg->max_ctx) return QW_CONTEXT_EXCEEDED;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(logits_dev) || ((uintptr_t)next_token_dev % 4))
         return QW_ALIGNMENT;
-    const bool i8 = cfg->weight_format == QW_W_INT8_G32;
+    const bool i8 = cfg->weight_format != QW_W_BF16;
     if (!aligned16(w->embed) || !aligned16(w->final_norm) || (w->lm_head && !aligned16(w->lm_head)))
         return QW_ALIGNMENT;
     for (int l = 0; l < cfg->n_layers; ++l) {

@@ -1245,6 +1245,12 @@ int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_laye
     if (!im) return 1;
     im->cfg = c;
     im->lay = prefill_layout(c, rows_max);
+    // int8 activations are a different arithmetic from the fp16 tensor-core prefill: such a model
+    // prefills through the decode path, one token at a time (ready stays 0)
+    if (c.weight_format == QW_W_Q8Q8) {
+        st->impl = im;
+        return 0;
+    }
     if (im->lay.total > bytes) {
         delete im;
         return 1;

@@ -43,7 +43,8 @@ bool mul_ok(size_t a, size_t b, size_t *out) {
 
 int validate_config(const qw_config *c) {
     if (!c) return QW_INVALID_ARGUMENT;
-    if (c->weight_format != QW_W_BF16 && c->weight_format != QW_W_INT8_G32) return QW_UNSUPPORTED_QUANTIZATION;
+    if (c->weight_format != QW_W_BF16 && c->weight_format != QW_W_INT8_G32 && c->weight_format != QW_W_Q8Q8)
+        return QW_UNSUPPORTED_QUANTIZATION;
     if (c->kv_format != QW_KV_F32 && c->kv_format != QW_KV_BF16) return QW_INVALID_ARGUMENT;
     if (c->n_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
         c->intermediate < 1 || c->vocab < 1 || c->max_ctx < 1)
@@ -259,7 +260,7 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     if (workspace_bytes < L.total) return QW_OUT_OF_MEMORY;
     if (!aligned(w->embed, 16) || !aligned(w->final_norm, 16) || (w->lm_head && !aligned(w->lm_head, 16)))
         return w->embed && w->final_norm ? QW_ALIGNMENT : QW_INVALID_ARGUMENT;
-    const bool i8 = cfg->weight_format == QW_W_INT8_G32;
+    const bool i8 = cfg->weight_format != QW_W_BF16;
     std::vector<qw::DevLayer> host_layers((size_t)cfg->n_layers);
     for (int l = 0; l < cfg->n_layers; ++l) {
         const qw_layer_weights &lw = w->layers[l];

@@ -31,6 +31,7 @@ CUDA_ERROR = 21
 
 W_BF16 = 0
 W_INT8_G32 = 1
+W_Q8Q8 = 2
 KV_F32 = 0
 KV_BF16 = 1
 DEBUG_HIDDEN = 1
@@ -191,6 +192,8 @@ def _check(rc: int, what: str):
 def make_config(dims, max_ctx: int | None = None) -> Config:
     """dims: any object with the Qwen3 dimension attributes (n_layers, hidden, ...)."""
     fmt = {"bf16": W_BF16, "int8_g32": W_INT8_G32}.get(getattr(dims, "weight_format", "bf16"), -1)
+    if getattr(dims, "act_format", "f32") == "q8":
+        fmt = W_Q8Q8 if fmt == W_INT8_G32 else -1
     kvf = {"f32": KV_F32, "bf16": KV_BF16}.get(getattr(dims, "kv_format", "f32"), -1)
     return Config(dims.n_layers, dims.hidden, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.intermediate,
                   dims.vocab, dims.rms_eps, dims.rope_theta, int(max_ctx or dims.max_ctx), fmt, kvf)
@@ -271,7 +274,7 @@ def decode_step_noalloc(cfg: Config, dev_weights: dict, k_cache, v_cache, pos: i
         raise ValueError("logits_out must be a contiguous CUDA float32 tensor of at least vocab elements")
     if not next_token_out.is_cuda or next_token_out.dtype != torch.int32 or next_token_out.numel() < 1:
         raise ValueError("next_token_out must be a CUDA int32 tensor")
-    w, layers = weight_table(dev_weights, cfg.weight_format == W_INT8_G32)
+    w, layers = weight_table(dev_weights, cfg.weight_format != W_BF16)
     st = stream if stream is not None else torch.cuda.current_stream()
     _check(_lib().qw_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), k_cache.data_ptr(), v_cache.data_ptr(),
                                          int(pos), int(token), logits_out.data_ptr(), next_token_out.data_ptr(),
@@ -313,7 +316,7 @@ class Model:
 
         self.dims = dims
         self.cfg = make_config(dims, max_ctx)
-        self.int8 = self.cfg.weight_format == W_INT8_G32
+        self.int8 = self.cfg.weight_format in (W_INT8_G32, W_Q8Q8)
         nbytes = workspace_bytes(self.cfg)
         if nbytes == 0:
             raise QwError(UNSUPPORTED_SHAPE, "workspace_bytes")
