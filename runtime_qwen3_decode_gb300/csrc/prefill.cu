@@ -46,7 +46,6 @@ using namespace tc;
 
 constexpr int BM = 128;  // GEMM tile rows (prompt rows) = TMEM lanes
 constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle span of fp16
-constexpr int kGemmThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
@@ -55,6 +54,8 @@ enum { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
 struct QkvOut {
     const __nv_bfloat16 *q_norm, *k_norm;  // [128] each
     const float2 *rope;                    // [max_ctx][64] (cos, sin)
+    const float2 *rope_t;                  // the same table frequency-major: [64][rope_ld]
+    int rope_ld;
     int pos0, Hq, Hkv;
     float eps;
     __half *q16;                           // [Hq][q_rows][128]
@@ -79,18 +80,39 @@ struct GemmParams {
     StepFlags *flags;
 };
 
-template <int BN>
+// Warp roles of a GEMM CTA: kProducers TMA warps (one issuing lane each, taking turns
+// over the stages: one thread's issue cost per stage would otherwise exceed the MMA time
+// of a stage), one MMA warp, kEpiWarps epilogue warps.  The q|k|v tile has eight epilogue
+// warps, one per (TMEM lane quarter, head); the others four.  A stage holds kKbPerStage
+// 64-deep k-blocks: with 128-wide tiles one thread's wait + issue + commit per 64-deep
+// block (measured ~430 cycles) exceeds the block's 256 tensor cycles, so those tiles
+// take 128-deep stages (8 MMAs per wait and commit).
+template <int BN, int EPI>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
-    static constexpr int kABytes = BM * BK * 2;
-    static constexpr int kBBytes = BN * BK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kProducers = BN == 256 ? 2 : 3;
+    static constexpr int kMmaWarp = kProducers;
+    static constexpr int kEpi0 = kProducers + 1;  // first epilogue warp
+    static constexpr int kEpiWarps = EPI == EPI_QKV ? 8 : 4;
+    static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+    static constexpr int kStgCols = EPI == EPI_QKV ? 16 : 32;  // columns per staged block
+    static constexpr int kStgStride = kStgCols + 4;            // floats per staged row
+    static constexpr int kStgWarpFloats = 32 * kStgStride;
+    static constexpr int kKbPerStage = BN == 256 ? 1 : 2;
+    static constexpr int kStages = BN == 256 ? 4 : 3;
+    static constexpr int kABytes = BM * BK * 2;  // one 64-deep k-block of A
+    static constexpr int kBBytes = BN * BK * 2;  // one 64-deep k-block of B
+    static constexpr int kStageA = kKbPerStage * kABytes;
+    static constexpr int kStageB = kKbPerStage * kBBytes;
     static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
     static constexpr int kBarBytes = 256;
-    static constexpr int kStgBytes = 4 * 32 * 36 * 4;  // epilogue staging, 4 warps x 32 rows x 36 floats
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStgBytes + kBarBytes;
+    static constexpr int kStgBytes = kEpiWarps * kStgWarpFloats * 4;
+    static constexpr int kNormBytes = EPI == EPI_QKV ? 2 * kHeadDim * 4 : 0;  // q_norm, k_norm as f32
+    static constexpr size_t kSmem =
+        1024 + (size_t)kStages * (kStageA + kStageB) + kStgBytes + kNormBytes + kBarBytes;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kProducers <= kStages, "each producer owns at most one stage at a time");
+    static_assert(EPI != EPI_QKV || BN == 2 * kHeadDim, "the q|k|v tile is two heads wide");
 };
 
 __device__ __forceinline__ void raise(StepFlags *f, unsigned code) {
@@ -120,31 +142,34 @@ __device__ __forceinline__ uint4 pack_half8(const float *v) {
 //
 // An epilogue warp holds 32 output rows, one per lane (TMEM lane = tile row).  Stores
 // straight from that layout would make every instruction touch 32 cache lines, so each
-// 32-column block goes through a per-warp shared-memory staging area (32 rows x 36
-// floats: 16-byte accesses of a quarter warp fall in distinct banks both ways) and
-// leaves transposed: one store instruction covers 4 rows x 32 columns.
+// block of SC columns goes through a per-warp shared-memory staging area (32 rows x
+// (SC + 4) floats) and leaves transposed, every store instruction covering whole row
+// segments.  The padding keeps both directions free of bank conflicts: writing, the
+// eight lanes of a quarter warp store the same 16-byte chunk of eight rows (row pitch
+// = 4 banks mod 32 x odd); reading, a quarter warp takes one row's eight chunks (SC = 32)
+// or one chunk of eight rows (SC = 16).
 
-constexpr int kStgStride = 36;                       // floats per staged row
-constexpr int kStgWarpFloats = 32 * kStgStride;     // per epilogue warp
-
-// Lane l's 32 values -> staging row l.
+// Lane l's SC values -> staging row l.
+template <int SC>
 __device__ __forceinline__ void stage_rows(float *stg, const float *v) {
     const int lane = threadIdx.x & 31;
-    float4 *d = reinterpret_cast<float4 *>(stg + lane * kStgStride);
+    float4 *d = reinterpret_cast<float4 *>(stg + lane * (SC + 4));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) d[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    for (int k = 0; k < SC / 4; ++k) d[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
     __syncwarp();
 }
 
-// Visit the staged block transposed: f(r, c4, x) for row r (0..31) and columns 4 c4..4 c4+3,
-// 8 passes of 4 rows per warp.  Ends with a __syncwarp so the area can be restaged.
-template <typename F>
+// Visit the staged block transposed: f(r, c4, x) for row r (0..31) and columns
+// 4 c4 .. 4 c4 + 3.  Ends with a __syncwarp so the area can be restaged.
+template <int SC, typename F>
 __device__ __forceinline__ void unstage(const float *stg, F &&f) {
+    static_assert(SC == 16 || SC == 32, "staging block width");
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = 4 * it + (lane >> 3), c4 = lane & 7;
-        f(r, c4, *reinterpret_cast<const float4 *>(stg + r * kStgStride + 4 * c4));
+    for (int it = 0; it < SC / 4; ++it) {
+        const int r = SC == 32 ? 4 * it + (lane >> 3) : 8 * it + (lane & 7);
+        const int c4 = SC == 32 ? lane & 7 : lane >> 3;
+        f(r, c4, *reinterpret_cast<const float4 *>(stg + r * (SC + 4) + 4 * c4));
     }
     __syncwarp();
 }
@@ -164,41 +189,18 @@ __device__ __forceinline__ float4 round_bf16(float4 x) {
                        __bfloat162float(__float2bfloat16_rn(x.z)), __bfloat162float(__float2bfloat16_rn(x.w)));
 }
 
-// One 128-wide head of the q|k|v tile for the warp's 32 prompt rows (lane = row, t = the
-// lane's row): QK-Norm and RoPE of q and k heads (the decode kernel's arithmetic:
-// r = rsqrt(mean(v^2) + eps), v = w * (v * r), then dims (i, i + 64) rotated by the
-// position's angle), then q -> q16, k and v -> the cache plus their fp16 shadows.
+// 32 columns d0 .. d0 + 31 of one q|k|v head for the warp's 32 prompt rows (lane = row):
+// q -> q16, k and v -> the cache plus their fp16 shadows.
 template <typename KT>
-__device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32], int slot, int t, int r0, int M,
-                                             float *stg) {
-    const int P = o.row_pos ? (t < M ? o.row_pos[t] : 0) : o.pos0 + t;
-    if (slot < o.Hq + o.Hkv) {
-        const __nv_bfloat16 *w = slot < o.Hq ? o.q_norm : o.k_norm;
-        float ss = 0.f;
+__device__ __forceinline__ void qkv_put32(const QkvOut &o, float (&v)[32], int d0, int slot, bool is_q, bool is_k,
+                                          int kvh, KT *cache, int t, int r0, int M, float *stg) {
 #pragma unroll
-        for (int i = 0; i < kHeadDim; ++i) ss += v[i >> 5][i & 31] * v[i >> 5][i & 31];
-        const float r = rsqrtf(ss * (1.0f / kHeadDim) + o.eps);
-#pragma unroll
-        for (int i = 0; i < kHeadDim; ++i) v[i >> 5][i & 31] = __bfloat162float(w[i]) * (v[i >> 5][i & 31] * r);
-        const float2 *cs = o.rope + (size_t)min(P, o.max_ctx - 1) * (kHeadDim / 2);
-#pragma unroll
-        for (int i = 0; i < kHeadDim / 2; ++i) {
-            const float2 c = cs[i];
-            const float a = v[i >> 5][i & 31], b = v[(i + 64) >> 5][i & 31];
-            v[i >> 5][i & 31] = a * c.x - b * c.y;
-            v[(i + 64) >> 5][i & 31] = b * c.x + a * c.y;
-        }
-    }
-    const bool is_q = slot < o.Hq, is_k = !is_q && slot < o.Hq + o.Hkv;
-    const int kvh = is_q ? 0 : is_k ? slot - o.Hq : slot - o.Hq - o.Hkv;
-    KT *cache = reinterpret_cast<KT *>(is_k ? o.kc : o.vc) + (size_t)kvh * o.max_ctx * kHeadDim;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        stage_rows(stg, v[k]);
-        unstage(stg, [&](int r, int c4, float4 x) {
+    for (int h = 0; h < 2; ++h) {
+        stage_rows<16>(stg, v + 16 * h);
+        unstage<16>(stg, [&](int r, int c4, float4 x) {
             const int tr = r0 + r;  // prompt row
             if (tr >= M) return;
-            const int d = 32 * k + 4 * c4;
+            const int d = d0 + 16 * h + 4 * c4;
             if (is_q) {
                 *reinterpret_cast<uint2 *>(o.q16 + ((size_t)slot * o.q_rows + tr) * kHeadDim + d) = pack_half4(x);
                 return;
@@ -219,32 +221,91 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, float (&v)[4][32],
     }
     // V^T shadow: for each dim the warp's 32 rows are 32 consecutive positions (64 B)
     if (!is_q && !is_k && t < M && o.v16t) {
-        __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P;
+        const int P = o.row_pos ? o.row_pos[t] : o.pos0 + t;
+        __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P + (size_t)d0 * o.kv_rows;
 #pragma unroll
-        for (int i = 0; i < kHeadDim; ++i) {
-            float x = v[i >> 5][i & 31];
+        for (int i = 0; i < 32; ++i) {
+            float x = v[i];
             if constexpr (sizeof(KT) == 2) x = __bfloat162float(__float2bfloat16_rn(x));
             dst[(size_t)i * o.kv_rows] = __float2half_rn(x);
         }
     }
 }
 
-// r0: the warp's first row (tile rows r0 .. r0 + 31); stg: its staging area.
+// One 128-wide head of the q|k|v tile (TMEM columns tcol .. tcol + 127) for the warp's
+// 32 prompt rows (lane = row, t = the lane's row): QK-Norm and RoPE of q and k heads (the
+// decode kernel's arithmetic: r = rsqrt(mean(v^2) + eps), v = w * (v * r), then dims
+// (i, i + 64) rotated by the position's angle), then the stores of qkv_put32.  The head
+// is read from TMEM twice (sum of squares, then the rotation pairs) so that at most 64
+// of its values are live.  snorm: q_norm then k_norm as f32 in shared memory.
+template <typename KT>
+__device__ __forceinline__ void qkv_head_out(const QkvOut &o, uint32_t tcol, int slot, int t, int r0, int M,
+                                             float *stg, const float *snorm) {
+    const bool is_q = slot < o.Hq, is_k = !is_q && slot < o.Hq + o.Hkv;
+    const int kvh = is_q ? 0 : is_k ? slot - o.Hq : slot - o.Hq - o.Hkv;
+    KT *cache = reinterpret_cast<KT *>(is_k ? o.kc : o.vc) + (size_t)kvh * o.max_ctx * kHeadDim;
+    if (!is_q && !is_k) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(tcol + 32 * c, v);
+            qkv_put32<KT>(o, v, 32 * c, slot, false, false, kvh, cache, t, r0, M, stg);
+        }
+        return;
+    }
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tcol + 32 * c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
+    }
+    const float r = rsqrtf(ss * (1.0f / kHeadDim) + o.eps);
+    const int P = o.row_pos ? (t < M ? o.row_pos[t] : 0) : o.pos0 + t;
+    // frequency-major table: for each frequency the warp's 32 rows read 32 consecutive
+    // positions (one coalesced request) instead of 32 rows 512 bytes apart
+    const float2 *cs = o.rope_t + min(P, o.max_ctx - 1);
+    const float *w = snorm + (is_q ? 0 : kHeadDim);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+        float a[32], b[32];
+        tmem_ld32(tcol + 32 * j, a);
+        tmem_ld32(tcol + 64 + 32 * j, b);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 wa = reinterpret_cast<const float4 *>(w + 32 * j)[k];
+            const float4 wb = reinterpret_cast<const float4 *>(w + 64 + 32 * j)[k];
+            const float wav[4] = {wa.x, wa.y, wa.z, wa.w}, wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * k + u;
+                const float2 c = cs[(size_t)(32 * j + i) * o.rope_ld];
+                const float x = wav[u] * (a[i] * r), y = wbv[u] * (b[i] * r);
+                a[i] = x * c.x - y * c.y;
+                b[i] = y * c.x + x * c.y;
+            }
+        }
+        qkv_put32<KT>(o, a, 32 * j, slot, is_q, is_k, kvh, cache, t, r0, M, stg);
+        qkv_put32<KT>(o, b, 64 + 32 * j, slot, is_q, is_k, kvh, cache, t, r0, M, stg);
+    }
+}
+
+// r0: the warp's first row (tile rows r0 .. r0 + 31); tacc: the accumulator buffer at the
+// warp's TMEM lane quarter; e: the warp's epilogue index; stg: its staging area.
 template <int BN, int EPI>
-__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int r0, int nt, float *stg) {
+__device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int r0, int nt, int e, float *stg,
+                                              const float *snorm) {
+    using C = GemmCfg<BN, EPI>;
+    constexpr int SC = C::kStgCols;
     const int lane = threadIdx.x & 31;
     if constexpr (EPI == EPI_QKV) {
-#pragma unroll 1
-        for (int hl = 0; hl < BN / kHeadDim; ++hl) {
-            float v[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tacc + hl * kHeadDim + 32 * c, v[c]);
-            const int slot = nt * (BN / kHeadDim) + hl;
-            if (p.qkv.kv_f32)
-                qkv_head_out<float>(p.qkv, v, slot, r0 + lane, r0, p.M, stg);
-            else
-                qkv_head_out<__nv_bfloat16>(p.qkv, v, slot, r0 + lane, r0, p.M, stg);
-        }
+        const int hl = e >> 2;  // warps e and e + 4 share a lane quarter and split the two heads
+        const int slot = nt * (BN / kHeadDim) + hl;
+        if (p.qkv.kv_f32)
+            qkv_head_out<float>(p.qkv, tacc + hl * kHeadDim, slot, r0 + lane, r0, p.M, stg, snorm);
+        else
+            qkv_head_out<__nv_bfloat16>(p.qkv, tacc + hl * kHeadDim, slot, r0 + lane, r0, p.M, stg, snorm);
     } else if constexpr (EPI == EPI_SWIGLU) {
         constexpr int HB = BN / 2;  // gate columns [0, HB), matching up columns [HB, BN)
 #pragma unroll 1
@@ -257,14 +318,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
             // of the output); the accurate forms made this epilogue ~2.3x longer than the
             // tile's mainloop.  g -> -inf gives g / inf = -0, g -> +inf gives g.
             for (int i = 0; i < 32; ++i) g[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
-            stage_rows(stg, g);
-            unstage(stg, [&](int r, int c4, float4 x) {
+            stage_rows<SC>(stg, g);
+            unstage<SC>(stg, [&](int r, int c4, float4 x) {
                 if (r0 + r < p.M)
                     *reinterpret_cast<uint2 *>(p.act + (size_t)(r0 + r) * p.ldh + (size_t)nt * HB + c + 4 * c4) =
                         pack_half4(x);
             });
         }
     } else {
+        static_assert(SC == 32, "the store / add epilogue reads 32-column blocks");
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
             float v[32];
@@ -280,11 +342,11 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
                 }
             }
             tmem_ld32(tacc + c, v);
-            stage_rows(stg, v);
+            stage_rows<SC>(stg, v);
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int r = 4 * it + (lane >> 3), c4 = lane & 7;
-                float4 x = *reinterpret_cast<const float4 *>(stg + r * kStgStride + 4 * c4);
+                float4 x = *reinterpret_cast<const float4 *>(stg + r * C::kStgStride + 4 * c4);
                 if (r0 + r >= p.M) continue;
                 if constexpr (EPI == EPI_ADD) {
                     x.x += y[it].x;
@@ -305,15 +367,16 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
 // with 128-byte swizzle.  Tiles BM x BN, tile index -> (m tile fastest, n tile).
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, EPI>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                 const GemmParams p) {
-    using C = GemmCfg<BN>;
+    using C = GemmCfg<BN, EPI>;
     uint8_t *base = smem_base1024();
     uint8_t *sa = base;
-    uint8_t *sb = base + C::kStages * C::kABytes;
-    float *stg_all = reinterpret_cast<float *>(sb + C::kStages * C::kBBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sb + C::kStages * C::kBBytes + C::kStgBytes);
+    uint8_t *sb = base + C::kStages * C::kStageA;
+    float *stg_all = reinterpret_cast<float *>(sb + C::kStages * C::kStageB);
+    float *snorm = stg_all + C::kEpiWarps * C::kStgWarpFloats;
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(snorm) + C::kNormBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
     uint64_t *tempty = tfull + 2;
@@ -325,6 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int tiles_m = (p.M + BM - 1) / BM;
     const int ntiles = tiles_m * (p.N / BN);
     const int nkb = p.K / BK;
+    const int nst = (nkb + C::kKbPerStage - 1) / C::kKbPerStage;  // stages per tile (the last may be short)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -333,37 +397,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+            mbar_init(&tempty[b], C::kEpiWarps);  // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
         *abort = 0;
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, C::kTmemCols);
+    if constexpr (EPI == EPI_QKV) {
+        for (int i = threadIdx.x; i < 2 * kHeadDim; i += C::kThreads)
+            snorm[i] = __bfloat162float(i < kHeadDim ? p.qkv.q_norm[i] : p.qkv.k_norm[i - kHeadDim]);
+    }
+    if (warp == C::kMmaWarp) tmem_alloc(tslot, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the setup above overlaps the previous kernel's tail; A and the outputs are its products
+    chain_wait();
+    chain_release();
 
-    if (warp == 0) {
+    if (warp < C::kProducers) {
         if (lane == 0) {
-            // ---- TMA producer
-            int s = 0;
+            // ---- TMA producers: producer `warp` fills stages warp, warp + kProducers, ...
+            // of the CTA's sequence (slot and phase advance over every stage)
+            int s = 0, turn = 0;
             unsigned ph = 0;
             int last_par[C::kStages];
             for (int i = 0; i < C::kStages; ++i) last_par[i] = -1;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
                 const int m0 = (tile % tiles_m) * BM, n0 = (tile / tiles_m) * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort, true, kWaitLimitNs)) {
-                        ok = false;
-                        break;
+                for (int st = 0; st < nst; ++st) {
+                    if (turn == warp) {
+                        if (!mbar_wait(&empty[s], ph ^ 1u, abort, true, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        const int kb0 = st * C::kKbPerStage;
+                        const int nk = min(C::kKbPerStage, nkb - kb0);
+                        mbar_expect_tx(&full[s], (unsigned)(nk * (C::kABytes + C::kBBytes)));
+                        for (int j = 0; j < nk; ++j) {
+                            tma_load_2d(sa + s * C::kStageA + j * C::kABytes, &tma, (kb0 + j) * BK, m0, &full[s]);
+                            tma_load_2d(sb + s * C::kStageB + j * C::kBBytes, &tmb, (kb0 + j) * BK, n0, &full[s]);
+                        }
+                        last_par[s] = (int)ph;
                     }
-                    mbar_expect_tx(&full[s], C::kStageBytes);
-                    tma_load_2d(sa + s * C::kABytes, &tma, kb * BK, m0, &full[s]);
-                    tma_load_2d(sb + s * C::kBBytes, &tmb, kb * BK, n0, &full[s]);
-                    last_par[s] = (int)ph;
+                    if (++turn == C::kProducers) turn = 0;
                     if (++s == C::kStages) {
                         s = 0;
                         ph ^= 1u;
@@ -378,7 +457,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (last_par[i] >= 0) mbar_wait(&full[i], (unsigned)last_par[i], abort, false, kWaitLimitNs);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == C::kMmaWarp) {
         if (lane == 0) {
             // ---- MMA issuer
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
@@ -392,17 +471,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int st = 0; st < nst; ++st) {
                     if (!mbar_wait(&full[s], ph, abort, true, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(su32(sa + s * C::kABytes));
-                    const uint64_t bd = desc_sw128(su32(sb + s * C::kBBytes));
+                    const int nk = min(C::kKbPerStage, nkb - st * C::kKbPerStage);
+                    for (int j = 0; j < nk; ++j) {
+                        const uint64_t ad = desc_sw128(su32(sa + s * C::kStageA + j * C::kABytes));
+                        const uint64_t bd = desc_sw128(su32(sb + s * C::kStageB + j * C::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step (address field >> 4)
-                        mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step (address field >> 4)
+                            mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (st | j | k) != 0);
+                    }
                     mma_commit(&empty[s]);
                     if (++s == C::kStages) {
                         s = 0;
@@ -425,8 +507,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(drain, 0, abort, false, kWaitLimitNs);
         }
     } else {
-        // ---- epilogue warps 2..5: TMEM lane quarter = warp % 4
-        const int q = warp & 3;
+        // ---- epilogue warps: TMEM lane quarter = warp % 4
+        const int e = warp - C::kEpi0, q = warp & 3;
+        float *stg = stg_all + e * C::kStgWarpFloats;
         int acc = 0;
         unsigned aph = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -443,7 +526,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             const int mt = tile % tiles_m, nt = tile / tiles_m;
             const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32, nt, stg_all + (warp - 2) * kStgWarpFloats);
+            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32, nt, e, stg, snorm);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -455,7 +538,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -487,6 +570,8 @@ __global__ void __launch_bounds__(kRowThreads) norm_rows_kernel(float *x, const 
                                                                 const __nv_bfloat16 *w, __half *h, int rows,
                                                                 float eps) {
     constexpr int H = 1024 * KM, NC = 4 * KM;
+    chain_wait();
+    chain_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * (kRowThreads / 32) + warp;
     if (t >= rows) return;
@@ -541,14 +626,10 @@ __global__ void __launch_bounds__(kRowThreads) norm_rows_kernel(float *x, const 
 }
 
 cudaError_t launch_norm_rows(float *x, const int32_t *tokens, const __nv_bfloat16 *embed, const __nv_bfloat16 *w,
-                             __half *h, int rows, int H, float eps, cudaStream_t st) {
-    const int grid = (rows + kRowThreads / 32 - 1) / (kRowThreads / 32);
-    switch (H >> 10) {
-        case 1: norm_rows_kernel<1><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
-        case 2: norm_rows_kernel<2><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
-        default: norm_rows_kernel<3><<<grid, kRowThreads, 0, st>>>(x, tokens, embed, w, h, rows, eps); break;
-    }
-    return cudaGetLastError();
+                             __half *h, int rows, int H, float eps, cudaStream_t st, bool chained) {
+    const dim3 grid((rows + kRowThreads / 32 - 1) / (kRowThreads / 32)), block(kRowThreads);
+    auto k = H >> 10 == 1 ? norm_rows_kernel<1> : H >> 10 == 2 ? norm_rows_kernel<2> : norm_rows_kernel<3>;
+    return launch_k(chained, k, grid, block, 0, st, x, tokens, embed, w, h, rows, eps);
 }
 
 // ------------------------------------------------------------------ K/V fp16 shadows
@@ -581,6 +662,8 @@ template <typename KT>
 __global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *vc, int max_ctx, int n_pos, int n_fill,
                                                        __half *k16, __half *v16t, int kv_rows) {
     __shared__ __align__(16) __half vt[kHeadDim][kShadowPos + 8];  // padded rows (144 B, 16-B aligned)
+    chain_wait();
+    chain_release();
     const int p0 = blockIdx.x * kShadowPos, kvh = blockIdx.y;
     const KT *ks = kc + (size_t)kvh * max_ctx * kHeadDim;
     const KT *vs = vc + (size_t)kvh * max_ctx * kHeadDim;
@@ -736,6 +819,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tO = tmem + kFaColO;  // S buffers at columns 0 and 128
+    chain_wait();
+    chain_release();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1027,6 +1112,8 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float *x, cons
     __shared__ float red[kHeadThreads / 32];
     __shared__ unsigned long long best[kHeadThreads / 32];
     __shared__ int bad_any;
+    chain_wait();
+    chain_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) bad_any = 0;
     float ss = 0.f;
@@ -1163,22 +1250,22 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_rows)
 template <int BN, int EPI>
 cudaError_t set_gemm_attr() {
     return cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)GemmCfg<BN>::kSmem);
+                                (int)GemmCfg<BN, EPI>::kSmem);
 }
 
 template <int BN, int EPI>
 cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int nsm,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool chained = false) {
     const int tiles = (p.M + BM - 1) / BM * (p.N / BN);
     const int grid = tiles < nsm ? tiles : nsm;
-    gemm_kernel<BN, EPI><<<grid, kGemmThreads, GemmCfg<BN>::kSmem, st>>>(ma, mb, p);
-    return cudaGetLastError();
+    return launch_k(chained, gemm_kernel<BN, EPI>, dim3(grid), dim3(GemmCfg<BN, EPI>::kThreads),
+                    GemmCfg<BN, EPI>::kSmem, st, ma, mb, p);
 }
 
 size_t align_up(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PrefillLayout {
-    size_t w16, x, h, q16, o16, act, k16, v16t, tok, misc, total;
+    size_t w16, x, h, q16, o16, act, k16, v16t, tok, misc, rope_t, total;
     size_t w_layer;  // fp16 weight elements per layer
     int kv_rows;     // positions per head in the fp16 K / V^T shadows (max_ctx rounded up to 128)
 };
@@ -1205,6 +1292,7 @@ PrefillLayout prefill_layout(const qw_config &c, int rows) {
     L.v16t = take((size_t)c.n_kv_heads * L.kv_rows * c.head_dim * 2);
     L.tok = take((size_t)rows * 4);
     L.misc = take(64);
+    L.rope_t = take((size_t)c.max_ctx * (c.head_dim / 2) * sizeof(float2));
     L.total = off;
     return L;
 }
@@ -1233,8 +1321,19 @@ cudaError_t prefill_prepare() {
     return cudaFuncSetAttribute(fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FaSmem::kDyn);
 }
 
-int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, uint8_t *buf, size_t bytes,
-                 int rows_max, int nsm, cudaStream_t stream) {
+namespace {
+// rope_t[i][p] = rope[p][i]: the RoPE table frequency-major for the q|k|v epilogue
+__global__ void rope_transpose_kernel(const float2 *rope, int ctx, int half, float2 *rope_t) {
+    const long long n = (long long)ctx * half;
+    for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(k / ctx), p = (int)(k % ctx);
+        rope_t[k] = rope[(size_t)p * half + i];
+    }
+}
+}  // namespace
+
+int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, const float2 *rope, uint8_t *buf,
+                 size_t bytes, int rows_max, int nsm, cudaStream_t stream) {
     st->buf = buf;
     st->bytes = bytes;
     st->rows_max = rows_max;
@@ -1252,6 +1351,12 @@ int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_laye
         return 0;
     }
     if (im->lay.total > bytes) {
+        delete im;
+        return 1;
+    }
+    rope_transpose_kernel<<<2 * nsm, 256, 0, stream>>>(rope, c.max_ctx, c.head_dim / 2,
+                                                        reinterpret_cast<float2 *>(buf + im->lay.rope_t));
+    if (cudaGetLastError() != cudaSuccess) {
         delete im;
         return 1;
     }
@@ -1339,9 +1444,13 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
         CUtensorMap mh, mo, ma;
         if (!make_map(&mh, h, m, H, BM) || !make_map(&mo, o16, m, QD, BM) || !make_map(&ma, act, m, I, BM))
             return 1;
-        launch_norm_rows(x, tok, a.embed, hl[0].input_norm, h, m, H, a.eps, stream);
-        if (debug & 1)
+        launch_norm_rows(x, tok, a.embed, hl[0].input_norm, h, m, H, a.eps, stream, false);
+        // chained launches (programmatic dependent launch) only directly after a kernel
+        bool ch = true;
+        if (debug & 1) {
             cudaMemcpyAsync(a.hidden, x + (size_t)(m - 1) * H, (size_t)H * 4, cudaMemcpyDeviceToDevice, stream);
+            ch = false;
+        }
         for (int l = 0; l < c.n_layers; ++l) {
             const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
             GemmParams gp{};
@@ -1354,14 +1463,18 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             // steps or an import); the chunk's own rows come from the q|k|v epilogue below
             if (p0 > 0) {
                 const dim3 sg((p0 + kShadowPos - 1) / kShadowPos, Hkv);
+                cudaError_t se;
                 if (a.kv_f32)
-                    kv_shadow_kernel<float><<<sg, 256, 0, stream>>>(reinterpret_cast<const float *>(kc),
-                                                                     reinterpret_cast<const float *>(vc), a.max_ctx,
-                                                                     p0, p0, k16, v16t, L.kv_rows);
+                    se = launch_k(ch, kv_shadow_kernel<float>, sg, dim3(256), 0, stream,
+                                  reinterpret_cast<const float *>(kc), reinterpret_cast<const float *>(vc), a.max_ctx,
+                                  p0, p0, k16, v16t, L.kv_rows);
                 else
-                    kv_shadow_kernel<__nv_bfloat16><<<sg, 256, 0, stream>>>(
-                        reinterpret_cast<const __nv_bfloat16 *>(kc), reinterpret_cast<const __nv_bfloat16 *>(vc),
-                        a.max_ctx, p0, p0, k16, v16t, L.kv_rows);
+                    se = launch_k(ch, kv_shadow_kernel<__nv_bfloat16>, sg, dim3(256), 0, stream,
+                                  reinterpret_cast<const __nv_bfloat16 *>(kc),
+                                  reinterpret_cast<const __nv_bfloat16 *>(vc), a.max_ctx, p0, p0, k16, v16t,
+                                  L.kv_rows);
+                if (se != cudaSuccess) return 1;
+                ch = true;
             }
             // q | k | v with QK-Norm, RoPE, the K/V append and the shadows in the epilogue
             gp.N = QD + 2 * KD;
@@ -1370,6 +1483,8 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             qo.q_norm = hl[l].q_norm;
             qo.k_norm = hl[l].k_norm;
             qo.rope = a.rope;
+            qo.rope_t = reinterpret_cast<const float2 *>(buf + L.rope_t);
+            qo.rope_ld = c.max_ctx;
             qo.pos0 = p0;
             qo.Hq = Hq;
             qo.Hkv = Hkv;
@@ -1383,7 +1498,7 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             qo.k16 = k16;
             qo.v16t = v16t;
             qo.kv_rows = L.kv_rows;
-            if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
+            if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream, ch) != cudaSuccess) return 1;
             FaParams fp{};
             fp.n = m;
             fp.pos0 = p0;
@@ -1395,45 +1510,50 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
             fp.o16 = o16;
             fp.flags = a.flags;
             const dim3 ag((m + 128 / G - 1) / (128 / G) * Hkv);
-            fa_kernel<<<ag, kFaThreads, FaSmem::kDyn, stream>>>(im->tq, im->tk, im->tv, fp);
+            if (launch_k(true, fa_kernel, ag, dim3(kFaThreads), FaSmem::kDyn, stream, im->tq, im->tk, im->tv, fp) !=
+                cudaSuccess)
+                return 1;
             // x += o Wo^T
             gp.N = H;
             gp.K = QD;
             gp.out = x;
             gp.ldo = H;
-            if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
-            launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, m, H, a.eps, stream);
+            if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+            if (launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, m, H, a.eps, stream, true) != cudaSuccess)
+                return 1;
             // a = silu(h Wg^T) * (h Wu^T)
             gp.N = 2 * I;
             gp.K = H;
             gp.act = act;
             gp.ldh = I;
-            if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream) != cudaSuccess) return 1;
+            if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream, true) != cudaSuccess) return 1;
             // x += a Wd^T
             gp.N = H;
             gp.K = I;
             gp.out = x;
             gp.ldo = H;
-            if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream) != cudaSuccess) return 1;
-            if (debug & 1)
+            if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+            ch = true;
+            if (debug & 1) {
                 cudaMemcpyAsync(a.hidden + (size_t)(l + 1) * H, x + (size_t)(m - 1) * H, (size_t)H * 4,
                                 cudaMemcpyDeviceToDevice, stream);
-            if (l + 1 < c.n_layers)
-                launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, m, H, a.eps, stream);
+                ch = false;
+            }
+            if (l + 1 < c.n_layers) {
+                if (launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, m, H, a.eps, stream, ch) !=
+                    cudaSuccess)
+                    return 1;
+                ch = true;
+            }
         }
         done += m;
         if (done == n) {
             const float *xl = x + (size_t)(m - 1) * H;
             const dim3 hg(4 * st->nsm);
-            if (H == 1024)
-                head_kernel<1><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
-                                                                key, count, a.flags);
-            else if (H == 2048)
-                head_kernel<2><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
-                                                                key, count, a.flags);
-            else
-                head_kernel<3><<<hg, kHeadThreads, 0, stream>>>(xl, a.final_norm, a.lm_head, a.V, H, a.eps, a.logits,
-                                                                key, count, a.flags);
+            auto hk = H == 1024 ? head_kernel<1> : H == 2048 ? head_kernel<2> : head_kernel<3>;
+            if (launch_k(ch, hk, hg, dim3(kHeadThreads), 0, stream, xl, a.final_norm, a.lm_head, a.V, H, a.eps,
+                         a.logits, key, count, a.flags) != cudaSuccess)
+                return 1;
         }
         if (cudaGetLastError() != cudaSuccess) return 1;
     }
@@ -1463,7 +1583,7 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
     CUtensorMap mh, mo, ma;
     if (!make_map(&mh, h, B, H, BM) || !make_map(&mo, o16, B, QD, BM) || !make_map(&ma, act, B, I, BM)) return 1;
     if (launch_batch_tokens(bs.tokens_in, bs.picks, B, bs.tokens, stream) != cudaSuccess) return 1;
-    launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream);
+    launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream, false);
     if (bs.hidden) cudaMemcpyAsync(bs.hidden, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, stream);
     for (int l = 0; l < c.n_layers; ++l) {
         const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
@@ -1479,6 +1599,8 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         qo.q_norm = hl[l].q_norm;
         qo.k_norm = hl[l].k_norm;
         qo.rope = a.rope;
+            qo.rope_t = reinterpret_cast<const float2 *>(buf + L.rope_t);
+            qo.rope_ld = c.max_ctx;
         qo.Hq = Hq;
         qo.Hkv = Hkv;
         qo.eps = a.eps;
@@ -1511,7 +1633,7 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         gp.out = x;
         gp.ldo = H;
         if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
-        launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream);
+        launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream, false);
         // a = silu(h Wg^T) * (h Wu^T)
         gp.N = 2 * I;
         gp.K = H;
@@ -1527,7 +1649,8 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         if (bs.hidden)
             cudaMemcpyAsync(bs.hidden + (size_t)(l + 1) * B * H, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
                             stream);
-        if (l + 1 < c.n_layers) launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream);
+        if (l + 1 < c.n_layers)
+            launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream, false);
     }
     BatchHead hp{};
     hp.x = x;

@@ -409,7 +409,7 @@ int qw_model_create(const qw_config *cfg, const qw_weights *w, void *workspace, 
     m->step_bytes = qw::kStepBlockBytes;
     m->logits = a.logits;
     m->hidden = a.hidden;
-    if (qw::prefill_init(&m->pf, *cfg, host_layers.data(), ws + L.prefill, L.prefill_bytes,
+    if (qw::prefill_init(&m->pf, *cfg, host_layers.data(), a.rope, ws + L.prefill, L.prefill_bytes,
                          cfg->max_ctx < kPrefillRowsMax ? cfg->max_ctx : kPrefillRowsMax, nsm, m->stream)) {
         fprintf(stderr, "qw: preparing the batched prefill failed\n");
         qw::prefill_destroy(&m->pf);

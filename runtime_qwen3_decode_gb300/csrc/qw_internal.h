@@ -232,4 +232,24 @@ int plan_groups(int device, uint8_t *probe_scratch, uint8_t *xregion, int H, int
 // region holds too few pages of a group.
 bool plan_exchange(const Topology &t, const int8_t *page_group, int npages, const size_t *words, XPlan *plan);
 
+// Launches kernel k on stream st; chained = true adds programmatic stream serialization,
+// letting k start while the stream's previous kernel finishes (k must call chain_wait()
+// before touching memory that kernel used).  Use it only when the previous operation of
+// the stream is a kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool chained, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 }  // namespace qw

@@ -23,8 +23,8 @@ cudaError_t prefill_prepare();
 // Converts the layer weights to fp16 in buf and encodes their tensor maps (stream-ordered,
 // synchronises once).  Returns non-zero on a CUDA failure; ready stays 0 (token-by-token
 // prefill) when a weight does not fit fp16.
-int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, uint8_t *buf, size_t bytes,
-                 int rows_max, int nsm, cudaStream_t stream);
+int prefill_init(PrefillState *st, const qw_config &c, const DevLayer *host_layers, const float2 *rope, uint8_t *buf,
+                 size_t bytes, int rows_max, int nsm, cudaStream_t stream);
 void prefill_destroy(PrefillState *st);
 inline bool prefill_supported(const PrefillState &st) { return st.ready != 0; }
 // Runs n prompt tokens at positions pos0.. and leaves logits + greedy pick of the last row

@@ -24,6 +24,19 @@ __device__ __forceinline__ unsigned long long gtime() {
     return t;
 }
 
+// ---------------------------------------------------------------- launch chaining
+//
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream is still running.
+// chain_wait() returns once that kernel has completed and its memory writes are
+// visible (at once when the launch was an ordinary one); chain_release() lets the next
+// kernel of the stream begin launching.  A chained kernel calls chain_wait() before its
+// first access to memory an earlier kernel writes or reads, and every kernel launched
+// chained calls it, so that completion stays ordered along the stream.
+
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
