@@ -701,10 +701,12 @@ __global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *
 // t0 + r%(128/G), so both heads of a group share every K/V tile.  Per 128-key block j:
 //   S_j = Q K_j^T into one of two TMEM buffers (the tensor core computes S_{j+1} while
 //   the softmax warps work on S_j);
-//   two warps per row apply the causal mask and the online softmax in the log2 domain,
-//   each over 64 of the block's keys, exchange their block maxima through shared
-//   memory, and write P_j (fp16) into tensor memory;
-//   O += P_j V_j accumulates in TMEM.
+//   one softmax lane per row applies the causal mask and the online softmax in the log2
+//   domain over the block's 128 keys (a whole row per lane: no partial maxima or sums
+//   cross warps) and writes P_j (fp16) over the first half of S_j's buffer, so that P is
+//   double-buffered with S and softmax j never waits for P_{j-1} V_{j-1};
+//   O += P_j V_j accumulates in TMEM.  The tensor core runs S_{j+1} during softmax j
+//   and P_j V_j right after it.
 // Both A operands live in tensor memory (Q copied there once by the softmax warps, P
 // written by them per block), so the tensor core reads only K and V^T from shared
 // memory.  Per block, shared memory then carries the two 32 KB TMA writes and the two
@@ -713,16 +715,16 @@ __global__ void __launch_bounds__(256) kv_shadow_kernel(const KT *kc, const KT *
 // O is rescaled only when a row's running max grows by more than 8 (factor 256): O and
 // the row sum l always refer to the same reference max, so O / l is unaffected, and
 // p <= 2^8 stays well inside fp16.
-// Warp 0 issues the TMA loads of Q once and K per block, warp 10 those of V^T per block,
+// Warp 0 issues the TMA loads of Q once and K per block, warp 6 those of V^T per block,
 // into two independent 3-stage rings (K of block j+3 streams in as soon as S_j is done,
 // V of block j+3 once P_j V_j is; under load a 32 KB tile takes about 3000 cycles to
 // arrive, more than one block's softmax).  The third V stage is the Q tile's shared
 // memory, refilled only after Q has been copied into TMEM.  The two producers sit in different warps: two
 // spinning branches of one warp are not guaranteed to interleave, and a K load held
 // behind a V wait delays S_{j+2} past the end of softmax j+1.  Warp 1 owns TMEM and
-// issues the MMAs; warps 2-9 copy Q into TMEM, run the softmax and the output epilogue.
+// issues the MMAs; warps 2-5 copy Q into TMEM, run the softmax and the output epilogue.
 
-constexpr int kFaSoftmaxWarps = 8;
+constexpr int kFaSoftmaxWarps = 4;
 constexpr int kFaVWarp = 2 + kFaSoftmaxWarps;
 constexpr int kFaThreads = 32 * (kFaVWarp + 1);
 constexpr int kFaKeys = 128;
@@ -734,13 +736,13 @@ struct FaSmem {
     static constexpr int kQ = 0;                              // Q, later V^T stage 2
     static constexpr int kK = kTile;                          // K stages 0..2
     static constexpr int kV = kK + kFaStages * kTile;         // V^T stages 0, 1
-    static constexpr int kX = kV + (kFaStages - 1) * kTile;   // f32 [2 parity][2 halves][128 rows]
-    static constexpr int kBar = kX + 2 * 2 * 128 * 4;
+    static constexpr int kBar = kV + (kFaStages - 1) * kTile;
     static constexpr int kBytes = kBar + 256;
     static constexpr size_t kDyn = 1024 + kBytes;
 };
-// TMEM columns: S buffers 0 and 128 and O 256 (f32); P 384 and Q 448 (fp16 pairs).
-constexpr uint32_t kFaColO = 256, kFaColP = 384, kFaColQ = 448;
+// TMEM columns: S buffers 0 and 128 (f32; P_j as fp16 pairs over the first 64 columns
+// of S_j's buffer), O 256 (f32), Q 448 (fp16 pairs).
+constexpr uint32_t kFaColO = 256, kFaColQ = 448;
 static_assert(FaSmem::kDyn <= 227 * 1024, "shared memory budget");
 static_assert(kFaStages == 3, "the last V^T stage is the Q tile");
 
@@ -771,11 +773,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
               const __grid_constant__ CUtensorMap tv, const FaParams p) {
     uint8_t *base = smem_base1024();
     uint8_t *sQ = base + FaSmem::kQ, *sK = base + FaSmem::kK, *sV = base + FaSmem::kV;
-    float *sX = reinterpret_cast<float *>(base + FaSmem::kX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + FaSmem::kBar);
     uint64_t *q_full = bars, *q_tm = bars + 1, *k_full = bars + 2, *k_empty = bars + 5, *v_full = bars + 8,
-             *v_empty = bars + 11, *s_full = bars + 14, *s_free = bars + 16, *p_full = bars + 18, *pv_done = bars + 19,
-             *xbar = bars + 20, *drain = bars + 24;
+             *v_empty = bars + 11, *s_full = bars + 14, *p_full = bars + 18, *pv_done = bars + 19,
+             *drain = bars + 24;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 25);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
 
@@ -802,13 +803,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], kFaSoftmaxWarps);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
         mbar_init(p_full, kFaSoftmaxWarps);
         mbar_init(pv_done, 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);  // the two warps of a lane quarter
         mbar_init(drain, 1);
         *abort = 0;
         mbar_fence_init();
@@ -885,18 +882,17 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer: S_j, then P_{j-2} V_{j-2}; A operands (Q, P) in TMEM.  S_j
-            // only needs softmax j-2 to have read S_{j-2} (the start of that softmax), so it
-            // goes ahead of P_{j-2} V_{j-2}, which needs the end of it: the next S is always
-            // ready before the softmax warps reach it.
+            // ---- MMA issuer, A operands (Q, P) in TMEM.  Iteration j issues S_{j+1} (it only
+            // needs K_{j+1}, so the tensor core computes it while the softmax warps work on
+            // block j) and then P_j V_j (after softmax j).  P_j sits in the first 64 columns of
+            // S_j's buffer; S_{j+2} overwrites that buffer only after P_j V_j, which the
+            // in-order tensor pipe guarantees by issue order.
             constexpr uint32_t idesc = idesc_f16_f32(128, 128);
             bool ok = mbar_wait(q_tm, 0, abort, true, kWaitLimitNs);
-            for (int j = 0; ok && j < nkb + 2; ++j) {
-                if (j < nkb) {
-                    const int st = j % kFaStages;
-                    if (!mbar_wait(&k_full[st], (unsigned)(j / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
-                        (j >= 2 && !mbar_wait(&s_free[j & 1], (unsigned)((j - 2) >> 1) & 1u, abort, true,
-                                              kWaitLimitNs))) {
+            for (int j = -1; ok && j < nkb; ++j) {
+                if (j + 1 < nkb) {
+                    const int jn = j + 1, st = jn % kFaStages;
+                    if (!mbar_wait(&k_full[st], (unsigned)(jn / kFaStages) & 1u, abort, true, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -905,15 +901,15 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kHeadDim / 16; ++k) {
                         const uint64_t bd = desc_sw128(sk + (k >> 2) * 16384) + 2u * (k & 3);
-                        mma_f16_ts(tmem + 128u * (j & 1), tmem + kFaColQ + 8u * k, bd, idesc, k != 0);
+                        mma_f16_ts(tmem + 128u * (jn & 1), tmem + kFaColQ + 8u * k, bd, idesc, k != 0);
                     }
-                    mma_commit(&s_full[j & 1]);
+                    mma_commit(&s_full[jn & 1]);
                     mma_commit(&k_empty[st]);
                 }
-                if (j >= 2) {
-                    const int i = j - 2, st = i % kFaStages;
-                    if (!mbar_wait(&v_full[st], (unsigned)(i / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
-                        !mbar_wait(p_full, (unsigned)i & 1u, abort, true, kWaitLimitNs)) {
+                if (j >= 0) {
+                    const int st = j % kFaStages;
+                    if (!mbar_wait(&v_full[st], (unsigned)(j / kFaStages) & 1u, abort, true, kWaitLimitNs) ||
+                        !mbar_wait(p_full, (unsigned)j & 1u, abort, true, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -922,7 +918,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kFaKeys / 16; ++k) {
                         const uint64_t bd = desc_sw128(sv + (k >> 2) * 16384) + 2u * (k & 3);
-                        mma_f16_ts(tO, tmem + kFaColP + 8u * k, bd, idesc, i > 0 || k > 0);
+                        mma_f16_ts(tO, tmem + 128u * (j & 1) + 8u * k, bd, idesc, j > 0 || k > 0);
                     }
                     mma_commit(pv_done);
                     mma_commit(&v_empty[st]);
@@ -937,31 +933,33 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             mbar_wait(drain, 0, abort, false, kWaitLimitNs);
         }
     } else {
-        // ---- softmax warps 2..9: lane quarter q = warp % 4, row r = 32 q + lane; warp half
-        // hf takes head dims [64 hf, +64) of Q, keys [64 hf, 64 hf + 64) of every block (P
-        // columns [32 hf, +32)) and O dims [64 hf, +64)
-        const int q = warp & 3, hf = (warp - 2) >> 2, r = 32 * q + lane;
+        // ---- softmax warps 2..5: lane quarter q = warp % 4, row r = 32 q + lane; each lane
+        // owns its row's whole block (128 keys), so no partial maxima or sums cross warps
+        const int q = warp & 3, r = 32 * q + lane;
         const int t = G == 2 ? t0 + (r & 63) : t0 + r;
         const int head = g * G + (G == 2 ? (r >> 6) : 0);
         const int pr = p.pos0 + t;
-        const uint32_t lb0 = (uint32_t)(32 * q) << 16, lb = lb0 + 64u * hf;
+        const uint32_t lb0 = (uint32_t)(32 * q) << 16;
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
-        // Q row r, dims [64 hf, +64): eight 16-byte chunks of the swizzled tile, already
-        // fp16 pairs in K order, into 32 TMEM columns
+        // Q row r: sixteen 16-byte chunks of the swizzled tile (two 64-dim regions), already
+        // fp16 pairs in K order, into 64 TMEM columns
         bool ok = warp_wait(q_full, 0, abort);
         if (ok) {
-            uint32_t qv[32];
-            const uint8_t *src = sQ + hf * 16384;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(src + swz128(r, c));
-                qv[4 * c] = u.x;
-                qv[4 * c + 1] = u.y;
-                qv[4 * c + 2] = u.z;
-                qv[4 * c + 3] = u.w;
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t qv[32];
+                const uint8_t *src = sQ + hf * 16384;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(src + swz128(r, c));
+                    qv[4 * c] = u.x;
+                    qv[4 * c + 1] = u.y;
+                    qv[4 * c + 2] = u.z;
+                    qv[4 * c + 3] = u.w;
+                }
+                tmem_st32u(tmem + lb0 + kFaColQ + 32u * hf, qv);
             }
-            tmem_st32u(tmem + lb0 + kFaColQ + 32u * hf, qv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(q_tm);
@@ -973,38 +971,23 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                 break;
             }
             tc_fence_after();
-            float s[2][32];
-            tmem_ld32(tmem + lb + 128u * b, s[0]);
-            tmem_ld32(tmem + lb + 128u * b + 32u, s[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
-            const int k0 = j * kFaKeys + 64 * hf;
+            float s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb0 + 128u * b + 32u * c, s[c]);
+            const int k0 = j * kFaKeys;
             float mb = -INFINITY;
             if (j >= first_masked) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < kFaKeys; ++i) {
                     float &v = s[i >> 5][i & 31];
                     v = k0 + i <= pr ? v : -INFINITY;
                     mb = fmaxf(mb, v);
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) mb = fmaxf(mb, s[i >> 5][i & 31]);
+                for (int i = 0; i < kFaKeys; ++i) mb = fmaxf(mb, s[i >> 5][i & 31]);
             }
-            // the row's maximum over the whole block, from both halves (the two warps of
-            // a lane quarter; exchange slots of parity b)
-            float *xb = sX + 256 * b;
-            xb[128 * hf + r] = mb;
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar[q]);
-            if (!warp_wait(&xbar[q], (unsigned)j & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            __syncwarp();
-            mb = fmaxf(mb, xb[128 * (hf ^ 1) + r]) * sc;
+            mb *= sc;
             const bool resc = mb > m_used + 8.f;
             const float m_new = resc ? mb : m_used;
             const float factor = resc ? fast_exp2(m_used - m_new) : 1.f;
@@ -1015,61 +998,47 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     float o[32];
-                    tmem_ld32(tO + lb + 32u * c, o);
+                    tmem_ld32(tO + lb0 + 32u * c, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= factor;
-                    tmem_st32(tO + lb + 32u * c, o);
+                    tmem_st32(tO + lb0 + 32u * c, o);
                 }
             }
             l *= factor;
             m_used = m_new;
-            // P for keys 2c, 2c + 1 of this half in column c
-            uint32_t pk[32];
+            // P_j (keys 2c, 2c + 1 in column c) over the first 64 columns of S_j's buffer: this
+            // lane's S values are in registers, and P_{j-2} V_{j-2} (the buffer's previous P)
+            // completed before S_j was written
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float e0 = fast_exp2(fmaf(s[c >> 4][2 * (c & 15)], sc, -m_used));
-                const float e1 = fast_exp2(fmaf(s[c >> 4][2 * (c & 15) + 1], sc, -m_used));
-                l += e0;
-                l += e1;
-                __half2 h = __floats2half2_rn(e0, e1);
-                pk[c] = *reinterpret_cast<uint32_t *>(&h);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float e0 = fast_exp2(fmaf(s[2 * hf + (c >> 4)][2 * (c & 15)], sc, -m_used));
+                    const float e1 = fast_exp2(fmaf(s[2 * hf + (c >> 4)][2 * (c & 15) + 1], sc, -m_used));
+                    l += e0;
+                    l += e1;
+                    __half2 h = __floats2half2_rn(e0, e1);
+                    pk[c] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                tmem_st32u(tmem + lb0 + 128u * b + 32u * hf, pk);
             }
-            // the P columns are free once P_{j-1} V_{j-1} has completed
-            if (j > 0 && !warp_wait(pv_done, (unsigned)(j - 1) & 1u, abort)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            tmem_st32u(tmem + lb0 + kFaColP + 32u * hf, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-        }
-        // row sum over both halves (exchange slots of the parity after the last block)
-        if (ok) {
-            float *xb = sX + 256 * (nkb & 1);
-            xb[128 * hf + r] = l;
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar[q]);
-            ok = warp_wait(&xbar[q], (unsigned)nkb & 1u, abort);
-            if (ok) {
-                __syncwarp();
-                l += xb[128 * (hf ^ 1) + r];
-            }
         }
         if (ok && !warp_wait(pv_done, (unsigned)(nkb - 1) & 1u, abort)) ok = false;
         if (ok) {
             tc_fence_after();
             const float inv = 1.0f / l;
-            __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim + 64 * hf;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            __half *dst = p.o16 + (size_t)t * p.Hq * kHeadDim + (size_t)head * kHeadDim;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
                 float o[32];
-                tmem_ld32(tO + lb + 32u * c, o);
+                tmem_ld32(tO + lb0 + 32u * c, o);
                 if (t < p.n) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= inv;
