@@ -18,6 +18,7 @@
 #include <cmath>
 
 #include "qw_batch.h"
+#include "tc.cuh"
 
 namespace qw {
 namespace {
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) batch_attn_kernel(BatchAttn p
     constexpr int G = kBatchG;
     __shared__ float wml[kAttnWarps][G][2];
     __shared__ float wacc[kAttnWarps][G][kHeadDim];
+    tc::chain_wait();
+    tc::chain_release();
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = p.row_pos[b] + 1;  // cached positions including this step's row
@@ -118,6 +121,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) batch_attn_kernel(BatchAttn p
 // One (query head, sequence): o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), splits in order.
 __global__ void __launch_bounds__(kHeadDim) batch_merge_kernel(const float *part, int S, int Hq, __half *o16,
                                                                 int ldo) {
+    tc::chain_wait();
+    tc::chain_release();
     const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const float *src = part + ((size_t)b * Hq + hq) * S * kBatchPartStride;
     float mx = -INFINITY;
@@ -165,6 +170,8 @@ __global__ void __launch_bounds__(kBatchHeadThreads) batch_head_kernel(BatchHead
     extern __shared__ __align__(16) float hf[];  // [B][H]
     __shared__ unsigned long long best[kBatchHeadThreads / 32][kBatchMax];
     __shared__ int bad_any;
+    tc::chain_wait();
+    tc::chain_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = p.B;
     if (threadIdx.x == 0) bad_any = 0;
@@ -225,6 +232,8 @@ __global__ void __launch_bounds__(kBatchHeadThreads) batch_head_kernel(BatchHead
 }
 
 __global__ void batch_pick_kernel(unsigned long long *keys, int B, int32_t *picks) {
+    tc::chain_wait();
+    tc::chain_release();
     const int b = threadIdx.x;
     if (b >= B) return;
     const unsigned long long k = keys[b];
@@ -234,6 +243,8 @@ __global__ void batch_pick_kernel(unsigned long long *keys, int B, int32_t *pick
 
 // tokens[b] = the caller's token, or (-1) this sequence's previous device-resident pick
 __global__ void batch_tokens_kernel(const int32_t *in, const int32_t *picks, int B, int32_t *tokens) {
+    tc::chain_wait();
+    tc::chain_release();
     const int b = threadIdx.x;
     if (b < B) tokens[b] = in[b] >= 0 ? in[b] : picks[b];
 }
@@ -250,36 +261,28 @@ cudaError_t batch_prepare() {
                                 kBatchMax * 3072 * 4);
 }
 
-cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st) {
-    batch_tokens_kernel<<<1, 32, 0, st>>>(in, picks, B, tokens);
-    return cudaGetLastError();
+cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st,
+                                bool chained) {
+    return launch_k(chained, batch_tokens_kernel, dim3(1), dim3(32), 0, st, in, picks, B, tokens);
 }
 
-cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st) {
-    const dim3 grid(p.S, Hkv, B);
-    if (kv_f32)
-        batch_attn_kernel<float><<<grid, kAttnWarps * 32, 0, st>>>(p);
-    else
-        batch_attn_kernel<__nv_bfloat16><<<grid, kAttnWarps * 32, 0, st>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st, bool chained) {
+    const dim3 grid(p.S, Hkv, B), block(kAttnWarps * 32);
+    return kv_f32 ? launch_k(chained, batch_attn_kernel<float>, grid, block, 0, st, p)
+                  : launch_k(chained, batch_attn_kernel<__nv_bfloat16>, grid, block, 0, st, p);
 }
 
-cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *o16, int ldo, cudaStream_t st) {
-    batch_merge_kernel<<<dim3(Hq, B), kHeadDim, 0, st>>>(part, S, Hq, o16, ldo);
-    return cudaGetLastError();
+cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *o16, int ldo, cudaStream_t st,
+                               bool chained) {
+    return launch_k(chained, batch_merge_kernel, dim3(Hq, B), dim3(kHeadDim), 0, st, part, S, Hq, o16, ldo);
 }
 
-cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st) {
+cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st, bool chained) {
     const size_t smem = (size_t)p.B * H * 4;
-    const int grid = 4 * nsm;
-    switch (H >> 10) {
-        case 1: batch_head_kernel<1><<<grid, kBatchHeadThreads, smem, st>>>(p); break;
-        case 2: batch_head_kernel<2><<<grid, kBatchHeadThreads, smem, st>>>(p); break;
-        default: batch_head_kernel<3><<<grid, kBatchHeadThreads, smem, st>>>(p); break;
-    }
-    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    batch_pick_kernel<<<1, 32, 0, st>>>(p.keys, p.B, p.picks);
-    return cudaGetLastError();
+    auto k = H >> 10 == 1 ? batch_head_kernel<1> : H >> 10 == 2 ? batch_head_kernel<2> : batch_head_kernel<3>;
+    cudaError_t e = launch_k(chained, k, dim3(4 * nsm), dim3(kBatchHeadThreads), smem, st, p);
+    if (e != cudaSuccess) return e;
+    return launch_k(true, batch_pick_kernel, dim3(1), dim3(32), 0, st, p.keys, p.B, p.picks);
 }
 
 }  // namespace qw

@@ -1551,9 +1551,15 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
     const int S = batch_splits(bs.max_n);
     CUtensorMap mh, mo, ma;
     if (!make_map(&mh, h, B, H, BM) || !make_map(&mo, o16, B, QD, BM) || !make_map(&ma, act, B, I, BM)) return 1;
-    if (launch_batch_tokens(bs.tokens_in, bs.picks, B, bs.tokens, stream) != cudaSuccess) return 1;
-    launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream, false);
-    if (bs.hidden) cudaMemcpyAsync(bs.hidden, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, stream);
+    // chained launches (programmatic dependent launch) only directly after a kernel
+    if (launch_batch_tokens(bs.tokens_in, bs.picks, B, bs.tokens, stream, false) != cudaSuccess) return 1;
+    if (launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream, true) != cudaSuccess)
+        return 1;
+    bool ch = true;
+    if (bs.hidden) {
+        cudaMemcpyAsync(bs.hidden, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, stream);
+        ch = false;
+    }
     for (int l = 0; l < c.n_layers; ++l) {
         const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
         uint8_t *kc = reinterpret_cast<uint8_t *>(bs.kc) + (size_t)l * plane * esz;
@@ -1568,8 +1574,8 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         qo.q_norm = hl[l].q_norm;
         qo.k_norm = hl[l].k_norm;
         qo.rope = a.rope;
-            qo.rope_t = reinterpret_cast<const float2 *>(buf + L.rope_t);
-            qo.rope_ld = c.max_ctx;
+        qo.rope_t = reinterpret_cast<const float2 *>(buf + L.rope_t);
+        qo.rope_ld = c.max_ctx;
         qo.Hq = Hq;
         qo.Hkv = Hkv;
         qo.eps = a.eps;
@@ -1581,7 +1587,7 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         qo.max_ctx = bs.max_ctx;
         qo.row_pos = bs.row_pos;
         qo.seq_elems = bs.seq_elems;
-        if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream) != cudaSuccess) return 1;
+        if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream, ch) != cudaSuccess) return 1;
         BatchAttn ap{};
         ap.q16 = q16;
         ap.q_rows = st->rows_max;
@@ -1594,32 +1600,40 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         ap.Hq = Hq;
         ap.scale_log2 = kLog2e / sqrtf((float)kHeadDim);
         ap.part = bs.part;
-        if (launch_batch_attn(ap, Hkv, B, a.kv_f32, stream) != cudaSuccess) return 1;
-        if (launch_batch_merge(bs.part, S, Hq, B, o16, QD, stream) != cudaSuccess) return 1;
+        if (launch_batch_attn(ap, Hkv, B, a.kv_f32, stream, true) != cudaSuccess) return 1;
+        if (launch_batch_merge(bs.part, S, Hq, B, o16, QD, stream, true) != cudaSuccess) return 1;
         // x += o Wo^T
         gp.N = H;
         gp.K = QD;
         gp.out = x;
         gp.ldo = H;
-        if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream) != cudaSuccess) return 1;
-        launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream, false);
+        if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+        if (launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream, true) != cudaSuccess)
+            return 1;
         // a = silu(h Wg^T) * (h Wu^T)
         gp.N = 2 * I;
         gp.K = H;
         gp.act = act;
         gp.ldh = I;
-        if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream) != cudaSuccess) return 1;
+        if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream, true) != cudaSuccess) return 1;
         // x += a Wd^T
         gp.N = H;
         gp.K = I;
         gp.out = x;
         gp.ldo = H;
-        if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream) != cudaSuccess) return 1;
-        if (bs.hidden)
+        if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+        ch = true;
+        if (bs.hidden) {
             cudaMemcpyAsync(bs.hidden + (size_t)(l + 1) * B * H, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
                             stream);
-        if (l + 1 < c.n_layers)
-            launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream, false);
+            ch = false;
+        }
+        if (l + 1 < c.n_layers) {
+            if (launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream, ch) !=
+                cudaSuccess)
+                return 1;
+            ch = true;
+        }
     }
     BatchHead hp{};
     hp.x = x;
@@ -1632,7 +1646,7 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
     hp.keys = bs.keys;
     hp.picks = bs.picks;
     hp.flags = a.flags;
-    if (launch_batch_head(hp, H, st->nsm, stream) != cudaSuccess) return 1;
+    if (launch_batch_head(hp, H, st->nsm, stream, ch) != cudaSuccess) return 1;
     return cudaGetLastError() != cudaSuccess;
 }
 

@@ -38,10 +38,15 @@ struct BatchHead {
 };
 
 cudaError_t batch_prepare();
-cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st);
-cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st);
-cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *o16, int ldo, cudaStream_t st);
-cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st);
+// chained: launch with programmatic stream serialization (the previous operation of the
+// stream must be a kernel); every batched kernel waits for its predecessor's completion
+// before its first memory access.
+cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st,
+                                bool chained);
+cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st, bool chained);
+cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *o16, int ldo, cudaStream_t st,
+                               bool chained);
+cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st, bool chained);
 
 // Splits per (sequence, KV head) for a step whose longest sequence caches n positions.
 inline int batch_splits(int n) {
