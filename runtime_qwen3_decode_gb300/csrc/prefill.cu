@@ -291,11 +291,30 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, uint32_t tcol, int
     }
 }
 
+// The residual block an EPI_ADD epilogue warp updates (rows r0 .. r0 + 31, the tile's BN
+// columns) in the transposed staging order: y[c][it] = row 4 it + lane / 8, columns
+// c 32 + 4 (lane % 8) .. + 3.  Loaded before the accumulator is ready, it overlaps the
+// mainloop; the tile's region of out is written only by this epilogue.
+template <int BN>
+__device__ __forceinline__ void load_residual(const GemmParams &p, int r0, int nt, float4 (&y)[BN / 32][8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = 4 * it + (lane >> 3);
+            y[c][it] = r0 + r < p.M ? reinterpret_cast<const float4 *>(p.out + (size_t)(r0 + r) * p.ldo +
+                                                                        (size_t)nt * BN + 32 * c)[lane & 7]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+}
+
 // r0: the warp's first row (tile rows r0 .. r0 + 31); tacc: the accumulator buffer at the
-// warp's TMEM lane quarter; e: the warp's epilogue index; stg: its staging area.
+// warp's TMEM lane quarter; e: the warp's epilogue index; stg: its staging area; y: the
+// residual block (EPI_ADD).
 template <int BN, int EPI>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc, int r0, int nt, int e, float *stg,
-                                              const float *snorm) {
+                                              const float *snorm, const float4 (&y)[BN / 32][8]) {
     using C = GemmCfg<BN, EPI>;
     constexpr int SC = C::kStgCols;
     const int lane = threadIdx.x & 31;
@@ -327,20 +346,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
         }
     } else {
         static_assert(SC == 32, "the store / add epilogue reads 32-column blocks");
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < BN; c += 32) {
             float v[32];
-            float4 y[8];
-            if constexpr (EPI == EPI_ADD) {
-                // the residual block this lane updates, loaded before the accumulator is read
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int r = 4 * it + (lane >> 3);
-                    y[it] = r0 + r < p.M ? reinterpret_cast<const float4 *>(p.out + (size_t)(r0 + r) * p.ldo +
-                                                                             (size_t)nt * BN + c)[lane & 7]
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
             tmem_ld32(tacc + c, v);
             stage_rows<SC>(stg, v);
 #pragma unroll
@@ -349,10 +357,11 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tacc
                 float4 x = *reinterpret_cast<const float4 *>(stg + r * C::kStgStride + 4 * c4);
                 if (r0 + r >= p.M) continue;
                 if constexpr (EPI == EPI_ADD) {
-                    x.x += y[it].x;
-                    x.y += y[it].y;
-                    x.z += y[it].z;
-                    x.w += y[it].w;
+                    const float4 yv = y[c / 32][it];
+                    x.x += yv.x;
+                    x.y += yv.y;
+                    x.z += yv.z;
+                    x.w += yv.w;
                 }
                 reinterpret_cast<float4 *>(p.out + (size_t)(r0 + r) * p.ldo + (size_t)nt * BN + c)[c4] = x;
             }
@@ -513,6 +522,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::kThreads, 1)
         int acc = 0;
         unsigned aph = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const int mt = tile % tiles_m, nt = tile / tiles_m;
+            float4 y[BN / 32][8];
+            if constexpr (EPI == EPI_ADD) load_residual<BN>(p, mt * BM + q * 32, nt, y);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort, true, kWaitLimitNs);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -524,9 +536,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int mt = tile % tiles_m, nt = tile / tiles_m;
             const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32, nt, e, stg, snorm);
+            gemm_epilogue<BN, EPI>(p, tacc, mt * BM + q * 32, nt, e, stg, snorm, y);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
