@@ -218,11 +218,12 @@ void qw_model_destroy(qw_model *m);
  * and length, decoded together one token per sequence per step ("Portable WebAssembly
  * Runtime Architecture for TinyRustLM", sections "Threads, Scheduling" and "Prefill
  * versus decode"; each sequence computes exactly the decode step of the single-sequence
- * calls).  The B rows of a step run through the batched prefill's tensor-core GEMMs
- * (fp16 operands, f32 accumulation, M = B), per-sequence split attention over each
- * cache, and one pass of the tied lm_head for all rows; the cache uses the model's
- * format.  Requires the batched prefill (qw_prefill's tensor-core path) to be available
- * and query heads = 2 x KV heads; max_ctx <= the model's max_ctx.
+ * calls).  The B rows of a step run through skinny projections that read every weight
+ * row once for all B rows (the batched prefill's fp16 weight copy, f32 accumulation),
+ * per-sequence split attention over each cache, and one pass of the tied lm_head for
+ * all rows; the cache uses the model's format.  Requires the batched prefill
+ * (qw_prefill's tensor-core path, which holds that weight copy) to be available and
+ * query heads = 2 x KV heads; max_ctx <= the model's max_ctx.
  *
  * Workspace: caller-owned device memory of qw_batch_workspace_bytes (256-byte aligned),
  * holding every sequence's cache ([n_layers][n_kv_heads][max_ctx][head_dim] K and V

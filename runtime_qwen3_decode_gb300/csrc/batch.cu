@@ -3,8 +3,11 @@
 // Scheduling" and "Prefill versus decode": every sequence runs the decode step of "Scalar-Native
 // Qwen3 Reference Runtime As The Numerical Authority", section 2, on its own K/V cache).
 //
-// The projections and the MLP of the B rows run as tensor-core GEMMs with M = B (prefill.cu,
-// prefill_batch_step); here are the parts that differ per sequence:
+// The step itself is sequenced by prefill_batch_step (prefill.cu); its kernels are here:
+//   bgemv_kernel        the projections and the MLP of the B rows: every weight row read once
+//                       and dotted with all B activation rows (residual add or SwiGLU fused)
+//   bqkv_post_kernel    QK-Norm and RoPE of each sequence's q and k heads at its own position,
+//                       q into the fp16 query rows, k and v appended to its own cache
 //   batch_attn_kernel   GQA attention of each sequence's new query rows over its own cache,
 //                       split over positions (one CTA per (split, KV head, sequence)), online
 //                       softmax, a partial (acc, max, sum) per query head and split
@@ -24,6 +27,7 @@ namespace qw {
 namespace {
 
 constexpr int kAttnWarps = 8;
+constexpr int kGemvWarps = 8;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -35,6 +39,161 @@ template <typename KT>
 __device__ __forceinline__ float to_f(KT v) {
     if constexpr (sizeof(KT) == 4) return v;
     else return __bfloat162float(v);
+}
+
+// ------------------------------------------------------------------ skinny projections
+//
+// y[b][r] = sum_k W[r][k] a[b][k] for the B <= 8 rows of a step.  With M = B the work is a
+// matrix-vector product per row: its bound is the weight bytes, each read once from HBM.
+// Every CTA stages the B activation rows (fp16) in shared memory; a warp takes two weight
+// rows per step (rows 2u, 2u + 1, or the gate and up rows of output u), issues all of
+// their 16-byte loads before the arithmetic, accumulates f32 dot products with all B rows
+// (lane l owns the 8-element chunks l + 32 c), and reduces the 2 x 8 sums with a
+// transposed butterfly.  Every output element has one owner: no atomics, the same
+// result every run.
+
+// Lane l of the warp ends with sum over lanes of v[i] for i = 8 b4 + 4 b3 + 2 b2 + b1,
+// b_k = bit k of l (lanes l and l ^ 1 hold the same sum): 9 shuffles for 16 sums.
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int s = 16, m = 8; m >= 1; s >>= 1, m >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < m; ++i) {
+            const float send = upper ? v[i] : v[i + m];
+            const float keep = upper ? v[i + m] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+__device__ __forceinline__ void half8_to_f(const uint4 &u, float (&f)[8]) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int EPI, int KC>  // KC = K / 256: 16-byte chunks per lane and row
+__global__ void __launch_bounds__(kGemvWarps * 32) bgemv_kernel(const BatchGemv p) {
+    extern __shared__ __align__(16) uint4 sa[];  // [B][K / 8] activation rows, 8 fp16 per entry
+    tc::chain_wait();
+    tc::chain_release();
+    constexpr int K8 = KC * 32;
+    const int B = p.B;
+    for (int i = threadIdx.x; i < B * K8; i += kGemvWarps * 32) sa[i] = reinterpret_cast<const uint4 *>(p.a)[i];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = EPI == BG_SWIGLU ? p.N : p.N / 2;
+    for (int u = blockIdx.x * kGemvWarps + warp; u < units; u += gridDim.x * kGemvWarps) {
+        // SWIGLU: gate row i of the interleaved weights is (i / 128) 256 + i % 128, up row +128
+        const int r0 = EPI == BG_SWIGLU ? (u >> 7) * 256 + (u & 127) : 2 * u;
+        const int r1 = EPI == BG_SWIGLU ? r0 + 128 : r0 + 1;
+        const uint4 *w0 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r0 * K8 + lane;
+        const uint4 *w1 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r1 * K8 + lane;
+        uint4 x0[KC], x1[KC];
+#pragma unroll
+        for (int c = 0; c < KC; ++c) {
+            x0[c] = ld_stream(w0 + 32 * c);
+            x1[c] = ld_stream(w1 + 32 * c);
+        }
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < KC; ++c) {
+            float f0[8], f1[8];
+            half8_to_f(x0[c], f0);
+            half8_to_f(x1[c], f1);
+#pragma unroll
+            for (int b = 0; b < kBatchMax; ++b) {
+                if (b < B) {
+                    float av[8];
+                    half8_to_f(sa[b * K8 + lane + 32 * c], av);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc[b] = fmaf(f0[e], av[e], acc[b]);
+                        acc[8 + b] = fmaf(f1[e], av[e], acc[8 + b]);
+                    }
+                }
+            }
+        }
+        const float v = warp_sum16(acc, lane);
+        const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+        const float other = __shfl_xor_sync(0xffffffffu, v, 16);  // idx ^ 8: the other row's sum
+        const int b = idx & 7;
+        if ((lane & 1) || b >= B) continue;
+        if constexpr (EPI == BG_SWIGLU) {
+            if (idx < 8) {  // g = v, u = other; SiLU(g) u as in the prefill epilogue
+                const float g = v;
+                p.act[(size_t)b * p.ldh + u] = __float2half_rn(__fdividef(g, 1.0f + __expf(-g)) * other);
+            }
+        } else {
+            const int row = idx < 8 ? r0 : r1;
+            float *o = p.out + (size_t)b * p.ldo + row;
+            if constexpr (EPI == BG_ADD) *o += v;
+            else *o = v;
+        }
+    }
+}
+
+// One (head slot, sequence): the raw q|k|v projection of the sequence's row -> QK-Norm and
+// RoPE for q and k heads at the sequence's position (the decode kernel's arithmetic:
+// r = rsqrt(mean(v^2) + eps), v = w * (v * r), dims (i, i + 64) rotated), q into the fp16
+// query row, k and v into the sequence's cache at that position.  Lane l holds dims l + 32 j.
+template <typename KT>
+__global__ void __launch_bounds__(32) bqkv_post_kernel(const BatchQkvPost p) {
+    tc::chain_wait();
+    tc::chain_release();
+    const int slot = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+    const int QD = p.Hq * kHeadDim, W = QD + 2 * p.Hkv * kHeadDim;
+    const bool is_q = slot < p.Hq, is_k = !is_q && slot < p.Hq + p.Hkv;
+    const float *src = p.qkv + (size_t)b * W + (size_t)slot * kHeadDim;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = src[lane + 32 * j];
+    const int pos = p.row_pos[b];
+    if (is_q || is_k) {
+        const __nv_bfloat16 *w = is_q ? p.q_norm : p.k_norm;
+        const float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+        const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __bfloat162float(w[lane + 32 * j]) * (v[j] * r);
+        const float2 *cs = p.rope + (size_t)pos * (kHeadDim / 2);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // pairs (lane + 32 j, lane + 32 j + 64)
+            const float2 c = cs[lane + 32 * j];
+            const float a = v[j], bb = v[j + 2];
+            v[j] = a * c.x - bb * c.y;
+            v[j + 2] = bb * c.x + a * c.y;
+        }
+    }
+    if (is_q) {
+        __half *dst = p.q16 + ((size_t)slot * p.q_rows + b) * kHeadDim;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = __float2half_rn(v[j]);
+        return;
+    }
+    const int kvh = is_k ? slot - p.Hq : slot - p.Hq - p.Hkv;
+    KT *dst = reinterpret_cast<KT *>(is_k ? p.kc : p.vc) + (size_t)b * p.seq_elems +
+              ((size_t)kvh * p.max_ctx + pos) * kHeadDim;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (sizeof(KT) == 4) dst[lane + 32 * j] = v[j];
+        else dst[lane + 32 * j] = __float2bfloat16_rn(v[j]);
+    }
 }
 
 // One (split, KV head, sequence).  Warp w takes positions p0 + w, p0 + w + 8, ...; lane L holds
@@ -251,14 +410,56 @@ __global__ void batch_tokens_kernel(const int32_t *in, const int32_t *picks, int
 
 }  // namespace
 
+template <int EPI>
+cudaError_t set_bgemv_attr() {
+    const int smem = kBatchMax * 6144 * 2;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(bgemv_kernel<EPI, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) ||
+        (e = cudaFuncSetAttribute(bgemv_kernel<EPI, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) ||
+        (e = cudaFuncSetAttribute(bgemv_kernel<EPI, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) ||
+        (e = cudaFuncSetAttribute(bgemv_kernel<EPI, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) ||
+        (e = cudaFuncSetAttribute(bgemv_kernel<EPI, 24>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
+        return e;
+    return cudaSuccess;
+}
+
 cudaError_t batch_prepare() {
     cudaError_t e = cudaFuncSetAttribute(batch_head_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBatchMax * 1024 * 4);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(batch_head_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBatchMax * 2048 * 4);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(batch_head_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kBatchMax * 3072 * 4);
+    e = cudaFuncSetAttribute(batch_head_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBatchMax * 3072 * 4);
+    if (e != cudaSuccess) return e;
+    if ((e = set_bgemv_attr<BG_STORE>()) != cudaSuccess || (e = set_bgemv_attr<BG_ADD>()) != cudaSuccess) return e;
+    return set_bgemv_attr<BG_SWIGLU>();
+}
+
+template <int EPI>
+cudaError_t launch_bgemv_k(const BatchGemv &p, int nsm, cudaStream_t st, bool chained) {
+    const size_t smem = (size_t)p.B * p.K * 2;
+    const dim3 grid(2 * nsm), block(kGemvWarps * 32);
+    switch (p.K) {
+        case 1024: return launch_k(chained, bgemv_kernel<EPI, 4>, grid, block, smem, st, p);
+        case 2048: return launch_k(chained, bgemv_kernel<EPI, 8>, grid, block, smem, st, p);
+        case 3072: return launch_k(chained, bgemv_kernel<EPI, 12>, grid, block, smem, st, p);
+        case 4096: return launch_k(chained, bgemv_kernel<EPI, 16>, grid, block, smem, st, p);
+        case 6144: return launch_k(chained, bgemv_kernel<EPI, 24>, grid, block, smem, st, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_bgemv(int epi, const BatchGemv &p, int nsm, cudaStream_t st, bool chained) {
+    if (p.B < 1 || p.B > kBatchMax || p.N < 1 || (epi != BG_SWIGLU && (p.N & 1))) return cudaErrorInvalidValue;
+    return epi == BG_STORE ? launch_bgemv_k<BG_STORE>(p, nsm, st, chained)
+           : epi == BG_ADD ? launch_bgemv_k<BG_ADD>(p, nsm, st, chained)
+                           : launch_bgemv_k<BG_SWIGLU>(p, nsm, st, chained);
+}
+
+cudaError_t launch_bqkv_post(const BatchQkvPost &p, int kv_f32, cudaStream_t st, bool chained) {
+    const dim3 grid(p.Hq + 2 * p.Hkv, p.B), block(32);
+    return kv_f32 ? launch_k(chained, bqkv_post_kernel<float>, grid, block, 0, st, p)
+                  : launch_k(chained, bqkv_post_kernel<__nv_bfloat16>, grid, block, 0, st, p);
 }
 
 cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st,

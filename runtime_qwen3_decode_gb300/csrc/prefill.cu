@@ -64,10 +64,6 @@ struct QkvOut {
     int kv_f32, max_ctx;
     __half *k16, *v16t;                    // fp16 shadows [Hkv][kv_rows][128] and [Hkv][128][kv_rows] (or null)
     int kv_rows;
-    // batched decode: row t is the new position row_pos[t] of sequence t, whose cache planes sit
-    // t * seq_elems elements after kc / vc; null for a prompt (row t at position pos0 + t)
-    const int *row_pos;
-    size_t seq_elems;
 };
 
 struct GemmParams {
@@ -205,9 +201,7 @@ __device__ __forceinline__ void qkv_put32(const QkvOut &o, float (&v)[32], int d
                 *reinterpret_cast<uint2 *>(o.q16 + ((size_t)slot * o.q_rows + tr) * kHeadDim + d) = pack_half4(x);
                 return;
             }
-            const size_t prow = (o.row_pos ? (size_t)tr * o.seq_elems + (size_t)o.row_pos[tr] * kHeadDim
-                                           : (size_t)(o.pos0 + tr) * kHeadDim) +
-                                d;
+            const size_t prow = (size_t)(o.pos0 + tr) * kHeadDim + d;
             if constexpr (sizeof(KT) == 4) {
                 *reinterpret_cast<float4 *>(cache + prow) = x;
             } else {
@@ -221,8 +215,7 @@ __device__ __forceinline__ void qkv_put32(const QkvOut &o, float (&v)[32], int d
     }
     // V^T shadow: for each dim the warp's 32 rows are 32 consecutive positions (64 B)
     if (!is_q && !is_k && t < M && o.v16t) {
-        const int P = o.row_pos ? o.row_pos[t] : o.pos0 + t;
-        __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + P + (size_t)d0 * o.kv_rows;
+        __half *dst = o.v16t + (size_t)kvh * kHeadDim * o.kv_rows + o.pos0 + t + (size_t)d0 * o.kv_rows;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             float x = v[i];
@@ -262,7 +255,7 @@ __device__ __forceinline__ void qkv_head_out(const QkvOut &o, uint32_t tcol, int
         for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
     }
     const float r = rsqrtf(ss * (1.0f / kHeadDim) + o.eps);
-    const int P = o.row_pos ? (t < M ? o.row_pos[t] : 0) : o.pos0 + t;
+    const int P = o.pos0 + t;
     // frequency-major table: for each frequency the warp's 32 rows read 32 consecutive
     // positions (one coalesced request) instead of 32 rows 512 bytes apart
     const float2 *cs = o.rope_t + min(P, o.max_ctx - 1);
@@ -1245,7 +1238,7 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 size_t align_up(size_t v) { return (v + 255) / 256 * 256; }
 
 struct PrefillLayout {
-    size_t w16, x, h, q16, o16, act, k16, v16t, tok, misc, rope_t, total;
+    size_t w16, x, h, q16, o16, act, k16, v16t, tok, misc, rope_t, bqkv, total;
     size_t w_layer;  // fp16 weight elements per layer
     int kv_rows;     // positions per head in the fp16 K / V^T shadows (max_ctx rounded up to 128)
 };
@@ -1273,6 +1266,7 @@ PrefillLayout prefill_layout(const qw_config &c, int rows) {
     L.tok = take((size_t)rows * 4);
     L.misc = take(64);
     L.rope_t = take((size_t)c.max_ctx * (c.head_dim / 2) * sizeof(float2));
+    L.bqkv = take((size_t)kBatchMax * (QD + 2 * KD) * 4);  // batched decode: raw q|k|v rows (f32)
     L.total = off;
     return L;
 }
@@ -1560,8 +1554,7 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
     const size_t plane = (size_t)Hkv * bs.max_ctx * kHeadDim;  // elements of one layer's K (or V) plane
     const DevLayer *hl = im->host_layers.data();
     const int S = batch_splits(bs.max_n);
-    CUtensorMap mh, mo, ma;
-    if (!make_map(&mh, h, B, H, BM) || !make_map(&mo, o16, B, QD, BM) || !make_map(&ma, act, B, I, BM)) return 1;
+    float *qkv_raw = reinterpret_cast<float *>(buf + L.bqkv);
     // chained launches (programmatic dependent launch) only directly after a kernel
     if (launch_batch_tokens(bs.tokens_in, bs.picks, B, bs.tokens, stream, false) != cudaSuccess) return 1;
     if (launch_norm_rows(x, bs.tokens, a.embed, hl[0].input_norm, h, B, H, a.eps, stream, true) != cudaSuccess)
@@ -1572,33 +1565,39 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         ch = false;
     }
     for (int l = 0; l < c.n_layers; ++l) {
-        const CUtensorMap *wm = &im->wmaps[(size_t)l * 4];
+        // this layer's fp16 weights (converted once by prefill_init)
+        const __half *wqkv = reinterpret_cast<const __half *>(buf + L.w16) + (size_t)l * L.w_layer;
+        const __half *wo = wqkv + (size_t)(QD + 2 * KD) * H, *wgu = wo + (size_t)H * QD, *wd = wgu + (size_t)2 * I * H;
         uint8_t *kc = reinterpret_cast<uint8_t *>(bs.kc) + (size_t)l * plane * esz;
         uint8_t *vc = reinterpret_cast<uint8_t *>(bs.vc) + (size_t)l * plane * esz;
-        GemmParams gp{};
-        gp.flags = a.flags;
-        gp.M = B;
-        // q | k | v: QK-Norm, RoPE at each sequence's position, K/V rows into each sequence's cache
-        gp.N = QD + 2 * KD;
-        gp.K = H;
-        QkvOut &qo = gp.qkv;
-        qo.q_norm = hl[l].q_norm;
-        qo.k_norm = hl[l].k_norm;
-        qo.rope = a.rope;
-        qo.rope_t = reinterpret_cast<const float2 *>(buf + L.rope_t);
-        qo.rope_ld = c.max_ctx;
-        qo.Hq = Hq;
-        qo.Hkv = Hkv;
-        qo.eps = a.eps;
-        qo.q16 = q16;
-        qo.q_rows = st->rows_max;
-        qo.kc = kc;
-        qo.vc = vc;
-        qo.kv_f32 = a.kv_f32;
-        qo.max_ctx = bs.max_ctx;
-        qo.row_pos = bs.row_pos;
-        qo.seq_elems = bs.seq_elems;
-        if (launch_gemm<256, EPI_QKV>(mh, wm[0], gp, st->nsm, stream, ch) != cudaSuccess) return 1;
+        // q | k | v of the B rows, then QK-Norm, RoPE at each sequence's position, K/V rows into
+        // each sequence's cache
+        BatchGemv g{};
+        g.B = B;
+        g.W = wqkv;
+        g.a = h;
+        g.N = QD + 2 * KD;
+        g.K = H;
+        g.out = qkv_raw;
+        g.ldo = QD + 2 * KD;
+        if (launch_bgemv(BG_STORE, g, st->nsm, stream, ch) != cudaSuccess) return 1;
+        BatchQkvPost qp{};
+        qp.qkv = qkv_raw;
+        qp.q_norm = hl[l].q_norm;
+        qp.k_norm = hl[l].k_norm;
+        qp.rope = a.rope;
+        qp.row_pos = bs.row_pos;
+        qp.B = B;
+        qp.Hq = Hq;
+        qp.Hkv = Hkv;
+        qp.eps = a.eps;
+        qp.q16 = q16;
+        qp.q_rows = st->rows_max;
+        qp.kc = kc;
+        qp.vc = vc;
+        qp.seq_elems = bs.seq_elems;
+        qp.max_ctx = bs.max_ctx;
+        if (launch_bqkv_post(qp, a.kv_f32, stream, true) != cudaSuccess) return 1;
         BatchAttn ap{};
         ap.q16 = q16;
         ap.q_rows = st->rows_max;
@@ -1614,25 +1613,31 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         if (launch_batch_attn(ap, Hkv, B, a.kv_f32, stream, true) != cudaSuccess) return 1;
         if (launch_batch_merge(bs.part, S, Hq, B, o16, QD, stream, true) != cudaSuccess) return 1;
         // x += o Wo^T
-        gp.N = H;
-        gp.K = QD;
-        gp.out = x;
-        gp.ldo = H;
-        if (launch_gemm<128, EPI_ADD>(mo, wm[1], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+        g.W = wo;
+        g.a = o16;
+        g.N = H;
+        g.K = QD;
+        g.out = x;
+        g.ldo = H;
+        if (launch_bgemv(BG_ADD, g, st->nsm, stream, true) != cudaSuccess) return 1;
         if (launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream, true) != cudaSuccess)
             return 1;
         // a = silu(h Wg^T) * (h Wu^T)
-        gp.N = 2 * I;
-        gp.K = H;
-        gp.act = act;
-        gp.ldh = I;
-        if (launch_gemm<256, EPI_SWIGLU>(mh, wm[2], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+        g.W = wgu;
+        g.a = h;
+        g.N = I;
+        g.K = H;
+        g.act = act;
+        g.ldh = I;
+        if (launch_bgemv(BG_SWIGLU, g, st->nsm, stream, true) != cudaSuccess) return 1;
         // x += a Wd^T
-        gp.N = H;
-        gp.K = I;
-        gp.out = x;
-        gp.ldo = H;
-        if (launch_gemm<128, EPI_ADD>(ma, wm[3], gp, st->nsm, stream, true) != cudaSuccess) return 1;
+        g.W = wd;
+        g.a = act;
+        g.N = H;
+        g.K = I;
+        g.out = x;
+        g.ldo = H;
+        if (launch_bgemv(BG_ADD, g, st->nsm, stream, true) != cudaSuccess) return 1;
         ch = true;
         if (bs.hidden) {
             cudaMemcpyAsync(bs.hidden + (size_t)(l + 1) * B * H, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,

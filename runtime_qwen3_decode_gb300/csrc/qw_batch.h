@@ -14,6 +14,34 @@ constexpr int kBatchHeadThreads = 256;
 constexpr int kBatchSplitRows = 128;    // cached positions per attention split (at most)
 constexpr int kBatchMaxSplits = 64;
 
+// Skinny projection of the B rows: y[b][r] = sum_k W[r][k] a[b][k] (bgemv_kernel).
+enum { BG_STORE = 0, BG_ADD = 1, BG_SWIGLU = 2 };
+
+struct BatchGemv {
+    const __half *W;       // [rows][K] fp16; BG_SWIGLU: gate/up rows interleaved in 128-row blocks
+    const __half *a;       // [B][K] fp16 activation rows
+    int B, N, K;           // N outputs (BG_STORE / BG_ADD: even); K in {1024, 2048, 3072, 4096, 6144}
+    float *out;            // BG_STORE: out[b][n] = y; BG_ADD: out[b][n] += y
+    int ldo;
+    __half *act;           // BG_SWIGLU: act[b][n] = silu(gate_n . a_b) (up_n . a_b)
+    int ldh;
+};
+
+// QK-Norm, RoPE and the K/V append of the B rows' raw q|k|v projections (bqkv_post_kernel).
+struct BatchQkvPost {
+    const float *qkv;                        // [B][Hq 128 + 2 Hkv 128]
+    const __nv_bfloat16 *q_norm, *k_norm;    // [128] each
+    const float2 *rope;                      // [max positions][64] (cos, sin)
+    const int *row_pos;                      // [B] each sequence's position this step
+    int B, Hq, Hkv;
+    float eps;
+    __half *q16;                             // [Hq][q_rows][128]: row b = sequence b's query heads
+    int q_rows;
+    void *kc, *vc;                           // this layer's planes of sequence 0: [Hkv][max_ctx][128]
+    size_t seq_elems;                        // elements from one sequence's cache to the next one's
+    int max_ctx;
+};
+
 struct BatchAttn {
     const __half *q16;    // [Hq][q_rows][128]: row b = sequence b's rotated query heads
     int q_rows;
@@ -41,6 +69,8 @@ cudaError_t batch_prepare();
 // chained: launch with programmatic stream serialization (the previous operation of the
 // stream must be a kernel); every batched kernel waits for its predecessor's completion
 // before its first memory access.
+cudaError_t launch_bgemv(int epi, const BatchGemv &p, int nsm, cudaStream_t st, bool chained);
+cudaError_t launch_bqkv_post(const BatchQkvPost &p, int kv_f32, cudaStream_t st, bool chained);
 cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st,
                                 bool chained);
 cudaError_t launch_batch_attn(const BatchAttn &p, int Hkv, int B, int kv_f32, cudaStream_t st, bool chained);

@@ -34,8 +34,9 @@ int prefill_run(PrefillState *st, const DecodeArgs &a, int pos0, const int32_t *
 // One batched decode step: B sequences, one new token each (their tokens resolved on the device:
 // -1 takes the sequence's previous pick).  Sequence b's cache is the block of seq_elems elements
 // starting seq_elems * b after kc / vc ([L][Hkv][max_ctx][128]); its new row goes to position
-// row_pos[b].  The B rows run through the tensor-core GEMMs of the prefill (M = B) and the
-// batched attention and head kernels of batch.cu; logits [B][V] and picks [B] come out.
+// row_pos[b].  The B rows run through the skinny projections (every fp16 weight row of the
+// prefill's converted copy read once for all B rows), the batched attention and the head
+// kernels of batch.cu; logits [B][V] and picks [B] come out.
 struct BatchStep {
     int B;
     const int32_t *tokens_in;  // device [B]: token or -1
