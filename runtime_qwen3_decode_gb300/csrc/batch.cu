@@ -45,12 +45,14 @@ __device__ __forceinline__ float to_f(KT v) {
 //
 // y[b][r] = sum_k W[r][k] a[b][k] for the B <= 8 rows of a step.  With M = B the work is a
 // matrix-vector product per row: its bound is the weight bytes, each read once from HBM.
-// Every CTA stages the B activation rows (fp16) in shared memory; a warp takes two weight
-// rows per step (rows 2u, 2u + 1, or the gate and up rows of output u), issues all of
-// their 16-byte loads before the arithmetic, accumulates f32 dot products with all B rows
-// (lane l owns the 8-element chunks l + 32 c), and reduces the 2 x 8 sums with a
-// transposed butterfly.  Every output element has one owner: no atomics, the same
-// result every run.
+// Every CTA stages the B activation rows (fp16) in shared memory.  A unit is two weight
+// rows (rows 2u, 2u + 1, or the gate and up rows of output u); a group of KS warps takes a
+// unit, each warp 1/KS of K (KS = 4 from K = 2048 up, else 1, so that a warp has at least
+// two chunks per row and the short rows keep one warp per unit): it issues all of its
+// 16-byte weight loads before the arithmetic, accumulates f32 dot products with all B
+// rows (lane l owns the 8-element chunks l + 32 c of its part) and reduces its 2 x 8 sums
+// with a transposed butterfly; the group's partial sums are then added in a fixed order.  Every output element has
+// one owner: no atomics, the same result every run.
 
 // Lane l of the warp ends with sum over lanes of v[i] for i = 8 b4 + 4 b3 + 2 b2 + b1,
 // b_k = bit k of l (lanes l and l ^ 1 hold the same sum): 9 shuffles for 16 sums.
@@ -88,64 +90,83 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
 
 template <int EPI, int KC>  // KC = K / 256: 16-byte chunks per lane and row
 __global__ void __launch_bounds__(kGemvWarps * 32) bgemv_kernel(const BatchGemv p) {
-    extern __shared__ __align__(16) uint4 sa[];  // [B][K / 8] activation rows, 8 fp16 per entry
+    constexpr int KS = KC >= 8 ? 4 : 1, NG = kGemvWarps / KS;  // warps per unit; units per pass
+    static_assert(KC % KS == 0 && kGemvWarps % KS == 0, "the warps of a unit split K evenly");
+    constexpr int K8 = KC * 32, KQ = KC / KS;  // row length in uint4; chunks per lane and warp
+    extern __shared__ __align__(16) uint4 sa[];  // [B][K8] activation rows, 8 fp16 per entry
+    __shared__ float part[NG][KS][16];            // [unit of the pass][K part][value]
     tc::chain_wait();
     tc::chain_release();
-    constexpr int K8 = KC * 32;
     const int B = p.B;
     for (int i = threadIdx.x; i < B * K8; i += kGemvWarps * 32) sa[i] = reinterpret_cast<const uint4 *>(p.a)[i];
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, grp = warp / KS, kq = warp % KS;
     const int units = EPI == BG_SWIGLU ? p.N : p.N / 2;
-    for (int u = blockIdx.x * kGemvWarps + warp; u < units; u += gridDim.x * kGemvWarps) {
+    for (int base = NG * blockIdx.x; base < units; base += NG * gridDim.x) {  // uniform over the CTA
+        const int u = base + grp;
         // SWIGLU: gate row i of the interleaved weights is (i / 128) 256 + i % 128, up row +128
         const int r0 = EPI == BG_SWIGLU ? (u >> 7) * 256 + (u & 127) : 2 * u;
         const int r1 = EPI == BG_SWIGLU ? r0 + 128 : r0 + 1;
-        const uint4 *w0 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r0 * K8 + lane;
-        const uint4 *w1 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r1 * K8 + lane;
-        uint4 x0[KC], x1[KC];
-#pragma unroll
-        for (int c = 0; c < KC; ++c) {
-            x0[c] = ld_stream(w0 + 32 * c);
-            x1[c] = ld_stream(w1 + 32 * c);
-        }
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        if (u < units) {
+            const int c0 = lane + 32 * KQ * kq;  // this warp's first chunk of the row
+            const uint4 *w0 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r0 * K8 + c0;
+            const uint4 *w1 = reinterpret_cast<const uint4 *>(p.W) + (size_t)r1 * K8 + c0;
+            uint4 x0[KQ], x1[KQ];
 #pragma unroll
-        for (int c = 0; c < KC; ++c) {
-            float f0[8], f1[8];
-            half8_to_f(x0[c], f0);
-            half8_to_f(x1[c], f1);
+            for (int c = 0; c < KQ; ++c) {
+                x0[c] = ld_stream(w0 + 32 * c);
+                x1[c] = ld_stream(w1 + 32 * c);
+            }
 #pragma unroll
-            for (int b = 0; b < kBatchMax; ++b) {
-                if (b < B) {
-                    float av[8];
-                    half8_to_f(sa[b * K8 + lane + 32 * c], av);
+            for (int c = 0; c < KQ; ++c) {
+                float f0[8], f1[8];
+                half8_to_f(x0[c], f0);
+                half8_to_f(x1[c], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc[b] = fmaf(f0[e], av[e], acc[b]);
-                        acc[8 + b] = fmaf(f1[e], av[e], acc[8 + b]);
+                for (int b = 0; b < kBatchMax; ++b) {
+                    if (b < B) {
+                        float av[8];
+                        half8_to_f(sa[b * K8 + c0 + 32 * c], av);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc[b] = fmaf(f0[e], av[e], acc[b]);
+                            acc[8 + b] = fmaf(f1[e], av[e], acc[8 + b]);
+                        }
                     }
                 }
             }
         }
         const float v = warp_sum16(acc, lane);
-        const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-        const float other = __shfl_xor_sync(0xffffffffu, v, 16);  // idx ^ 8: the other row's sum
-        const int b = idx & 7;
-        if ((lane & 1) || b >= B) continue;
-        if constexpr (EPI == BG_SWIGLU) {
-            if (idx < 8) {  // g = v, u = other; SiLU(g) u as in the prefill epilogue
-                const float g = v;
-                p.act[(size_t)b * p.ldh + u] = __float2half_rn(__fdividef(g, 1.0f + __expf(-g)) * other);
-            }
-        } else {
-            const int row = idx < 8 ? r0 : r1;
-            float *o = p.out + (size_t)b * p.ldo + row;
-            if constexpr (EPI == BG_ADD) *o += v;
-            else *o = v;
+        if ((lane & 1) == 0) {
+            const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+            part[grp][kq][idx] = v;
         }
+        if (KS > 1) __syncthreads();
+        else __syncwarp();
+        if (u < units && kq == 0 && lane < 16) {  // value lane: row (lane < 8 ? r0 : r1), sequence lane % 8
+            const int b = lane & 7;
+            float y = 0.f, up = 0.f;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                y += part[grp][k][lane];
+                if (EPI == BG_SWIGLU && lane < 8) up += part[grp][k][lane + 8];
+            }
+            if constexpr (EPI == BG_SWIGLU) {
+                if (lane < 8 && b < B) {  // g = y (gate row), up from value lane + 8
+                    // SiLU(g) u as in the prefill epilogue
+                    p.act[(size_t)b * p.ldh + u] = __float2half_rn(__fdividef(y, 1.0f + __expf(-y)) * up);
+                }
+            } else if (b < B) {
+                float *o = p.out + (size_t)b * p.ldo + (lane < 8 ? r0 : r1);
+                if constexpr (EPI == BG_ADD) *o += y;
+                else *o = y;
+            }
+        }
+        if (KS > 1) __syncthreads();  // part is rewritten by the next pass
+        else __syncwarp();
     }
 }
 
@@ -345,38 +366,61 @@ __global__ void __launch_bounds__(kBatchHeadThreads) batch_head_kernel(BatchHead
     unsigned long long kbest = 0;  // for value lane / 4 (a sequence)
     bool bad = false;
     const int gw = blockIdx.x * (kBatchHeadThreads / 32) + warp, nw = gridDim.x * (kBatchHeadThreads / 32);
-    for (int vr = gw; vr < p.V; vr += nw) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(p.E + (size_t)vr * H);
-        uint4 u[NC];
+    // two rows per pass (vr and vr + nw): every normalised value read from shared memory
+    // serves both, and all loads of both rows are issued before the arithmetic
+    for (int v0 = gw; v0 < p.V; v0 += 2 * nw) {
+        const int v1 = v0 + nw < p.V ? v0 + nw : v0;
+        const uint4 *row0 = reinterpret_cast<const uint4 *>(p.E + (size_t)v0 * H);
+        const uint4 *row1 = reinterpret_cast<const uint4 *>(p.E + (size_t)v1 * H);
+        uint4 u0[NC], u1[NC];
 #pragma unroll
-        for (int i = 0; i < NC; ++i) u[i] = __ldg(row + lane + 32 * i);
-        float acc[8];
+        for (int i = 0; i < NC; ++i) {
+            u0[i] = __ldg(row0 + lane + 32 * i);
+            u1[i] = __ldg(row1 + lane + 32 * i);
+        }
+        float acc0[8], acc1[8];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc[b] = 0.f;
+        for (int b = 0; b < 8; ++b) acc0[b] = acc1[b] = 0.f;
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
             const int c = 8 * (lane + 32 * i);
-            const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&u[i]);
-            float2 w[4];
+            float w0[8], w1[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = __bfloat1622float2(w2[e]);
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&u0[i])[e]);
+                const float2 bq = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&u1[i])[e]);
+                w0[2 * e] = a.x;
+                w0[2 * e + 1] = a.y;
+                w1[2 * e] = bq.x;
+                w1[2 * e + 1] = bq.y;
+            }
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 if (b < B) {
                     const float4 h0 = *reinterpret_cast<const float4 *>(hf + b * H + c);
                     const float4 h1 = *reinterpret_cast<const float4 *>(hf + b * H + c + 4);
-                    acc[b] += w[0].x * h0.x + w[0].y * h0.y + w[1].x * h0.z + w[1].y * h0.w + w[2].x * h1.x +
-                              w[2].y * h1.y + w[3].x * h1.z + w[3].y * h1.w;
+                    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc0[b] = fmaf(w0[e], hv[e], acc0[b]);
+                        acc1[b] = fmaf(w1[e], hv[e], acc1[b]);
+                    }
                 }
             }
         }
-        const float t = warp_sum8(acc, lane);
+        const float t0 = warp_sum8(acc0, lane), t1 = warp_sum8(acc1, lane);
         const int b = lane >> 2;
         if ((lane & 3) == 0 && b < B) {
-            p.logits[(size_t)b * p.V + vr] = t;
-            if (!isfinite(t)) bad = true;
-            const unsigned long long k = argmax_key(t, vr);
+            p.logits[(size_t)b * p.V + v0] = t0;
+            if (!isfinite(t0)) bad = true;
+            unsigned long long k = argmax_key(t0, v0);
             kbest = k > kbest ? k : kbest;
+            if (v1 != v0) {
+                p.logits[(size_t)b * p.V + v1] = t1;
+                if (!isfinite(t1)) bad = true;
+                k = argmax_key(t1, v1);
+                kbest = k > kbest ? k : kbest;
+            }
         }
     }
     if ((lane & 3) == 0 && (lane >> 2) < kBatchMax) best[warp][lane >> 2] = kbest;
