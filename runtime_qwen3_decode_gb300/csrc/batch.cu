@@ -366,34 +366,38 @@ __global__ void __launch_bounds__(kBatchHeadThreads) batch_head_kernel(BatchHead
     unsigned long long kbest = 0;  // for value lane / 4 (a sequence)
     bool bad = false;
     const int gw = blockIdx.x * (kBatchHeadThreads / 32) + warp, nw = gridDim.x * (kBatchHeadThreads / 32);
-    // two rows per pass (vr and vr + nw): every normalised value read from shared memory
-    // serves both, and all loads of both rows are issued before the arithmetic
-    for (int v0 = gw; v0 < p.V; v0 += 2 * nw) {
-        const int v1 = v0 + nw < p.V ? v0 + nw : v0;
-        const uint4 *row0 = reinterpret_cast<const uint4 *>(p.E + (size_t)v0 * H);
-        const uint4 *row1 = reinterpret_cast<const uint4 *>(p.E + (size_t)v1 * H);
-        uint4 u0[NC], u1[NC];
+    // four rows per pass (v0 + j nw): every normalised value read from shared memory serves
+    // all four (the pass is bound by those reads, not by the rows' HBM bytes), and all loads
+    // of the four rows are issued before the arithmetic
+    constexpr int R = 4;
+    for (int v0 = gw; v0 < p.V; v0 += R * nw) {
+        int vr[R];
 #pragma unroll
-        for (int i = 0; i < NC; ++i) {
-            u0[i] = __ldg(row0 + lane + 32 * i);
-            u1[i] = __ldg(row1 + lane + 32 * i);
+        for (int j = 0; j < R; ++j) vr[j] = v0 + j * nw < p.V ? v0 + j * nw : v0;
+        uint4 u[R][NC];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(p.E + (size_t)vr[j] * H);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) u[j][i] = __ldg(row + lane + 32 * i);
         }
-        float acc0[8], acc1[8];
+        float acc[R][8];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc0[b] = acc1[b] = 0.f;
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[j][b] = 0.f;
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
             const int c = 8 * (lane + 32 * i);
-            float w0[8], w1[8];
+            float w[R][8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&u0[i])[e]);
-                const float2 bq = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&u1[i])[e]);
-                w0[2 * e] = a.x;
-                w0[2 * e + 1] = a.y;
-                w1[2 * e] = bq.x;
-                w1[2 * e + 1] = bq.y;
-            }
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 t = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&u[j][i])[e]);
+                    w[j][2 * e] = t.x;
+                    w[j][2 * e + 1] = t.y;
+                }
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 if (b < B) {
@@ -401,24 +405,21 @@ __global__ void __launch_bounds__(kBatchHeadThreads) batch_head_kernel(BatchHead
                     const float4 h1 = *reinterpret_cast<const float4 *>(hf + b * H + c + 4);
                     const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc0[b] = fmaf(w0[e], hv[e], acc0[b]);
-                        acc1[b] = fmaf(w1[e], hv[e], acc1[b]);
-                    }
+                    for (int j = 0; j < R; ++j)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[j][b] = fmaf(w[j][e], hv[e], acc[j][b]);
                 }
             }
         }
-        const float t0 = warp_sum8(acc0, lane), t1 = warp_sum8(acc1, lane);
         const int b = lane >> 2;
-        if ((lane & 3) == 0 && b < B) {
-            p.logits[(size_t)b * p.V + v0] = t0;
-            if (!isfinite(t0)) bad = true;
-            unsigned long long k = argmax_key(t0, v0);
-            kbest = k > kbest ? k : kbest;
-            if (v1 != v0) {
-                p.logits[(size_t)b * p.V + v1] = t1;
-                if (!isfinite(t1)) bad = true;
-                k = argmax_key(t1, v1);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const float t = warp_sum8(acc[j], lane);
+            const bool dup = j > 0 && vr[j] == v0;  // past the end: row v0 again, already taken
+            if ((lane & 3) == 0 && b < B && !dup) {
+                p.logits[(size_t)b * p.V + vr[j]] = t;
+                if (!isfinite(t)) bad = true;
+                const unsigned long long k = argmax_key(t, vr[j]);
                 kbest = k > kbest ? k : kbest;
             }
         }
