@@ -245,12 +245,28 @@ __global__ void __launch_bounds__(kAttnWarps * 32) batch_attn_kernel(BatchAttn p
         m[g] = -INFINITY;
         l[g] = 0.f;
     }
+    // the next position's K and V rows load while this one's are used
+    float kn[4], vn[4];
+    if (p0 + warp < p1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            kn[i] = to_f(K[(size_t)(p0 + warp) * kHeadDim + lane + 32 * i]);
+            vn[i] = to_f(Vp[(size_t)(p0 + warp) * kHeadDim + lane + 32 * i]);
+        }
+    }
     for (int j = p0 + warp; j < p1; j += kAttnWarps) {
         float k[4], v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            k[i] = to_f(K[(size_t)j * kHeadDim + lane + 32 * i]);
-            v[i] = to_f(Vp[(size_t)j * kHeadDim + lane + 32 * i]);
+            k[i] = kn[i];
+            v[i] = vn[i];
+        }
+        if (j + kAttnWarps < p1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                kn[i] = to_f(K[(size_t)(j + kAttnWarps) * kHeadDim + lane + 32 * i]);
+                vn[i] = to_f(Vp[(size_t)(j + kAttnWarps) * kHeadDim + lane + 32 * i]);
+            }
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {

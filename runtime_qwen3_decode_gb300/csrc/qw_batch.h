@@ -11,7 +11,7 @@ constexpr int kBatchMax = 8;            // sequences per batched step
 constexpr int kBatchG = 2;              // query heads per KV head (the Qwen3-0.6B block)
 constexpr int kBatchPartStride = 132;   // floats per attention partial: acc[128], max, sum, pad
 constexpr int kBatchHeadThreads = 256;
-constexpr int kBatchSplitRows = 128;    // cached positions per attention split (at most)
+constexpr int kBatchSplitRows = 32;     // cached positions per attention split (at most, up to 64 splits)
 constexpr int kBatchMaxSplits = 64;
 
 // Skinny projection of the B rows: y[b][r] = sum_k W[r][k] a[b][k] (bgemv_kernel).
@@ -78,10 +78,14 @@ cudaError_t launch_batch_merge(const float *part, int S, int Hq, int B, __half *
                                bool chained);
 cudaError_t launch_batch_head(const BatchHead &p, int H, int nsm, cudaStream_t st, bool chained);
 
-// Splits per (sequence, KV head) for a step whose longest sequence caches n positions.
+// Splits per (sequence, KV head) for a step whose longest sequence caches n positions: at
+// most kBatchSplitRows positions per split, the count rounded up to a power of two so that
+// the step's captured graph (one per split count) changes only when n doubles.
 inline int batch_splits(int n) {
-    int s = (n + kBatchSplitRows - 1) / kBatchSplitRows;
-    return s < 1 ? 1 : s > kBatchMaxSplits ? kBatchMaxSplits : s;
+    const int need = (n + kBatchSplitRows - 1) / kBatchSplitRows;
+    int s = 1;
+    while (s < need && s < kBatchMaxSplits) s *= 2;
+    return s;
 }
 
 }  // namespace qw
