@@ -71,6 +71,12 @@ def test_tiny_batch_matches_independent_sequences(qw, B):
     print(B, run_batch(qw, qi.WORKLOADS["tiny"], B, 5, 6))
 
 
+def test_tiny_batch_long_sequences_many_splits(qw):
+    # prompts of 118..124 tokens + 12 steps: the attention runs 4 splits of at most 32
+    # positions, then 8 once the longest sequence passes 128 (a second captured graph)
+    print(run_batch(qw, qi.WORKLOADS["tiny"], 3, 118, 12))
+
+
 def test_tiny_batch_int8_weights(qw):
     print(run_batch(qw, qi.WORKLOADS["tiny"].with_(weight_format="int8_g32"), 3, 4, 4))
 
