@@ -98,9 +98,45 @@ __global__ void __launch_bounds__(kGemvWarps * 32) bgemv_kernel(const BatchGemv 
     tc::chain_wait();
     tc::chain_release();
     const int B = p.B;
-    for (int i = threadIdx.x; i < B * K8; i += kGemvWarps * 32) sa[i] = reinterpret_cast<const uint4 *>(p.a)[i];
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, grp = warp / KS, kq = warp % KS;
+    if (p.a) {
+        for (int i = threadIdx.x; i < B * K8; i += kGemvWarps * 32) sa[i] = reinterpret_cast<const uint4 *>(p.a)[i];
+    } else {
+        // RMSNorm of the residual rows while staging them, in the norm_rows kernel's order:
+        // lane l's chunks l + 32 c summed in place, then the warp butterfly
+        for (int b = warp; b < B; b += kGemvWarps) {
+            const float4 *xr = reinterpret_cast<const float4 *>(p.x + (size_t)b * K8 * 8);
+            float v[KC][8];
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+                const float4 a0 = xr[2 * (lane + 32 * c)], a1 = xr[2 * (lane + 32 * c) + 1];
+                v[c][0] = a0.x, v[c][1] = a0.y, v[c][2] = a0.z, v[c][3] = a0.w;
+                v[c][4] = a1.x, v[c][5] = a1.y, v[c][6] = a1.z, v[c][7] = a1.w;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < KC; ++c)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss += v[c][i] * v[c][i];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = rsqrtf(ss / (float)(K8 * 8) + p.eps);
+            const uint4 *wr = reinterpret_cast<const uint4 *>(p.norm_w);
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+                const uint4 u = wr[lane + 32 * c];
+                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+                __half2 hv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(b2[i]);
+                    hv[i] = __floats2half2_rn(f.x * (v[c][2 * i] * r), f.y * (v[c][2 * i + 1] * r));
+                }
+                sa[b * K8 + lane + 32 * c] = *reinterpret_cast<const uint4 *>(hv);
+            }
+        }
+    }
+    __syncthreads();
     const int units = EPI == BG_SWIGLU ? p.N : p.N / 2;
     for (int base = NG * blockIdx.x; base < units; base += NG * gridDim.x) {  // uniform over the CTA
         const int u = base + grp;

@@ -1575,7 +1575,10 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         BatchGemv g{};
         g.B = B;
         g.W = wqkv;
-        g.a = h;
+        g.a = nullptr;  // RMSNorm(x) with the layer's input norm, fused into the staging
+        g.x = x;
+        g.norm_w = hl[l].input_norm;
+        g.eps = a.eps;
         g.N = QD + 2 * KD;
         g.K = H;
         g.out = qkv_raw;
@@ -1620,11 +1623,10 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
         g.out = x;
         g.ldo = H;
         if (launch_bgemv(BG_ADD, g, st->nsm, stream, true) != cudaSuccess) return 1;
-        if (launch_norm_rows(x, nullptr, nullptr, hl[l].post_norm, h, B, H, a.eps, stream, true) != cudaSuccess)
-            return 1;
-        // a = silu(h Wg^T) * (h Wu^T)
+        // a = silu(h Wg^T) * (h Wu^T), h = RMSNorm(x) with the post-attention norm (fused)
         g.W = wgu;
-        g.a = h;
+        g.a = nullptr;
+        g.norm_w = hl[l].post_norm;
         g.N = I;
         g.K = H;
         g.act = act;
@@ -1643,12 +1645,6 @@ int prefill_batch_step(PrefillState *st, const DecodeArgs &a, const BatchStep &b
             cudaMemcpyAsync(bs.hidden + (size_t)(l + 1) * B * H, x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
                             stream);
             ch = false;
-        }
-        if (l + 1 < c.n_layers) {
-            if (launch_norm_rows(x, nullptr, nullptr, hl[l + 1].input_norm, h, B, H, a.eps, stream, ch) !=
-                cudaSuccess)
-                return 1;
-            ch = true;
         }
     }
     BatchHead hp{};

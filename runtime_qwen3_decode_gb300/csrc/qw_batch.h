@@ -19,7 +19,10 @@ enum { BG_STORE = 0, BG_ADD = 1, BG_SWIGLU = 2 };
 
 struct BatchGemv {
     const __half *W;       // [rows][K] fp16; BG_SWIGLU: gate/up rows interleaved in 128-row blocks
-    const __half *a;       // [B][K] fp16 activation rows
+    const __half *a;       // [B][K] fp16 activation rows, or null: RMSNorm of x below
+    const float *x;        // with a == null: [B][K] f32 residual rows, staged as fp16(w (x r))
+    const __nv_bfloat16 *norm_w;  //   r = rsqrt(mean(x^2) + eps), the norm_rows kernel's arithmetic
+    float eps;
     int B, N, K;           // N outputs (BG_STORE / BG_ADD: even); K in {1024, 2048, 3072, 4096, 6144}
     float *out;            // BG_STORE: out[b][n] = y; BG_ADD: out[b][n] += y
     int ldo;
