@@ -21,13 +21,19 @@
 // up rows are interleaved in blocks of 128 so that one 256-wide output tile holds a
 // gate block and its matching up block and the SwiGLU product happens in the epilogue.
 //
-// GEMM kernel: persistent, one CTA per SM, warp-specialised: warp 0 issues TMA tile
-// loads into a ring of shared-memory stages, warp 1 owns the TMEM allocation and
-// issues tcgen05.mma from one thread, warps 2-5 drain the double-buffered TMEM
-// accumulator (tcgen05.ld) and apply the epilogue while the next tile accumulates.
-// Every wait is bounded: on expiry the CTA records QW_INTERNAL_INVARIANT, raises a
-// shared abort flag, waits (bounded) for its own copies and MMAs in flight, frees
-// TMEM and returns.
+// GEMM kernel: persistent, one CTA per SM, warp-specialised: 2 or 3 producer warps take
+// turns issuing the TMA tile loads of a ring of shared-memory stages, one warp owns the
+// TMEM allocation and issues tcgen05.mma from one thread, and 4 (q|k|v: 8) epilogue
+// warps drain the double-buffered TMEM accumulator (tcgen05.ld) and apply the epilogue
+// while the next tile accumulates.  Every wait is bounded: on expiry the CTA records
+// QW_INTERNAL_INVARIANT, raises a shared abort flag, waits (bounded) for its own copies
+// and MMAs in flight, frees TMEM and returns.
+//
+// Every kernel of a chunk after its first is launched chained (programmatic dependent
+// launch): it waits with griddepcontrol.wait before touching memory an earlier kernel
+// used, so its launch and setup overlap the previous kernel's tail.  The batched decode
+// step (prefill_batch_step) reuses the fp16 weight copy and the row kernel here, with the
+// skinny projections of batch.cu.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
