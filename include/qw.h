@@ -223,7 +223,9 @@ void qw_model_destroy(qw_model *m);
  * per-sequence split attention over each cache, and one pass of the tied lm_head for
  * all rows; the cache uses the model's format.  Requires the batched prefill
  * (qw_prefill's tensor-core path, which holds that weight copy) to be available and
- * query heads = 2 x KV heads; max_ctx <= the model's max_ctx.
+ * query heads = 2 x KV heads, hidden, query heads x head_dim and intermediate each one
+ * of 1024, 2048, 3072, 4096, 6144 (else QW_UNSUPPORTED_SHAPE); max_ctx <= the model's
+ * max_ctx.
  *
  * Workspace: caller-owned device memory of qw_batch_workspace_bytes (256-byte aligned),
  * holding every sequence's cache ([n_layers][n_kv_heads][max_ctx][head_dim] K and V

@@ -547,7 +547,8 @@ cudaError_t launch_bgemv_k(const BatchGemv &p, int nsm, cudaStream_t st, bool ch
 }
 
 cudaError_t launch_bgemv(int epi, const BatchGemv &p, int nsm, cudaStream_t st, bool chained) {
-    if (p.B < 1 || p.B > kBatchMax || p.N < 1 || (epi != BG_SWIGLU && (p.N & 1))) return cudaErrorInvalidValue;
+    if (p.B < 1 || p.B > kBatchMax || p.N < 1 || (epi != BG_SWIGLU && (p.N & 1)) || !bgemv_supported(p.K))
+        return cudaErrorInvalidValue;
     return epi == BG_STORE ? launch_bgemv_k<BG_STORE>(p, nsm, st, chained)
            : epi == BG_ADD ? launch_bgemv_k<BG_ADD>(p, nsm, st, chained)
                            : launch_bgemv_k<BG_SWIGLU>(p, nsm, st, chained);

@@ -774,6 +774,9 @@ int qw_batch_create(qw_model *m, int32_t max_batch, int32_t max_ctx, void *works
         return QW_INVALID_ARGUMENT;
     if (!qw::prefill_supported(m->pf) || max_batch > m->pf.rows_max || m->cfg.n_heads != qw::kBatchG * m->cfg.n_kv_heads)
         return QW_UNSUPPORTED_SHAPE;
+    const int qd = m->cfg.n_heads * m->cfg.head_dim;  // the skinny projections' row lengths: H, Hq 128, I
+    if (!qw::bgemv_supported(m->cfg.hidden) || !qw::bgemv_supported(qd) || !qw::bgemv_supported(m->cfg.intermediate))
+        return QW_UNSUPPORTED_SHAPE;
     if (!aligned(workspace_dev, 256)) return QW_ALIGNMENT;
     BatchLayout L;
     batch_layout(m->cfg, max_batch, max_ctx, &L);

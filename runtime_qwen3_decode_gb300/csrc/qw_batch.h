@@ -73,6 +73,8 @@ cudaError_t batch_prepare();
 // stream must be a kernel); every batched kernel waits for its predecessor's completion
 // before its first memory access.
 cudaError_t launch_bgemv(int epi, const BatchGemv &p, int nsm, cudaStream_t st, bool chained);
+// Row lengths the skinny projection is built for (launch_bgemv refuses the others).
+inline bool bgemv_supported(int K) { return K == 1024 || K == 2048 || K == 3072 || K == 4096 || K == 6144; }
 cudaError_t launch_bqkv_post(const BatchQkvPost &p, int kv_f32, cudaStream_t st, bool chained);
 cudaError_t launch_batch_tokens(const int32_t *in, const int32_t *picks, int B, int32_t *tokens, cudaStream_t st,
                                 bool chained);
